@@ -1,0 +1,13 @@
+"""CPU float64 oracle of the latent-MoE block (test infrastructure only).
+
+Only `tests/`, the package smoke check and the benchmark's CPU-baseline leg may
+import this package; the library never does.
+"""
+from .moe_oracle import (moe_forward, route, rmsnorm, router_logits, topk_route,
+                         route_margin, expert_swiglu, expert_down, silu,
+                         storage_kinds)
+from . import formats
+
+__all__ = ["moe_forward", "route", "rmsnorm", "router_logits", "topk_route",
+           "route_margin", "expert_swiglu", "expert_down", "silu", "storage_kinds",
+           "formats"]

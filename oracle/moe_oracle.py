@@ -1,0 +1,242 @@
+"""CPU oracle of the latent mixture-of-experts block, in float64.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, the package smoke check and the
+benchmark's CPU-baseline leg may import this module.  The library never does, and
+this module imports nothing from the library.
+
+What it computes is the plain definition of the block, taken from "SGLang and Miles
+Add Day-0 Support for Muse Spark Open", section "MoE with Pooler, Unpooler and
+Per-Expert Normalization", with the widths of "Muse Spark Open Day-0 on vLLM",
+section "潜空间 MoE", and the router precision of the same page's "Nvidia" section:
+
+    h_t   = RMSNorm_{g_in}(x_t)                       full-width norm
+    l_t   = W_r h_t                                   router logits (TF32 operands)
+    (e_t, w_t) = top-k of softmax(l_t), renormalised   k experts, weights sum to 1
+    u_t   = RMSNorm_{g_pool}(W_pool h_t)              pooler 8192->4096, then the
+                                                      pooled-input norm
+    y_tj  = W_down_e (silu(W_gate_e u_t) * W_up_e u_t) routed SwiGLU expert e = e_tj
+    c_t   = sum_j w_tj * RMSNorm_{g_exp[e_tj]}(y_tj)   per-expert norm BEFORE the
+                                                      weighting, sum in order j
+    out_t = W_unpool c_t                              unpooler 4096->8192
+
+with RMSNorm_g(v) = v / sqrt(mean(v^2) + eps) * g and silu(a) = a * sigmoid(a).
+
+Dispatching tokens to experts and running grouped GEMMs reaches exactly this
+per-token result (up to rounding order), so the oracle computes it token by
+token with dense float64 products (numpy matmul as the only library step) and
+no blocking, fusion or reordering.
+
+Two modes:
+* chain=False ("exact"): float64 throughout.  Router operands are still rounded
+  to TF32 (ties away), because the page fixes a TF32 router GEMM fed by the
+  norm's FP32 output, and the routing decision must be taken in the precision
+  the kernel uses.
+* chain=True ("precision chain", the parity gate): float64 arithmetic, with every
+  value rounded where the GPU path stores it (see `_store`): h (FP32 for the
+  router, BF16 or TF32 for the pooler), pooled (FP32), u, s, y, c (BF16, or
+  TF32/FP32 in FP32 mode) and out.  The page fixes the FP32 route-weighted sum
+  and the BF16 values the per-expert norm is taken on; the other storage types
+  are the kernel's.
+
+Readings of points the pages leave open (each is also listed with the design
+notes): softmax over all E logits, top-k, renormalised (= softmax over the k
+chosen logits); slots ordered by logit, ties to the lower expert id; no biases;
+every norm has a learned gain; per-expert gains are [E, p]; eps inside the
+square root.
+
+NVFP4 experts (block-scaled FP4, "NVFP4 as a third MMA kind") are emulated in
+`nvfp4.py`.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import formats as F
+
+
+# ---- storage rounding --------------------------------------------------------------
+
+def _store(v: np.ndarray, kind: str) -> np.ndarray:
+    """Round float64 values to the storage format `kind` of the GPU path."""
+    if kind == "f64":
+        return v
+    if kind == "f32":
+        return F.fp32(v)
+    if kind == "bf16":
+        return F.bf16(v)
+    if kind == "tf32":          # FP32 storage, pre-rounded for a TF32 MMA operand
+        return F.tf32_rna(F.fp32(v))
+    raise ValueError(kind)
+
+
+def as_f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# ---- the steps ---------------------------------------------------------------------
+
+def rmsnorm(v: np.ndarray, g, eps: float) -> np.ndarray:
+    """Row-wise RMSNorm with gain: v / sqrt(mean(v^2) + eps) * g."""
+    v = as_f64(v)
+    ms = np.mean(v * v, axis=-1, keepdims=True)
+    return v / np.sqrt(ms + eps) * as_f64(g)
+
+
+def router_logits(h: np.ndarray, w_router) -> np.ndarray:
+    """logits[t, e] = sum_i tf32(h[t, i]) * tf32(W_r[e, i]).
+
+    The Nvidia section of the vLLM page: the router GEMM is TF32, fed by the
+    norm's FP32 output.  h is first stored as FP32, then both operands are
+    rounded to TF32; products and the sum are float64.
+    """
+    a = F.tf32_rna(F.fp32(h))
+    b = F.tf32_rna(as_f64(w_router))
+    return a @ b.T
+
+
+def topk_route(logits: np.ndarray, k: int):
+    """Top-k experts per row and their renormalised softmax weights.
+
+    Slots are ordered by logit, largest first; equal logits go to the lower id.
+    softmax over all E followed by renormalisation over the chosen k equals the
+    softmax over the chosen logits, which is what is computed here.
+    """
+    logits = as_f64(logits)
+    order = np.argsort(-logits, axis=-1, kind="stable")
+    ids = order[:, :k]
+    chosen = np.take_along_axis(logits, ids, axis=-1)
+    z = np.exp(chosen - chosen[:, :1])
+    w = z / np.sum(z, axis=-1, keepdims=True)
+    return ids.astype(np.int32), w
+
+
+def route_margin(logits: np.ndarray, k: int) -> np.ndarray:
+    """Smallest gap between consecutive sorted logits among the top min(k+1, E).
+
+    A row whose margin exceeds the routing noise has a unique top-k set and a
+    unique slot order.
+    """
+    s = -np.sort(-as_f64(logits), axis=-1)
+    m = min(k + 1, s.shape[-1])
+    if m < 2:
+        return np.full(s.shape[0], np.inf)
+    return np.min(s[:, : m - 1] - s[:, 1:m], axis=-1)
+
+
+def silu(a: np.ndarray) -> np.ndarray:
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_swiglu(u: np.ndarray, w_gate_e, w_up_e) -> np.ndarray:
+    """s = silu(W_gate u) * W_up u for rows u [n, p]; W_gate, W_up are [I, p]."""
+    a = u @ as_f64(w_gate_e).T
+    b = u @ as_f64(w_up_e).T
+    return silu(a) * b
+
+
+def expert_down(s: np.ndarray, w_down_e) -> np.ndarray:
+    """y = W_down s for rows s [n, I]; W_down is [p, I]."""
+    return s @ as_f64(w_down_e).T
+
+
+# ---- the layer ---------------------------------------------------------------------
+
+def storage_kinds(act: str, expert: str, out: str, chain: bool) -> dict:
+    """Where the GPU path stores each intermediate, as `_store` kinds."""
+    if not chain:
+        return dict(h_pool="f64", pooled="f64", u="f64", s="f64", y="f64", c="f64",
+                    out="f64", w_proj="f64", w_exp="f64")
+    tc = act == "f32"            # FP32 activations run their GEMMs on TF32 operands
+    te = expert == "f32"
+    return dict(
+        h_pool="tf32" if tc else "bf16",
+        pooled="f32",
+        u="tf32" if te else "bf16",
+        s="tf32" if te else "bf16",
+        y="f32" if te else "bf16",
+        c="tf32" if tc else "bf16",
+        out=out,
+        w_proj="tf32" if tc else "f64",      # BF16 weights are exact as given
+        w_exp="tf32" if te else "f64",
+    )
+
+
+def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
+                expert: str = "bf16", out: str = "f32", chain: bool = True,
+                tokens=None, ids=None, weights=None, norm_after_sum: bool = False,
+                return_parts: bool = False):
+    """The latent-MoE block for the rows `tokens` of inp["x"] (all rows if None).
+
+    inp holds x [T,d], g_in [d], w_router [E,d], w_pool [p,d], g_pool [p],
+    w_gate/w_up [E,I,p], w_down [E,p,I], g_exp [E,p], w_unpool [d,p]; expert
+    tensors only need to support w[e] (one expert at a time is converted).
+    `ids`/`weights` ([n,k]) replace the router when given (routing replay).
+    `norm_after_sum=True` computes the variant that normalises the combined vector
+    instead of each expert output, which the page rules out; it exists so tests
+    can show the two orders differ.
+    Returns out [n, d] (float64 holding values of the output storage type), or a
+    dict of every intermediate with return_parts.
+    """
+    st = storage_kinds(act, expert, out, chain)
+    x = as_f64(inp["x"])
+    if tokens is not None:
+        x = x[np.asarray(tokens)]
+    n = x.shape[0]
+
+    h = rmsnorm(x, inp["g_in"], eps)
+    if ids is None:
+        logits = router_logits(h, inp["w_router"])
+        ids, wts = topk_route(logits, top_k)
+    else:
+        logits = None
+        ids = np.asarray(ids, dtype=np.int32)
+        wts = as_f64(weights)
+        top_k = ids.shape[1]
+
+    h_pool = _store(F.fp32(h) if chain else h, st["h_pool"])
+    w_pool = _store(as_f64(inp["w_pool"]), st["w_proj"])
+    pooled = _store(h_pool @ w_pool.T, st["pooled"])
+    u = _store(rmsnorm(pooled, inp["g_pool"], eps), st["u"])
+
+    p = u.shape[1]
+    g_exp = as_f64(inp["g_exp"])
+    y_all = np.zeros((n, top_k, p))
+    s_all = None
+    for e in np.unique(ids):
+        rows, slots = np.nonzero(ids == e)
+        wg = _store(as_f64(inp["w_gate"][e]), st["w_exp"])
+        wu = _store(as_f64(inp["w_up"][e]), st["w_exp"])
+        wd = _store(as_f64(inp["w_down"][e]), st["w_exp"])
+        s = _store(expert_swiglu(u[rows], wg, wu), st["s"])
+        if return_parts:
+            if s_all is None:
+                s_all = np.zeros((n, top_k, s.shape[1]))
+            s_all[rows, slots] = s
+        y_all[rows, slots] = _store(expert_down(s, wd), st["y"])
+
+    c = np.zeros((n, p))
+    if not norm_after_sum:
+        for j in range(top_k):     # the route-weighted sum, in slot order
+            yn = rmsnorm(y_all[:, j], g_exp[ids[:, j]], eps)
+            c = c + wts[:, j: j + 1] * yn
+    else:
+        for j in range(top_k):
+            c = c + wts[:, j: j + 1] * y_all[:, j]
+        c = rmsnorm(c, np.ones(p), eps)
+    c = _store(c, st["c"])
+    w_unpool = _store(as_f64(inp["w_unpool"]), st["w_proj"])
+    res = _store(c @ w_unpool.T, st["out"])
+    if not return_parts:
+        return res
+    return dict(out=res, h=h, logits=logits, ids=ids, w=wts, pooled=pooled, u=u,
+                s=s_all, y=y_all, c=c)
+
+
+def route(inp: dict, *, top_k: int, eps: float, tokens=None):
+    """Router only: (ids [n,k] int32, weights [n,k] float64, logits [n,E])."""
+    x = as_f64(inp["x"])
+    if tokens is not None:
+        x = x[np.asarray(tokens)]
+    logits = router_logits(rmsnorm(x, inp["g_in"], eps), inp["w_router"])
+    ids, w = topk_route(logits, top_k)
+    return ids, w, logits
