@@ -1,0 +1,460 @@
+"""Throughput of one latent-MoE layer (the prefill chunk: T=16384, d=8192, p=4096,
+E=256, top-k 8, I=4096, BF16) through the C ABI on GB300s.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload prefill_bf16|decode_bf16|skewed_bf16|tiny_f32]
+
+A step is one moe_forward over one batch of T synthetic tokens (all eight stages:
+norm, router + top-k, pooler, dispatch, gate/up + SwiGLU, down, combine, unpooler).
+Inputs are resident in HBM when the timed region starts; the 24 GB of expert weights
+and the 256 MB activation batch are larger than L2, so no flush is needed between
+steps.  Under torchrun each rank runs its own batch (weak scaling, no collective on
+the data path); the elapsed time is the max over ranks.
+
+Prints one JSON line (rank 0).  `--impl reference` times the float64 CPU oracle on
+the host cores on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "latent-MoE layer tokens/s on 1 GB300; % of BF16/FP4 tensor peak and HBM BW"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="prefill_bf16")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---- algorithmic work --------------------------------------------------------------------
+
+def flops_per_token(s) -> dict:
+    """FLOPs per token of each GEMM stage (multiply-add = 2), routed work only."""
+    return {
+        "router": 2.0 * s.d * s.E,
+        "pool": 2.0 * s.d * s.p,
+        "gemm1_gate_up_swiglu": 2.0 * s.top_k * s.p * 2 * s.I,
+        "gemm2_down": 2.0 * s.top_k * s.I * s.p,
+        "unpool": 2.0 * s.p * s.d,
+    }
+
+
+def bytes_per_token(s, act_bytes=2) -> dict:
+    """Compulsory HBM bytes per token of the memory-bound stages (each operand read
+    once, each result written once)."""
+    k = s.top_k
+    return {
+        "norm": s.d * act_bytes + s.d * 4 + s.d * act_bytes,            # x in; h32, h16 out
+        "dispatch": s.p * 4 + k * s.p * act_bytes + 16 * k,             # pooled in; k rows out
+        "combine": k * s.p * act_bytes + s.p * act_bytes + 8 * k,       # k rows in; c out
+    }
+
+
+# ---- clocks --------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---- ncu traffic record ----------------------------------------------------------------
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "latent_moe_layer_rmsnorm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the summary
+    is missing or was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    if not m or not sha or sha.group(1) != kernel_source_sha():
+        return None
+    return float(m.group(1))
+
+
+# ---- our arm -----------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from latent_moe_layer_rmsnorm_gb300 import build, synth
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    shape = synth.WORKLOADS[args.workload]
+    if shape.expert == "nvfp4":
+        raise SystemExit("the NVFP4 workload is not available in this build")
+    seed = args.seed + 1000 * rank             # each rank: its own batch
+    inp = synth.make_inputs(shape, seed=seed, device="cuda")
+    out_kind = "bf16" if shape.act == "bf16" else "f32"
+    layer = LatentMoE(shape, inp, out=out_kind, keep_canonical=False)
+    del inp["w_gate"], inp["w_up"]
+    x = inp["x"]
+    T = shape.T
+    out = torch.empty((T, shape.d), dtype=layer.out_dtype(), device="cuda")
+    stream = torch.cuda.current_stream()
+    from latent_moe_layer_rmsnorm_gb300 import _lib as nst
+    n_stages = nst.moe_num_stages()
+    stage_names = [nst.moe_stage_name(i) for i in range(n_stages)]
+
+    def make_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record(stream)           # create the handles; re-recorded by the library
+        return evs
+
+    for _ in range(args.warmup):
+        layer.forward(x, out=out)
+    torch.cuda.synchronize()
+    st = layer.read_status()
+    if st != (0, 0):
+        raise SystemExit(f"device status after warm-up: {st}")
+
+    # timed region: K steps, stage events recorded between the kernels
+    step_events = [make_events(n_stages + 1) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        layer.forward(x, out=out, events=[e.cuda_event for e in step_events[k]])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    st = layer.read_status()
+    if st != (0, 0):
+        raise SystemExit(f"device status after the timed steps: {st}")
+
+    stage_ms = {n: 0.0 for n in stage_names}
+    for evs in step_events:
+        for i, n in enumerate(stage_names):
+            stage_ms[n] += evs[i].elapsed_time(evs[i + 1]) / args.steps
+
+    ms_per_step = elapsed_ms / args.steps
+    tokens = T * args.steps * world
+    value = tokens / (elapsed_ms / 1e3)
+
+    # ---- end to end from pinned host buffers ------------------------------------------
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        hx.copy_(x)
+        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        dx = torch.empty_like(x)
+        for _ in range(2):
+            dx.copy_(hx, non_blocking=True)
+            layer.forward(dx, out=out)
+            ho.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(3, args.steps // 2)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            dx.copy_(hx, non_blocking=True)
+            layer.forward(dx, out=out)
+            ho.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": T * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": x.numel() * x.element_size(),
+               "d2h_bytes_per_step": out.numel() * out.element_size(),
+               "ms_per_step": e2e_ms / n_e2e}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel -------------------------------------------------
+    peaks, peak_src = load_peaks()
+    fl = flops_per_token(shape)
+    by = bytes_per_token(shape)
+    stage_tflops = {n: fl[n] * T / (stage_ms[n] / 1e3) / 1e12 for n in fl if stage_ms.get(n)}
+    stage_gbs = {n: by[n] * T / (stage_ms[n] / 1e3) / 1e9 for n in by if stage_ms.get(n)}
+    dominant = max(fl, key=lambda n: stage_ms.get(n, 0.0))
+    achieved = stage_tflops[dominant]
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = recorded_traffic(args.workload, dominant)
+    roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "peak_kind": f"bf16_tflops_sustained ({peak_src}); the kernel runs inside "
+                             f"a {ms_per_step:.1f} ms step, back to back",
+                "flops_per_launch": fl[dominant] * T,
+                "peak_burst": float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline_from_gpu_inputs(shape, layer, x, seed)
+
+    launches = layer.launches(T) * args.steps
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights, U(0.5,1.5) gains)",
+        "config": {"workload": f"{shape.name}: T={T} d={shape.d} p={shape.p} E={shape.E} "
+                               f"top_k={shape.top_k} I={shape.I} act={shape.act} "
+                               f"expert={shape.expert} out={out_kind}",
+                   "global_batch": T * world, "parallelism": f"replicas x{world} (token batches)",
+                   "l2": "inputs larger than L2 (24 GB expert weights, 256 MB x per step)"},
+        "roofline": roofline,
+        "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "stages_tflops": {k: round(v, 1) for k, v in stage_tflops.items()},
+        "stages_gbs": {k: round(v, 1) for k, v in stage_gbs.items()},
+        "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---- CPU oracle baselines ------------------------------------------------------------------
+
+def _oracle_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline_from_gpu_inputs(shape, layer, x, seed, n_tokens=4):
+    """Time the oracle, as it stands, on n_tokens of the benchmark's own batch.  The
+    inputs (dense weights and the routed experts' matrices) are staged on the host
+    before the clock starts; the oracle's float64 conversion is timed."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from latent_moe_layer_rmsnorm_gb300 import synth
+
+    toks = list(range(0, shape.T, shape.T // n_tokens))[:n_tokens]
+    dense = synth.make_dense(shape, seed=seed, device="cuda")
+    view = {k: v.float().cpu().numpy() for k, v in dense.items()}
+    view["x"] = x[toks].float().cpu().numpy()
+    ids, _ = layer.route(x[toks].contiguous())
+    need = sorted(set(ids.cpu().numpy().reshape(-1).tolist()))
+    experts = {e: {k: v.float().cpu().numpy() for k, v in
+                   synth.make_expert(shape, seed, e, device="cuda").items()} for e in need}
+
+    class Sparse:
+        def __init__(self, key):
+            self.key = key
+
+        def __getitem__(self, e):
+            e = int(e)
+            if e not in experts:     # the oracle routed a token elsewhere than the GPU
+                experts[e] = {k: v.float().cpu().numpy() for k, v in
+                              synth.make_expert(shape, seed, e, device="cuda").items()}
+            return experts[e][self.key]
+
+    for key in ("w_gate", "w_up", "w_down"):
+        view[key] = Sparse(key)
+    t0 = time.perf_counter()
+    oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act=shape.act,
+                       expert=shape.expert, out="bf16", chain=True)
+    dt = time.perf_counter() - t0
+    del np
+    return {"value": round(len(toks) / dt, 4), "unit": "tokens/s", "cores": _oracle_cores(),
+            "kind": "oracle",
+            "sample": f"{len(toks)} tokens of the {shape.name} batch ({len(need)} experts), "
+                      f"float64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle on the host cores: each step is one token of the workload with its
+    routed experts (drawn on the CPU from the same generator recipe)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from latent_moe_layer_rmsnorm_gb300 import synth
+
+    shape = synth.WORKLOADS[args.workload]
+    n_tok = max(args.steps + args.warmup, 1)
+    small = shape.replace(T=n_tok)
+    # inputs are only drawn on the GPU when one is present (faster); the timed work is
+    # the oracle on the host cores either way
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    dense = synth.make_dense(small, seed=args.seed, device=gen_dev)
+    view = {k: v.float().cpu().numpy() for k, v in dense.items()}
+    ids, _, _ = oracle.route(view, top_k=shape.top_k, eps=shape.eps)
+    cache = {}
+
+    def experts_for(t):
+        out = {}
+        for e in ids[t]:
+            e = int(e)
+            if e not in cache:
+                cache[e] = {k: v.float().cpu().numpy()
+                            for k, v in synth.make_expert(shape, args.seed, e, gen_dev).items()}
+            out[e] = cache[e]
+        return out
+
+    class Sparse:
+        def __init__(self, key, ex):
+            self.key, self.ex = key, ex
+
+        def __getitem__(self, e):
+            return self.ex[int(e)][self.key]
+
+    times = []
+    for t in range(n_tok):
+        ex = experts_for(t)
+        v = dict(view)
+        for key in ("w_gate", "w_up", "w_down"):
+            v[key] = Sparse(key, ex)
+        t0 = time.perf_counter()
+        oracle.moe_forward(v, top_k=shape.top_k, eps=shape.eps, act=shape.act,
+                           expert=shape.expert, out="bf16", chain=True, tokens=[t])
+        times.append(time.perf_counter() - t0)
+        if len(cache) > 64:
+            cache.clear()
+    timed = times[args.warmup:] if len(times) > args.warmup else times
+    total = sum(timed)
+    value = len(timed) / total
+    cores = _oracle_cores()
+    sample = (f"{len(timed)} tokens of {shape.name}, one per step, float64 numpy oracle "
+              f"with its routed experts")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s",
+            "n_gpus": world, "steps": len(timed), "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total / len(timed), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{shape.name}: T={shape.T} d={shape.d} p={shape.p} "
+                                   f"E={shape.E} top_k={shape.top_k} I={shape.I}",
+                       "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    del np, torch
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * latent_moe.h -- C ABI of the latent mixture-of-experts block on one GB300 (sm_103a).
+ *
+ * The block (from "SGLang and Miles Add Day-0 Support for Muse Spark Open", section
+ * "MoE with Pooler, Unpooler and Per-Expert Normalization"; widths from "Muse Spark
+ * Open Day-0 on vLLM", section "潜空间 MoE"; router precision from the same page's
+ * "Nvidia" section):
+ *
+ *   h_t   = RMSNorm_{g_in}(x_t)                         full-width norm        [T,d]
+ *   l_t   = W_r h_t  (TF32 operands, FP32 accumulate)   router logits          [T,E]
+ *   (e_t, w_t) = top-k of softmax(l_t), renormalised     packed ids/weights     [T,k]
+ *   u_t   = RMSNorm_{g_pool}(W_pool h_t)                pooler + pooled norm   [T,p]
+ *   y_tj  = W2_e (silu(Wg_e u_t) * Wu_e u_t), e = e_tj  routed SwiGLU experts
+ *   c_t   = sum_j w_tj RMSNorm_{g_exp[e_tj]}(y_tj)      per-expert norm BEFORE the
+ *                                                       FP32 route-weighted sum
+ *   out_t = W_unpool c_t                                unpooler               [T,d]
+ *
+ * RMSNorm_g(v) = v / sqrt(mean(v^2) + eps) * g.  Slots j are ordered by logit, largest
+ * first, ties to the lower expert id; the weighted sum runs in slot order in FP32.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are row-major and dense.  Pointers named "device" must point to
+ *    device memory of the current CUDA device; the library reads or writes them only
+ *    from kernels on `stream`.  Host pointers (configs, weight tables) are read during
+ *    the call only.
+ *  - The library allocates no memory and keeps no state beyond a per-device cache of
+ *    attributes and kernel settings.  Every buffer belongs to the caller.
+ *  - Calls are asynchronous on `stream` and never synchronise or read device memory
+ *    from the host (except moe_read_status), so they can be captured in a CUDA graph.
+ *  - Errors found on the host (null pointers, unsupported sizes, a workspace that is
+ *    too small) are returned before anything is launched.  Errors found on the device
+ *    (a bounded wait that ran out) are recorded in the workspace's status word and
+ *    reported by moe_read_status; CUDA launch errors are returned as MOE_ERR_CUDA.
+ *  - Results are deterministic: identical inputs give bit-identical outputs.
+ *  - Outputs must not alias inputs.
+ */
+#ifndef LATENT_MOE_H
+#define LATENT_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA runtime's stream and event handles (same layout as cudaStream_t /
+ * cudaEvent_t), declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* moe_stream_t;
+typedef struct CUevent_st* moe_event_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, k > E, bad dtype combination          */
+  MOE_ERR_UNSUPPORTED = 2,   /* sizes outside what the kernels handle (see below)   */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small          */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed                */
+  MOE_ERR_TIMEOUT = 5,       /* device: a pipeline wait ran past its time limit     */
+  MOE_ERR_DEVICE_CHECK = 6   /* device: an index check failed                       */
+} moe_status_t;
+
+typedef enum {
+  MOE_F32 = 0,     /* float32; GEMM operands rounded to TF32 (ties away) */
+  MOE_BF16 = 1,    /* bfloat16 */
+  MOE_NVFP4 = 2    /* E2M1 codes + UE4M3 scale per 16 + FP32 tensor scale */
+} moe_dtype_t;
+
+/* Layer configuration.
+ *   T      tokens in this call (>= 0; T = 0 is a no-op)
+ *   d      model width           (multiple of 128, <= 32768)
+ *   p      pooled (expert) width (multiple of 128, <= 8192)
+ *   E      routed experts        (1..256)
+ *   top_k  experts per token     (1..8, <= E)
+ *   I      SwiGLU intermediate   (multiple of 128, <= 32768)
+ *   eps    RMSNorm epsilon (added to mean(v^2) inside the square root)
+ *   act    MOE_BF16 or MOE_F32: dtype of x, w_pool, w_unpool and the stored
+ *          activations between the GEMMs
+ *   expert MOE_BF16 or MOE_F32 (must equal act in this version)
+ *   out    MOE_BF16 or MOE_F32: dtype of the layer output
+ *   flags  0, or MOE_FLAG_TEST_TIMEOUT (other bits must be zero)                  */
+/* Test hook for the error path: the gate/up GEMM never issues its first operand load,
+ * so its MMA wait runs out after 20 ms; the call's kernels then end early and
+ * moe_read_status reports MOE_ERR_TIMEOUT.  Outputs are undefined.  Tests only. */
+#define MOE_FLAG_TEST_TIMEOUT 0x80000000u
+typedef struct {
+  int32_t T, d, p, E, top_k, I;
+  float eps;
+  int32_t act, expert, out;
+  uint32_t flags;
+} moe_config_t;
+
+/* Weights as moe_forward consumes them (all device pointers, read only):
+ *   g_in      [d]        FP32 gain of the full-width norm
+ *   w_router  [E,d]      FP32 router rows, already rounded to TF32 by moe_pack_weights
+ *   w_pool    [p,d]      pooler (act dtype; F32: TF32-rounded by moe_pack_weights)
+ *   g_pool    [p]        FP32 gain of the pooled-input norm
+ *   w13       packed gate/up rows of every expert, written by moe_pack_weights
+ *   w2        [E,p,I]    down projections (expert dtype; F32: TF32-rounded)
+ *   g_exp     [E,p]      FP32 per-expert output-norm gains
+ *   w_unpool  [d,p]      unpooler (act dtype; F32: TF32-rounded)               */
+typedef struct {
+  const float* g_in;
+  const float* w_router;
+  const void* w_pool;
+  const float* g_pool;
+  const void* w13;
+  const void* w2;
+  const float* g_exp;
+  const void* w_unpool;
+} moe_weights_t;
+
+/* Canonical (unpacked) weights, as a checkpoint stores them (device pointers):
+ *   w_router [E,d] FP32; w_pool [p,d]; w_gate, w_up [E,I,p]; w_down [E,p,I];
+ *   w_unpool [d,p] (act / expert dtype as in the config).                     */
+typedef struct {
+  const float* w_router;
+  const void* w_pool;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+  const void* w_unpool;
+} moe_canonical_weights_t;
+
+/* Bytes of device workspace moe_route / moe_forward need for this config
+ * (0 when the config is invalid).  The workspace holds the intermediates
+ * (normalised rows, pooled rows, permuted expert inputs, SwiGLU and expert outputs,
+ * the dispatch maps) and the status word.  It must be 256-byte aligned. */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Clears the workspace's status word.  Call once after allocating a workspace
+ * (before its first use); moe_read_status clears it again after each read. */
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Bytes of the packed buffers moe_pack_weights writes.  which: 0 = w_router (TF32
+ * copy), 1 = w13, 2 = w2, 3 = w_pool, 4 = w_unpool.  Returns 0 for a buffer this
+ * config does not need packed (BF16 w2 / w_pool / w_unpool are used as given). */
+size_t moe_packed_bytes(const moe_config_t* cfg, int which);
+
+/* Prepares weights for moe_forward ("SGLang and Miles Add Day-0 Support for Muse Spark
+ * Open", section "Reading TensorRT-LLM's weights", describes the same need: the expert
+ * GEMM reads gate and up rows of one tile together; this library uses its own layout).
+ *  - w_router_out [E,d] FP32: w_router rounded to TF32 (ties away), the router's
+ *    operand precision (the vLLM page's "Nvidia" section: TF32 router GEMM).
+ *  - w13_out: gate and up rows interleaved in blocks of G rows (G = 128), so one
+ *    256-row tile of the gate/up GEMM holds gate rows i..i+G and the matching up rows.
+ *  - w2_out, w_pool_out, w_unpool_out: F32 configs only, TF32-rounded copies; pass
+ *    NULL for BF16 configs (those tensors are then used as given).
+ * Output buffers are caller-allocated with moe_packed_bytes; none may alias a source. */
+moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weights_t* src,
+                              float* w_router_out, void* w13_out, void* w2_out,
+                              void* w_pool_out, void* w_unpool_out, moe_stream_t stream);
+
+/* Router only: full-width RMSNorm, TF32 router GEMM and top-k.
+ *   x    [T,d] act dtype (device)
+ *   ids  [T,k] int32 (device, written): chosen expert ids, slot order = logit order
+ *   w    [T,k] FP32  (device, written): softmax over the chosen logits (sums to 1)
+ * Routing replay passes these back to moe_forward. */
+moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                       int32_t* ids, float* w, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
+
+/* The whole block for T tokens.
+ *   x    [T,d] act dtype (device)
+ *   ids, w  NULL: route internally.  Otherwise [T,k] int32 ids (each in [0,E)) and
+ *           FP32 weights used instead of the router's (routing replay).
+ *   out  [T,d] out dtype (device, written) */
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                         const int32_t* ids, const float* w, void* out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* moe_forward with CUDA events recorded on `stream` at each stage boundary:
+ * events[0] before the first kernel and events[i] after stage i-1 (i = 1..n_events-1,
+ * at most moe_num_stages()+1 events).  For measurement only; same results. */
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* W,
+                                  const void* x, const int32_t* ids, const float* w,
+                                  void* out, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream, moe_event_t* events, int n_events);
+
+/* Number and names of the stages moe_forward_profiled brackets. */
+int moe_num_stages(void);
+const char* moe_stage_name(int stage);
+
+/* Number of kernels moe_forward launches for this config (for launch accounting). */
+int moe_forward_launches(const moe_config_t* cfg, int route_internally);
+
+/* Byte offsets, inside the workspace of this config, of the intermediates a test may
+ * inspect after a call (the buffers stay valid until the next call on the workspace):
+ *   0 h32 [T,d] FP32 (TF32-rounded)   1 h16 [T,d] BF16     2 ids [T,k] int32
+ *   3 w [T,k] FP32                    4 pooled [T,p] FP32   5 row_off [E+1] int32
+ *   6 src [T*k] int32 (dispatched row -> t*k+j)              7 inv [T*k] int32
+ *   8 A_perm [T*k,p]  9 s [T*k,I]  10 y [T*k,p] (expert dtype)  11 c [T,p] (act dtype)
+ * Writes min(n, 12) offsets and returns how many it wrote (0 for an invalid config). */
+int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n);
+
+/* Synchronises `stream`, returns the device-side status of every call since the last
+ * read (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears it.  detail (may
+ * be NULL) receives a code naming the wait or check that failed. */
+moe_status_t moe_read_status(void* ws, size_t ws_bytes, moe_stream_t stream,
+                             int32_t* detail);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LATENT_MOE_H */

@@ -1,0 +1,412 @@
+// kernels_mem.cuh -- the memory-bound steps of the latent-MoE block:
+//   norm_in        full-width RMSNorm of x -> h32 (TF32-rounded FP32, router operand)
+//                  and h16 (BF16, pooler operand)
+//   dispatch       histogram of expert ids -> per-expert row offsets -> stable
+//                  counting-sort positions (token-major order) and the inverse map
+//   pool_permute   RMSNorm of the pooled row, cast, written to the k permuted rows
+//                  of the expert GEMM input
+//   combine        per-expert RMSNorm of each selected expert output, times its route
+//                  weight, summed in FP32 in slot order
+//   pack           gate/up interleave and TF32 rounding of weights
+// ("SGLang and Miles Add Day-0 Support for Muse Spark Open": section "MoE with Pooler,
+// Unpooler and Per-Expert Normalization"; "The Fused Post-per-expert Norm" for the
+// combine; "Kernel Optimizations" for the norm fused into the boundary kernel and the
+// packed routing output.)
+#pragma once
+
+#include "common.cuh"
+
+namespace lmoe {
+
+constexpr int MEM_THREADS = 256;
+constexpr int DISPATCH_CHUNK = 2048;   // (token, slot) pairs per counting-sort chunk
+constexpr int MAX_TOPK = 8;
+
+// Sum over the block; every thread gets the result.  `red` holds >= 32 floats.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = (l < (blockDim.x >> 5)) ? red[l] : 0.f;
+  s = warp_sum(s);
+  return s;
+}
+
+// ---- full-width RMSNorm ---------------------------------------------------------------
+// One block per token.  Pass 1 sums squares; pass 2 re-reads the row (L1-resident) and
+// writes h = x * rsqrt(mean(x^2) + eps) * g twice: TF32-rounded FP32 and BF16.
+template <bool ACT_F32>
+__global__ void __launch_bounds__(MEM_THREADS)
+    norm_in_kernel(const void* __restrict__ x, const float* __restrict__ g,
+                   float* __restrict__ h32, __nv_bfloat16* __restrict__ h16, int d, float eps) {
+  __shared__ float red[32];
+  const size_t t = blockIdx.x;
+  const int nchunk = d >> 3;  // 8 elements per chunk
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    float v[8];
+    if constexpr (ACT_F32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + t * d) + 2 * c;
+      const float4 a = src[0], b = src[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+      const uint4 a = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + t * d)[c];
+      float2 f;
+      f = unpack_bf16x2(a.x); v[0] = f.x; v[1] = f.y;
+      f = unpack_bf16x2(a.y); v[2] = f.x; v[3] = f.y;
+      f = unpack_bf16x2(a.z); v[4] = f.x; v[5] = f.y;
+      f = unpack_bf16x2(a.w); v[6] = f.x; v[7] = f.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss = fmaf(v[i], v[i], ss);
+  }
+  const float total = block_sum(ss, red);
+  const float rs = rsqrtf(total / static_cast<float>(d) + eps);
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    float v[8];
+    if constexpr (ACT_F32) {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + t * d) + 2 * c;
+      const float4 a = src[0], b = src[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+      const uint4 a = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + t * d)[c];
+      float2 f;
+      f = unpack_bf16x2(a.x); v[0] = f.x; v[1] = f.y;
+      f = unpack_bf16x2(a.y); v[2] = f.x; v[3] = f.y;
+      f = unpack_bf16x2(a.z); v[4] = f.x; v[5] = f.y;
+      f = unpack_bf16x2(a.w); v[6] = f.x; v[7] = f.y;
+    }
+    const float4 g0 = reinterpret_cast<const float4*>(g)[2 * c];
+    const float4 g1 = reinterpret_cast<const float4*>(g)[2 * c + 1];
+    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    float h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = v[i] * rs * gg[i];
+    float4* o32 = reinterpret_cast<float4*>(h32 + t * d) + 2 * c;
+    o32[0] = make_float4(tf32_rna(h[0]), tf32_rna(h[1]), tf32_rna(h[2]), tf32_rna(h[3]));
+    o32[1] = make_float4(tf32_rna(h[4]), tf32_rna(h[5]), tf32_rna(h[6]), tf32_rna(h[7]));
+    if constexpr (!ACT_F32) {
+      uint4 o;
+      o.x = pack_bf16x2(h[0], h[1]); o.y = pack_bf16x2(h[2], h[3]);
+      o.z = pack_bf16x2(h[4], h[5]); o.w = pack_bf16x2(h[6], h[7]);
+      reinterpret_cast<uint4*>(h16 + t * d)[c] = o;
+    }
+  }
+}
+
+// ---- dispatch: counting sort of (token, slot) pairs by expert -------------------------
+// 1) per-chunk histograms.  Ids outside [0, E) are counted nowhere and reported.
+__global__ void __launch_bounds__(MEM_THREADS)
+    dispatch_hist_kernel(const int32_t* __restrict__ ids, int n, int E,
+                         int* __restrict__ chunk_counts, int* status) {
+  __shared__ int hist[256];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * DISPATCH_CHUNK;
+  const int end = min(base + DISPATCH_CHUNK, n);
+  for (int i = base + threadIdx.x; i < end; i += blockDim.x) {
+    const int e = ids[i];
+    if (e >= 0 && e < E) atomicAdd(&hist[e], 1);
+    else report_error(status, ST_DEVICE_CHECK, CHECK_EXPERT_ID);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) chunk_counts[blockIdx.x * E + e] = hist[e];
+}
+
+// exclusive scan over the block (blockDim = 256); returns the prefix, *total = sum
+__device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
+  const int l = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (l >= o) x += y;
+  }
+  __syncthreads();
+  if (l == 31) sh[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    int s = (l < (blockDim.x >> 5)) ? sh[l] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (l >= o) s += y;
+    }
+    if (l < (blockDim.x >> 5)) sh[l] = s;   // inclusive warp totals
+  }
+  __syncthreads();
+  const int warp_prefix = (w > 0) ? sh[w - 1] : 0;
+  *total = sh[(blockDim.x >> 5) - 1];
+  return warp_prefix + x - v;
+}
+
+// 2) one block: chunk bases per expert, expert row offsets and 128-row tile offsets.
+__global__ void __launch_bounds__(256)
+    dispatch_scan_kernel(int* __restrict__ chunk_counts, int nchunks, int E,
+                         int* __restrict__ row_off, int* __restrict__ mt_off) {
+  __shared__ int sh[32];
+  const int e = threadIdx.x;
+  int running = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[c * E + e];
+      chunk_counts[c * E + e] = running;
+      running += v;
+    }
+  }
+  int total;
+  const int off = block_excl_scan(e < E ? running : 0, sh, &total);
+  const int mt = (e < E) ? (running + 127) / 128 : 0;
+  int mt_total;
+  const int mto = block_excl_scan(mt, sh, &mt_total);
+  if (e < E) {
+    row_off[e] = off;
+    mt_off[e] = mto;
+    for (int c = 0; c < nchunks; ++c) chunk_counts[c * E + e] += off;
+  }
+  if (e == 0) {
+    row_off[E] = total;
+    mt_off[E] = mt_total;
+  }
+}
+
+// 3) one warp per chunk: stable positions in (token, slot) order.  Lanes holding the
+// same expert rank themselves by lane order; chunks and rounds run in order, so the
+// rows of each expert keep token order.
+__global__ void __launch_bounds__(32)
+    dispatch_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
+                            const int* __restrict__ chunk_base, int* __restrict__ inv,
+                            int* __restrict__ src) {
+  __shared__ int cnt[256];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32) cnt[e] = chunk_base[blockIdx.x * E + e];
+  __syncwarp();
+  const int base = blockIdx.x * DISPATCH_CHUNK;
+  const int end = min(base + DISPATCH_CHUNK, n);
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i0 = base; i0 < end; i0 += 32) {
+    const int i = i0 + lane;
+    int e = (i < end) ? ids[i] : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & lt);
+    const int pos0 = (e >= 0) ? cnt[e] : 0;
+    __syncwarp();
+    if (e >= 0 && (__ffs(peers) - 1) == lane) cnt[e] = pos0 + __popc(peers);
+    __syncwarp();
+    if (i < end) {
+      if (e >= 0) {
+        const int pos = pos0 + rank;
+        inv[i] = pos;
+        src[pos] = i;
+      } else {
+        inv[i] = -1;
+      }
+    }
+  }
+}
+
+// ---- pooled-input RMSNorm + cast + permute ---------------------------------------------
+// One block per token: u = pooled * rsqrt(mean(pooled^2) + eps) * g_pool, written in the
+// GEMM operand format to the token's k dispatched rows.
+template <bool OUT_F32>
+__global__ void __launch_bounds__(MEM_THREADS)
+    pool_permute_kernel(const float* __restrict__ pooled, const float* __restrict__ g,
+                        const int* __restrict__ inv, void* __restrict__ a_perm, int p, int k,
+                        float eps) {
+  __shared__ float red[32];
+  __shared__ int rows[MAX_TOPK];
+  const size_t t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = inv[t * k + threadIdx.x];
+  const int nchunk = p >> 3;
+  constexpr int CPT = 4;  // chunks of 8 per thread: p <= 8192
+  float v[CPT][8];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + j * MEM_THREADS;
+    if (c < nchunk) {
+      const float4* s = reinterpret_cast<const float4*>(pooled + t * p) + 2 * c;
+      const float4 a = s[0], b = s[1];
+      v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+      v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(v[j][i], v[j][i], ss);
+    }
+  }
+  const float total = block_sum(ss, red);   // also orders rows[] before its use
+  const float rs = rsqrtf(total / static_cast<float>(p) + eps);
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = threadIdx.x + j * MEM_THREADS;
+    if (c < nchunk) {
+      const float4 g0 = reinterpret_cast<const float4*>(g)[2 * c];
+      const float4 g1 = reinterpret_cast<const float4*>(g)[2 * c + 1];
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      float u[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = v[j][i] * rs * gg[i];
+      if constexpr (OUT_F32) {
+        const float4 o0 = make_float4(tf32_rna(u[0]), tf32_rna(u[1]), tf32_rna(u[2]), tf32_rna(u[3]));
+        const float4 o1 = make_float4(tf32_rna(u[4]), tf32_rna(u[5]), tf32_rna(u[6]), tf32_rna(u[7]));
+        for (int s = 0; s < k; ++s) {
+          const int r = rows[s];
+          if (r < 0) continue;
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a_perm) + size_t(r) * p) + 2 * c;
+          dst[0] = o0;
+          dst[1] = o1;
+        }
+      } else {
+        uint4 o;
+        o.x = pack_bf16x2(u[0], u[1]); o.y = pack_bf16x2(u[2], u[3]);
+        o.z = pack_bf16x2(u[4], u[5]); o.w = pack_bf16x2(u[6], u[7]);
+        for (int s = 0; s < k; ++s) {
+          const int r = rows[s];
+          if (r < 0) continue;
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a_perm) + size_t(r) * p)[c] = o;
+        }
+      }
+    }
+  }
+}
+
+// ---- combine -----------------------------------------------------------------------
+// One block per token.  Pass 1: sum of squares of each selected expert output row (the
+// values as stored).  Pass 2: c = sum_j w_j * y_j * rsqrt(mean(y_j^2) + eps) * g_exp[e_j]
+// accumulated in FP32 in slot order j = 0..k-1.
+template <bool Y_F32, bool C_F32>
+__global__ void __launch_bounds__(MEM_THREADS)
+    combine_kernel(const void* __restrict__ y, const int* __restrict__ inv,
+                   const int32_t* __restrict__ ids, const float* __restrict__ wts,
+                   const float* __restrict__ g_exp, void* __restrict__ c_out, int p, int k,
+                   int E, float eps) {
+  __shared__ float red[32 * MAX_TOPK];
+  __shared__ int rows[MAX_TOPK];
+  __shared__ int eids[MAX_TOPK];
+  __shared__ float wj[MAX_TOPK];
+  __shared__ float rsj[MAX_TOPK];
+  const size_t t = blockIdx.x;
+  if (threadIdx.x < k) {
+    int r = inv[t * k + threadIdx.x];
+    int e = ids[t * k + threadIdx.x];
+    if (e < 0 || e >= E) { r = -1; e = 0; }
+    rows[threadIdx.x] = r;
+    eids[threadIdx.x] = e;
+    wj[threadIdx.x] = wts[t * k + threadIdx.x];
+  }
+  __syncthreads();
+  const int nchunk = p >> 3;
+  auto load8 = [&](int r, int c, float (&v)[8]) {
+    if constexpr (Y_F32) {
+      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(y) + size_t(r) * p) + 2 * c;
+      const float4 a = s[0], b = s[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+      const uint4 a = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + size_t(r) * p)[c];
+      float2 f;
+      f = unpack_bf16x2(a.x); v[0] = f.x; v[1] = f.y;
+      f = unpack_bf16x2(a.y); v[2] = f.x; v[3] = f.y;
+      f = unpack_bf16x2(a.z); v[4] = f.x; v[5] = f.y;
+      f = unpack_bf16x2(a.w); v[6] = f.x; v[7] = f.y;
+    }
+  };
+  float ss[MAX_TOPK];
+#pragma unroll
+  for (int j = 0; j < MAX_TOPK; ++j) ss[j] = 0.f;
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+#pragma unroll
+    for (int j = 0; j < MAX_TOPK; ++j) {
+      if (j < k && rows[j] >= 0) {
+        float v[8];
+        load8(rows[j], c, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ss[j] = fmaf(v[i], v[i], ss[j]);
+      }
+    }
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < MAX_TOPK; ++j) {
+    const float s = warp_sum(ss[j]);
+    if (l == 0) red[j * 32 + w] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    float s = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[threadIdx.x * 32 + i];
+    rsj[threadIdx.x] = rsqrtf(s / static_cast<float>(p) + eps);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int r = rows[j];
+      if (r < 0) continue;
+      float v[8];
+      load8(r, c, v);
+      const float s = wj[j] * rsj[j];
+      const float4 g0 = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p)[2 * c];
+      const float4 g1 = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p)[2 * c + 1];
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s, v[i] * gg[i], acc[i]);
+    }
+    if constexpr (C_F32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(c_out) + t * p) + 2 * c;
+      dst[0] = make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]), tf32_rna(acc[2]), tf32_rna(acc[3]));
+      dst[1] = make_float4(tf32_rna(acc[4]), tf32_rna(acc[5]), tf32_rna(acc[6]), tf32_rna(acc[7]));
+    } else {
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]); o.w = pack_bf16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(c_out) + t * p)[c] = o;
+    }
+  }
+}
+
+// ---- weight preparation ----------------------------------------------------------------
+__global__ void round_tf32_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                  size_t n4) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n4;
+       i += size_t(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(src)[i];
+    reinterpret_cast<float4*>(dst)[i] = make_float4(tf32_rna(a.x), tf32_rna(a.y), tf32_rna(a.z), tf32_rna(a.w));
+  }
+}
+
+// One block per destination row of w13 [E, 2I, p]: rows are interleaved in blocks of G:
+// dst[e][2G*b + i] = gate[e][G*b + i], dst[e][2G*b + G + i] = up[e][G*b + i].
+template <bool ROUND_TF32>
+__global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __restrict__ up,
+                                void* __restrict__ dst, int I, int p, int G, int elem_bytes) {
+  const size_t drow = blockIdx.x;         // e * 2I + r
+  const size_t e = drow / (2 * I);
+  const int r = static_cast<int>(drow - e * 2 * I);
+  const int b = r / (2 * G);
+  const int i = r - b * 2 * G;
+  const bool is_up = i >= G;
+  const size_t srow = e * I + size_t(b) * G + (is_up ? i - G : i);
+  const uint8_t* s = static_cast<const uint8_t*>(is_up ? up : gate) + srow * p * elem_bytes;
+  uint8_t* o = static_cast<uint8_t*>(dst) + drow * p * elem_bytes;
+  const int n16 = p * elem_bytes / 16;
+  for (int c = threadIdx.x; c < n16; c += blockDim.x) {
+    uint4 v = reinterpret_cast<const uint4*>(s)[c];
+    if constexpr (ROUND_TF32) {
+      v.x = __float_as_uint(tf32_rna(__uint_as_float(v.x)));
+      v.y = __float_as_uint(tf32_rna(__uint_as_float(v.y)));
+      v.z = __float_as_uint(tf32_rna(__uint_as_float(v.z)));
+      v.w = __float_as_uint(tf32_rna(__uint_as_float(v.w)));
+    }
+    reinterpret_cast<uint4*>(o)[c] = v;
+  }
+}
+
+__global__ void clear_status_kernel(int* status) {
+  if (threadIdx.x < 2) status[threadIdx.x] = 0;
+}
+
+}  // namespace lmoe

@@ -1,0 +1,521 @@
+// moe_api.cu -- the C ABI of the latent-MoE block (declared in include/latent_moe.h):
+// argument validation, workspace carving, TMA descriptors and the launch sequence.
+// Nothing here allocates device memory; every buffer is the caller's.
+#include <mutex>
+
+#include "../../include/latent_moe.h"
+#include "common.cuh"
+#include "gemm_tcgen05.cuh"
+#include "kernels_mem.cuh"
+
+using namespace lmoe;
+
+namespace {
+
+
+constexpr unsigned long long WAIT_LIMIT_NS = 1000000000ull;       // 1 s
+constexpr unsigned long long TEST_WAIT_LIMIT_NS = 20000000ull;    // 20 ms
+
+enum Stage { STG_NORM = 0, STG_ROUTER, STG_POOL, STG_DISPATCH, STG_GEMM1, STG_GEMM2,
+             STG_COMBINE, STG_UNPOOL, STG_COUNT };
+const char* const kStageNames[STG_COUNT] = {"norm", "router", "pool", "dispatch",
+                                            "gemm1_gate_up_swiglu", "gemm2_down",
+                                            "combine", "unpool"};
+
+constexpr int W13_GROUP = 128;   // gate/up interleave block (rows)
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// ---- driver entry point for tensor maps ------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, inner] operand, tiles of box_rows x 128 bytes, 128-byte swizzle,
+// zero fill outside the tensor.
+bool make_tmap(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t rows,
+               uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const uint32_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * es};
+  cuuint32_t box[2] = {128u / es, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---- per-device cache -------------------------------------------------------------------
+struct DevInfo {
+  int sms = 0;
+  bool ready = false;
+};
+DevInfo g_dev[64];
+std::mutex g_mu;
+
+template <bool TF32, int EPI>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(gemm_tcgen05_kernel<TF32, EPI>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(gemm_smem_bytes()));
+}
+
+moe_status_t device_ready(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& D = g_dev[dev];
+  if (!D.ready) {
+    if (cudaDeviceGetAttribute(&D.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_smem_attr<true, EPI_ROUTER>();
+    if (e == cudaSuccess) e = set_smem_attr<true, EPI_STORE>();
+    if (e == cudaSuccess) e = set_smem_attr<false, EPI_STORE>();
+    if (e == cudaSuccess) e = set_smem_attr<true, EPI_SWIGLU>();
+    if (e == cudaSuccess) e = set_smem_attr<false, EPI_SWIGLU>();
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    D.ready = true;
+  }
+  *sms = D.sms;
+  return MOE_OK;
+}
+
+// ---- validation and workspace layout ------------------------------------------------------
+moe_status_t validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d <= 0 || c->p <= 0 || c->I <= 0 || c->E <= 0 || c->top_k <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->E) return MOE_ERR_INVALID_ARG;
+  if (!(c->eps >= 0.0f) || c->eps > 1.0f) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_BF16 && c->act != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (c->out != MOE_BF16 && c->out != MOE_F32) return MOE_ERR_INVALID_ARG;
+  if (c->expert != MOE_BF16 && c->expert != MOE_F32 && c->expert != MOE_NVFP4)
+    return MOE_ERR_INVALID_ARG;
+  if (c->expert != c->act) return MOE_ERR_UNSUPPORTED;
+  if ((c->flags & ~MOE_FLAG_TEST_TIMEOUT) != 0) return MOE_ERR_INVALID_ARG;
+  if (c->E > 256 || c->top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+  if (c->d % 128 || c->p % 128 || c->I % 128) return MOE_ERR_UNSUPPORTED;
+  if (c->d > 32768 || c->p > 8192 || c->I > 32768) return MOE_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(c->T) * c->top_k;
+  if (rows > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(c->E) * 2 * c->I > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+struct WsLayout {
+  size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, src, inv, a_perm, s, y,
+      c, total;
+  int nchunks;
+};
+
+WsLayout ws_layout(const moe_config_t& c) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t T = c.T, d = c.d, p = c.p, E = c.E, k = c.top_k, I = c.I;
+  const size_t ea = c.act == MOE_F32 ? 4 : 2;
+  const size_t ee = c.expert == MOE_F32 ? 4 : 2;
+  L.nchunks = static_cast<int>((T * k + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
+  L.status = take(256);
+  L.h32 = take(T * d * 4);
+  L.h16 = take(c.act == MOE_BF16 ? T * d * 2 : 0);
+  L.ids = take(T * k * 4);
+  L.wts = take(T * k * 4);
+  L.pooled = take(T * p * 4);
+  L.chunk = take(size_t(L.nchunks) * E * 4);
+  L.row_off = take((E + 1) * 4);
+  L.mt_off = take((E + 1) * 4);
+  L.src = take(T * k * 4);
+  L.inv = take(T * k * 4);
+  L.a_perm = take(T * k * p * ee);
+  L.s = take(T * k * I * ee);
+  L.y = take(T * k * p * ee);
+  L.c = take(T * p * ea);
+  L.total = off;
+  return L;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* W, bool route_only,
+                           bool need_router) {
+  if (!W) return MOE_ERR_INVALID_ARG;
+  const void* need[] = {W->g_in, need_router ? W->w_router : W->g_in};
+  for (const void* p : need)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (route_only) return MOE_OK;
+  const void* more[] = {W->w_pool, W->g_pool, W->w13, W->w2, W->g_exp, W->w_unpool};
+  for (const void* p : more)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+inline moe_status_t last_launch() {
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline int bn_for(int n) { return (n % 256 == 0) ? 256 : 128; }
+
+template <bool TF32, int EPI>
+moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& P,
+                         int grid, cudaStream_t st) {
+  if (grid <= 0) return MOE_OK;
+  gemm_tcgen05_kernel<TF32, EPI><<<grid, GEMM_THREADS, gemm_smem_bytes(), st>>>(ta, tb, P);
+  return last_launch();
+}
+
+GemmParams base_params(int* status, uint32_t flags) {
+  GemmParams P{};
+  P.status = status;
+  P.timeout_ns = (flags & MOE_FLAG_TEST_TIMEOUT) ? TEST_WAIT_LIMIT_NS : WAIT_LIMIT_NS;
+  return P;
+}
+
+struct Events {
+  cudaEvent_t* ev;
+  int n;
+  cudaStream_t st;
+  void mark(int i) {   // after stage i-1
+    if (ev && i < n && ev[i]) cudaEventRecord(ev[i], st);
+  }
+};
+
+#define MOE_TRY(expr)                \
+  do {                               \
+    moe_status_t _s = (expr);        \
+    if (_s != MOE_OK) return _s;     \
+  } while (0)
+
+// The block.  route_only: stop after the router, writing ids_out / w_out.
+moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                       const int32_t* ids_in, const float* w_in, void* out, int32_t* ids_out,
+                       float* w_out, bool route_only, void* ws, size_t ws_bytes,
+                       cudaStream_t st, cudaEvent_t* ev, int nev) {
+  MOE_TRY(validate(cfg));
+  const moe_config_t& c = *cfg;
+  const bool internal_route = route_only || ids_in == nullptr;
+  if (!route_only && ((ids_in == nullptr) != (w_in == nullptr))) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_weights(c, W, route_only, internal_route));
+  if (!x || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  if (route_only && (!ids_out || !w_out)) return MOE_ERR_INVALID_ARG;
+  if (!route_only && (!out || !aligned16(out))) return MOE_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(c);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  Events E{ev, nev, st};
+  E.mark(0);
+  if (c.T == 0) return MOE_OK;
+  int sms = 0;
+  MOE_TRY(device_ready(&sms));
+
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  int* status = reinterpret_cast<int*>(base + L.status);
+  float* h32 = reinterpret_cast<float*>(base + L.h32);
+  __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(base + L.h16);
+  const bool act_f32 = c.act == MOE_F32;
+  const bool exp_f32 = c.expert == MOE_F32;
+  const int T = c.T, d = c.d, p = c.p, E_ = c.E, k = c.top_k, I = c.I;
+  const int rows = T * k;
+  const int mtiles = (T + GEMM_BM - 1) / GEMM_BM;
+
+  // ---- stage: full-width RMSNorm ------------------------------------------------------
+  if (act_f32)
+    norm_in_kernel<true><<<T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, d, c.eps);
+  else
+    norm_in_kernel<false><<<T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, h16, d, c.eps);
+  MOE_TRY(last_launch());
+  E.mark(1);
+
+  // ---- stage: router GEMM (TF32) + top-k ------------------------------------------------
+  int32_t* ids = route_only ? ids_out : reinterpret_cast<int32_t*>(base + L.ids);
+  float* wts = route_only ? w_out : reinterpret_cast<float*>(base + L.wts);
+  if (internal_route) {
+    const int bn = (E_ + 15) / 16 * 16;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, h32, true, d, T, GEMM_BM) ||
+        !make_tmap(&tb, W->w_router, true, d, E_, bn))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.M = T; P.N = bn; P.K = d; P.bn = bn; P.groups = 0;
+    P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
+    MOE_TRY((launch_gemm<true, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st)));
+  } else {
+    ids = const_cast<int32_t*>(ids_in);
+    wts = const_cast<float*>(w_in);
+  }
+  E.mark(2);
+  if (route_only) return MOE_OK;
+
+  // ---- stage: pooler GEMM -> pooled FP32 ------------------------------------------------
+  float* pooled = reinterpret_cast<float*>(base + L.pooled);
+  {
+    CUtensorMap ta, tb;
+    const int bn = bn_for(p);
+    if (!make_tmap(&ta, act_f32 ? static_cast<const void*>(h32) : h16, act_f32, d, T, GEMM_BM) ||
+        !make_tmap(&tb, W->w_pool, act_f32, d, p, bn))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.M = T; P.N = p; P.K = d; P.bn = bn; P.groups = 0;
+    P.out = pooled; P.ld_out = p; P.out_fmt = OUT_F32;
+    const int grid = std::min(sms, mtiles * (p / bn));
+    if (act_f32) MOE_TRY((launch_gemm<true, EPI_STORE>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<false, EPI_STORE>(ta, tb, P, grid, st)));
+  }
+  E.mark(3);
+
+  // ---- stage: dispatch (counting sort) + pooled RMSNorm + permute ---------------------
+  int* chunk = reinterpret_cast<int*>(base + L.chunk);
+  int* row_off = reinterpret_cast<int*>(base + L.row_off);
+  int* mt_off = reinterpret_cast<int*>(base + L.mt_off);
+  int* src = reinterpret_cast<int*>(base + L.src);
+  int* inv = reinterpret_cast<int*>(base + L.inv);
+  void* a_perm = base + L.a_perm;
+  dispatch_hist_kernel<<<L.nchunks, MEM_THREADS, 0, st>>>(ids, rows, E_, chunk, status);
+  MOE_TRY(last_launch());
+  dispatch_scan_kernel<<<1, 256, 0, st>>>(chunk, L.nchunks, E_, row_off, mt_off);
+  MOE_TRY(last_launch());
+  dispatch_scatter_kernel<<<L.nchunks, 32, 0, st>>>(ids, rows, E_, chunk, inv, src);
+  MOE_TRY(last_launch());
+  if (exp_f32)
+    pool_permute_kernel<true><<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv, a_perm, p, k, c.eps);
+  else
+    pool_permute_kernel<false><<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv, a_perm, p, k, c.eps);
+  MOE_TRY(last_launch());
+  E.mark(4);
+
+  // ---- stage: grouped gate/up GEMM + SwiGLU -------------------------------------------
+  void* s_buf = base + L.s;
+  const int max_mt = (rows + GEMM_BM - 1) / GEMM_BM + E_;
+  {
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, a_perm, exp_f32, p, rows, GEMM_BM) ||
+        !make_tmap(&tb, W->w13, exp_f32, p, static_cast<uint64_t>(E_) * 2 * I, 2 * W13_GROUP))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.N = 2 * I; P.K = p; P.bn = 2 * W13_GROUP; P.groups = E_;
+    P.row_off = row_off; P.mt_off = mt_off;
+    P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
+    P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
+    const int grid = std::min(sms, max_mt * (2 * I / P.bn));
+    if (exp_f32) MOE_TRY((launch_gemm<true, EPI_SWIGLU>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<false, EPI_SWIGLU>(ta, tb, P, grid, st)));
+  }
+  E.mark(5);
+
+  // ---- stage: grouped down GEMM -> y ------------------------------------------------------
+  void* y_buf = base + L.y;
+  {
+    CUtensorMap ta, tb;
+    const int bn = bn_for(p);
+    if (!make_tmap(&ta, s_buf, exp_f32, I, rows, GEMM_BM) ||
+        !make_tmap(&tb, W->w2, exp_f32, I, static_cast<uint64_t>(E_) * p, bn))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.N = p; P.K = I; P.bn = bn; P.groups = E_;
+    P.row_off = row_off; P.mt_off = mt_off;
+    P.out = y_buf; P.ld_out = p; P.out_fmt = exp_f32 ? OUT_F32 : OUT_BF16;
+    const int grid = std::min(sms, max_mt * (p / bn));
+    if (exp_f32) MOE_TRY((launch_gemm<true, EPI_STORE>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<false, EPI_STORE>(ta, tb, P, grid, st)));
+  }
+  E.mark(6);
+
+  // ---- stage: per-expert RMSNorm + FP32 weighted sum -------------------------------------
+  void* c_buf = base + L.c;
+  if (exp_f32) {
+    if (act_f32)
+      combine_kernel<true, true><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+    else
+      combine_kernel<true, false><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+  } else {
+    if (act_f32)
+      combine_kernel<false, true><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+    else
+      combine_kernel<false, false><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+  }
+  MOE_TRY(last_launch());
+  E.mark(7);
+
+  // ---- stage: unpooler GEMM -> out ----------------------------------------------------------
+  {
+    CUtensorMap ta, tb;
+    const int bn = bn_for(d);
+    if (!make_tmap(&ta, c_buf, act_f32, p, T, GEMM_BM) ||
+        !make_tmap(&tb, W->w_unpool, act_f32, p, d, bn))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.M = T; P.N = d; P.K = p; P.bn = bn; P.groups = 0;
+    P.out = out; P.ld_out = d; P.out_fmt = c.out == MOE_F32 ? OUT_F32 : OUT_BF16;
+    const int grid = std::min(sms, mtiles * (d / bn));
+    if (act_f32) MOE_TRY((launch_gemm<true, EPI_STORE>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<false, EPI_STORE>(ta, tb, P, grid, st)));
+  }
+  E.mark(8);
+  return MOE_OK;
+}
+
+}  // namespace
+
+// =====================================================================================
+extern "C" {
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  return ws_layout(*cfg).total;
+}
+
+moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
+  clear_status_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<int*>(ws));
+  return last_launch();
+}
+
+size_t moe_packed_bytes(const moe_config_t* cfg, int which) {
+  if (validate(cfg) != MOE_OK) return 0;
+  const moe_config_t& c = *cfg;
+  const size_t ea = c.act == MOE_F32 ? 4 : 2;
+  const size_t ee = c.expert == MOE_F32 ? 4 : 2;
+  switch (which) {
+    case 0: return size_t(c.E) * c.d * 4;
+    case 1: return size_t(c.E) * 2 * c.I * c.p * ee;
+    case 2: return c.expert == MOE_F32 ? size_t(c.E) * c.p * c.I * ee : 0;
+    case 3: return c.act == MOE_F32 ? size_t(c.p) * c.d * ea : 0;
+    case 4: return c.act == MOE_F32 ? size_t(c.d) * c.p * ea : 0;
+    default: return 0;
+  }
+}
+
+moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weights_t* src,
+                              float* w_router_out, void* w13_out, void* w2_out,
+                              void* w_pool_out, void* w_unpool_out, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config_t& c = *cfg;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!src || !src->w_router || !src->w_gate || !src->w_up || !w_router_out || !w13_out)
+    return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {src->w_router, src->w_gate, src->w_up, w_router_out, w13_out};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const bool act_f32 = c.act == MOE_F32, exp_f32 = c.expert == MOE_F32;
+  if (exp_f32 && (!src->w_down || !w2_out || !aligned16(w2_out))) return MOE_ERR_INVALID_ARG;
+  if (act_f32 && (!src->w_pool || !src->w_unpool || !w_pool_out || !w_unpool_out ||
+                  !aligned16(w_pool_out) || !aligned16(w_unpool_out)))
+    return MOE_ERR_INVALID_ARG;
+  auto round = [&](const void* s, void* d, size_t n) {
+    const size_t n4 = n / 4;
+    const int grid = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 4096));
+    round_tf32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(s), static_cast<float*>(d), n4);
+    return last_launch();
+  };
+  MOE_TRY(round(src->w_router, w_router_out, size_t(c.E) * c.d));
+  const int es = exp_f32 ? 4 : 2;
+  const unsigned rows13 = static_cast<unsigned>(c.E) * 2u * c.I;
+  if (exp_f32)
+    pack_w13_kernel<true><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
+  else
+    pack_w13_kernel<false><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
+  MOE_TRY(last_launch());
+  if (exp_f32) MOE_TRY(round(src->w_down, w2_out, size_t(c.E) * c.p * c.I));
+  if (act_f32) {
+    MOE_TRY(round(src->w_pool, w_pool_out, size_t(c.p) * c.d));
+    MOE_TRY(round(src->w_unpool, w_unpool_out, size_t(c.d) * c.p));
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                       int32_t* ids, float* w, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+  return run_layer(cfg, W, x, nullptr, nullptr, nullptr, ids, w, true, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                         const int32_t* ids, const float* w, void* out, void* ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+  return run_layer(cfg, W, x, ids, w, out, nullptr, nullptr, false, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
+}
+
+moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* W,
+                                  const void* x, const int32_t* ids, const float* w,
+                                  void* out, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                  moe_event_t* events, int n_events) {
+  if (n_events < 0 || (n_events > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  return run_layer(cfg, W, x, ids, w, out, nullptr, nullptr, false, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream),
+                   reinterpret_cast<cudaEvent_t*>(events), n_events);
+}
+
+int moe_num_stages(void) { return STG_COUNT; }
+
+const char* moe_stage_name(int stage) {
+  return (stage >= 0 && stage < STG_COUNT) ? kStageNames[stage] : "";
+}
+
+int moe_forward_launches(const moe_config_t* cfg, int route_internally) {
+  if (validate(cfg) != MOE_OK || cfg->T == 0) return 0;
+  // norm, [router], pooler, 4 dispatch kernels, gate/up, down, combine, unpooler
+  return 10 + (route_internally ? 1 : 0);
+}
+
+int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n) {
+  if (validate(cfg) != MOE_OK || !offsets || n <= 0) return 0;
+  const WsLayout L = ws_layout(*cfg);
+  const size_t all[12] = {L.h32, L.h16, L.ids, L.wts, L.pooled, L.row_off,
+                          L.src, L.inv, L.a_perm, L.s, L.y, L.c};
+  const int m = n < 12 ? n : 12;
+  for (int i = 0; i < m; ++i) offsets[i] = all[i];
+  return m;
+}
+
+moe_status_t moe_read_status(void* ws, size_t ws_bytes, moe_stream_t stream, int32_t* detail) {
+  if (!ws || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  clear_status_kernel<<<1, 32, 0, st>>>(static_cast<int*>(ws));
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return static_cast<moe_status_t>(h[0]);
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device index check failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

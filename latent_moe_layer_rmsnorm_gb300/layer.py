@@ -1,0 +1,159 @@
+"""Torch-facing wrapper of the C ABI: owns the device buffers, marshals pointers.
+
+PyTorch only allocates memory and supplies the stream; every step of the layer runs
+in libmoe_latent.so's kernels.  There is no CPU path: without the library or a CUDA
+device the constructor raises.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+from .synth import Shape
+
+_DT = {"bf16": L.MOE_BF16, "f32": L.MOE_F32, "nvfp4": L.MOE_NVFP4}
+_TORCH = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def make_config(shape: Shape, T: int | None = None, out: str = "bf16",
+                flags: int = 0) -> L.moe_config_t:
+    return L.moe_config_t(T=shape.T if T is None else T, d=shape.d, p=shape.p, E=shape.E,
+                          top_k=shape.top_k, I=shape.I, eps=shape.eps, act=_DT[shape.act],
+                          expert=_DT[shape.expert], out=_DT[out], flags=flags)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+class LatentMoE:
+    """One latent-MoE layer with packed weights resident on the current CUDA device.
+
+    weights: canonical tensors as produced by synth.make_inputs (x is ignored):
+    g_in, w_router, w_pool, g_pool, w_gate, w_up, w_down, g_exp, w_unpool.
+    keep_canonical=False releases the gate/up tensors after packing.
+    """
+
+    def __init__(self, shape: Shape, weights: dict, out: str = "bf16",
+                 keep_canonical: bool = True):
+        if not torch.cuda.is_available():
+            raise RuntimeError("LatentMoE needs a CUDA device (no CPU path)")
+        L.lib()
+        self.shape = shape
+        self.out = out
+        cfg = make_config(shape, out=out)
+        dev = weights["w_router"].device
+        self.device = dev
+        w = {k: v.contiguous() for k, v in weights.items() if isinstance(v, torch.Tensor)}
+
+        def buf(which, dtype):
+            n = L.moe_packed_bytes(cfg, which)
+            if n == 0:
+                return None
+            es = torch.tensor([], dtype=dtype).element_size()
+            return torch.empty(n // es, dtype=dtype, device=dev)
+
+        act = _TORCH[shape.act]
+        self.w_router = buf(L.PACK_ROUTER, torch.float32)
+        self.w13 = buf(L.PACK_W13, act)
+        w2p, poolp, unpoolp = buf(L.PACK_W2, act), buf(L.PACK_POOL, act), buf(L.PACK_UNPOOL, act)
+        src = L.moe_canonical_weights_t(
+            w_router=_ptr(w["w_router"]), w_pool=_ptr(w["w_pool"]), w_gate=_ptr(w["w_gate"]),
+            w_up=_ptr(w["w_up"]), w_down=_ptr(w["w_down"]), w_unpool=_ptr(w["w_unpool"]))
+        L.check(L.moe_pack_weights(cfg, src, _ptr(self.w_router), _ptr(self.w13), _ptr(w2p),
+                                   _ptr(poolp), _ptr(unpoolp), _stream()), "moe_pack_weights")
+        self.w2 = w2p if w2p is not None else w["w_down"]
+        self.w_pool = poolp if poolp is not None else w["w_pool"]
+        self.w_unpool = unpoolp if unpoolp is not None else w["w_unpool"]
+        self.g_in, self.g_pool, self.g_exp = (w["g_in"].float().contiguous(),
+                                              w["g_pool"].float().contiguous(),
+                                              w["g_exp"].float().contiguous())
+        self.W = L.moe_weights_t(g_in=_ptr(self.g_in), w_router=_ptr(self.w_router),
+                                 w_pool=_ptr(self.w_pool), g_pool=_ptr(self.g_pool),
+                                 w13=_ptr(self.w13), w2=_ptr(self.w2), g_exp=_ptr(self.g_exp),
+                                 w_unpool=_ptr(self.w_unpool))
+        if keep_canonical:
+            self.canonical = w
+        self.ws = None
+        self.ws_bytes = 0
+
+    # ---- buffers -----------------------------------------------------------------------
+    def config(self, T: int, flags: int = 0) -> L.moe_config_t:
+        return make_config(self.shape, T=T, out=self.out, flags=flags)
+
+    def workspace(self, T: int) -> tuple[int, int]:
+        need = L.moe_workspace_size(self.config(T))
+        if need == 0:
+            raise L.MoeError(L.MOE_ERR_INVALID_ARG, "moe_workspace_size")
+        if self.ws is None or self.ws_bytes < need:
+            self.ws = torch.empty(need + 256, dtype=torch.uint8, device=self.device)
+            self.ws_off = (-self.ws.data_ptr()) % 256
+            self.ws_bytes = need
+            L.check(L.moe_workspace_init(self.ws.data_ptr() + self.ws_off, need, _stream()),
+                    "moe_workspace_init")
+        return self.ws.data_ptr() + self.ws_off, self.ws_bytes
+
+    def out_dtype(self):
+        return _TORCH[self.out]
+
+    # ---- calls -----------------------------------------------------------------------
+    def forward(self, x: torch.Tensor, ids: torch.Tensor | None = None,
+                w: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                flags: int = 0, events=None) -> torch.Tensor:
+        T = x.shape[0]
+        assert x.is_contiguous() and x.dtype == _TORCH[self.shape.act]
+        if out is None:
+            out = torch.empty((T, self.shape.d), dtype=self.out_dtype(), device=x.device)
+        ws, nbytes = self.workspace(T)
+        cfg = self.config(T, flags)
+        if ids is not None:
+            ids = ids.to(torch.int32).contiguous()
+            w = w.to(torch.float32).contiguous()
+        if events is None:
+            st = L.moe_forward(cfg, self.W, x.data_ptr(), _ptr(ids), _ptr(w), out.data_ptr(),
+                               ws, nbytes, _stream())
+        else:
+            st = L.moe_forward_profiled(cfg, self.W, x.data_ptr(), _ptr(ids), _ptr(w),
+                                        out.data_ptr(), ws, nbytes, _stream(), events)
+        L.check(st, "moe_forward")
+        return out
+
+    def route(self, x: torch.Tensor):
+        T = x.shape[0]
+        k = self.shape.top_k
+        ids = torch.empty((T, k), dtype=torch.int32, device=x.device)
+        w = torch.empty((T, k), dtype=torch.float32, device=x.device)
+        ws, nbytes = self.workspace(T)
+        L.check(L.moe_route(self.config(T), self.W, x.data_ptr(), ids.data_ptr(), w.data_ptr(),
+                            ws, nbytes, _stream()), "moe_route")
+        return ids, w
+
+    def read_status(self):
+        ws, nbytes = self.workspace(1) if self.ws is None else (self.ws.data_ptr() + self.ws_off,
+                                                                 self.ws_bytes)
+        return L.moe_read_status(ws, nbytes, _stream())
+
+    def intermediate(self, name: str, T: int) -> torch.Tensor:
+        """Copy of one workspace intermediate after a call with T tokens (for tests)."""
+        sh, k = self.shape, self.shape.top_k
+        act, exp = _TORCH[sh.act], _TORCH[sh.expert]
+        spec = {"h32": ((T, sh.d), torch.float32), "h16": ((T, sh.d), torch.bfloat16),
+                "ids": ((T, k), torch.int32), "w": ((T, k), torch.float32),
+                "pooled": ((T, sh.p), torch.float32), "row_off": ((sh.E + 1,), torch.int32),
+                "src": ((T * k,), torch.int32), "inv": ((T * k,), torch.int32),
+                "a_perm": ((T * k, sh.p), exp), "s": ((T * k, sh.I), exp),
+                "y": ((T * k, sh.p), exp), "c": ((T, sh.p), act)}
+        shape, dtype = spec[name]
+        off = L.moe_workspace_offsets(self.config(T))[name] + self.ws_off
+        n = 1
+        for v in shape:
+            n *= v
+        es = torch.tensor([], dtype=dtype).element_size()
+        return self.ws[off: off + n * es].view(dtype).reshape(shape).clone()
+
+    def launches(self, T: int, route_internally: bool = True) -> int:
+        return L.moe_forward_launches(self.config(T), route_internally)

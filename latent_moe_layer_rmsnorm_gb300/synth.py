@@ -70,8 +70,18 @@ def storage_dtype(kind: str) -> torch.dtype:
 
 def _gen(seed: int, device) -> torch.Generator:
     g = torch.Generator(device=device)
-    g.manual_seed(int(seed))
+    g.manual_seed(int(seed) & 0x7FFFFFFFFFFFFFFF)
     return g
+
+
+_STREAM_IDS = {"x": 1, "g_in": 2, "w_router": 3, "w_pool": 4, "g_pool": 5, "w_gate": 6,
+               "w_up": 7, "w_down": 8, "g_exp": 9, "w_unpool": 10}
+
+
+def _stream_seed(seed: int, name: str, expert: int = 0) -> int:
+    """Independent seed per (workload seed, tensor, expert): any tensor or expert can be
+    drawn on its own, in any order."""
+    return (int(seed) * 1000003 + _STREAM_IDS[name] * 65537 + expert * 257) % (1 << 62)
 
 
 def _normal(shape, std, gen, device, out_dtype):
@@ -87,34 +97,55 @@ def _uniform_gain(shape, gen, device, store_dtype):
     return t.to(store_dtype).to(torch.float32)
 
 
+def make_expert(shape: Shape, seed: int, e: int, device="cpu") -> dict:
+    """Gate, up and down matrices of expert e: [I,p], [I,p], [p,I]."""
+    exp = storage_dtype(shape.expert)
+    p, I = shape.p, shape.I
+    return {
+        "w_gate": _normal((I, p), 1.0 / math.sqrt(p), _gen(_stream_seed(seed, "w_gate", e), device),
+                          device, exp),
+        "w_up": _normal((I, p), 1.0 / math.sqrt(p), _gen(_stream_seed(seed, "w_up", e), device),
+                        device, exp),
+        "w_down": _normal((p, I), 1.0 / math.sqrt(I), _gen(_stream_seed(seed, "w_down", e), device),
+                          device, exp),
+    }
+
+
+def make_dense(shape: Shape, seed: int = 0, device="cpu") -> dict:
+    """Every input except the expert matrices."""
+    act = storage_dtype(shape.act)
+    T, d, p, E = shape.T, shape.d, shape.p, shape.E
+    g = lambda name: _gen(_stream_seed(seed, name), device)  # noqa: E731
+    out = {
+        "x": _normal((T, d), 1.0, g("x"), device, act),
+        "g_in": _uniform_gain((d,), g("g_in"), device, act),
+        "w_router": _normal((E, d), 1.0 / math.sqrt(d), g("w_router"), device, torch.float32),
+        "w_pool": _normal((p, d), 1.0 / math.sqrt(d), g("w_pool"), device, act),
+        "g_pool": _uniform_gain((p,), g("g_pool"), device, act),
+        "g_exp": _uniform_gain((E, p), g("g_exp"), device, act),
+        "w_unpool": _normal((d, p), 1.0 / math.sqrt(p), g("w_unpool"), device, act),
+    }
+    if shape.zipf_s > 0:
+        apply_zipf_skew(out, shape, seed)
+    return out
+
+
 def make_inputs(shape: Shape, seed: int = 0, device="cpu") -> dict:
     """Draw every input of one layer call.  Deterministic for (shape, seed, device).
 
-    Expert tensors are drawn one expert at a time so that the FP32 staging
-    buffer stays one expert large even for the 24 GB expert weight set.
+    Expert tensors are drawn one expert at a time, so the FP32 staging buffer stays
+    one expert large even for the 24 GB expert weight set.
     """
-    gen = _gen(seed, device)
-    act = storage_dtype(shape.act)
+    out = make_dense(shape, seed, device)
     exp = storage_dtype(shape.expert)
-    T, d, p, E, I = shape.T, shape.d, shape.p, shape.E, shape.I
-    out = {}
-    out["x"] = _normal((T, d), 1.0, gen, device, act)
-    out["g_in"] = _uniform_gain((d,), gen, device, act)
-    out["w_router"] = _normal((E, d), 1.0 / math.sqrt(d), gen, device, torch.float32)
-    out["w_pool"] = _normal((p, d), 1.0 / math.sqrt(d), gen, device, act)
-    out["g_pool"] = _uniform_gain((p,), gen, device, act)
+    E, p, I = shape.E, shape.p, shape.I
     w_gate = torch.empty((E, I, p), dtype=exp, device=device)
     w_up = torch.empty((E, I, p), dtype=exp, device=device)
     w_down = torch.empty((E, p, I), dtype=exp, device=device)
     for e in range(E):
-        w_gate[e] = _normal((I, p), 1.0 / math.sqrt(p), gen, device, exp)
-        w_up[e] = _normal((I, p), 1.0 / math.sqrt(p), gen, device, exp)
-        w_down[e] = _normal((p, I), 1.0 / math.sqrt(I), gen, device, exp)
+        m = make_expert(shape, seed, e, device)
+        w_gate[e], w_up[e], w_down[e] = m["w_gate"], m["w_up"], m["w_down"]
     out["w_gate"], out["w_up"], out["w_down"] = w_gate, w_up, w_down
-    out["g_exp"] = _uniform_gain((E, p), gen, device, act)
-    out["w_unpool"] = _normal((d, p), 1.0 / math.sqrt(p), gen, device, act)
-    if shape.zipf_s > 0:
-        apply_zipf_skew(out, shape, seed)
     return out
 
 
@@ -161,7 +192,7 @@ def apply_zipf_skew(inp: dict, shape: Shape, seed: int, strength: float = SKEW_S
     expert e on every token.  Returns the offsets b.
     """
     device = inp["x"].device
-    gen = _gen(seed + 104729, device)
+    gen = _gen(seed * 7 + 104729, device)
     d = shape.d
     v = (torch.randint(0, 2, (d,), generator=gen, device=device, dtype=torch.int32) * 2 - 1
          ).to(torch.float32)

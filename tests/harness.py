@@ -18,17 +18,14 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 
 class LazyExperts:
-    """w[e] -> numpy FP32 copy of one expert's matrix (host copy on demand)."""
+    """w[e] -> numpy FP32 copy of one expert's matrix, copied to the host on demand
+    (nothing is cached: the full expert set can be tens of GB)."""
 
     def __init__(self, t: torch.Tensor):
         self.t = t
-        self.cache = {}
 
     def __getitem__(self, e):
-        e = int(e)
-        if e not in self.cache:
-            self.cache[e] = to_np(self.t[e])
-        return self.cache[e]
+        return to_np(self.t[int(e)])
 
     def __len__(self):
         return self.t.shape[0]
