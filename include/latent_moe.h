@@ -89,15 +89,22 @@ typedef struct {
   uint32_t flags;
 } moe_config_t;
 
-/* Weights as moe_forward consumes them (all device pointers, read only):
+/* Weights as moe_forward consumes them (all device pointers, read only).  "Packed"
+ * tensors are written by moe_pack_weights:
  *   g_in      [d]        FP32 gain of the full-width norm
- *   w_router  [E,d]      FP32 router rows, already rounded to TF32 by moe_pack_weights
- *   w_pool    [p,d]      pooler (act dtype; F32: TF32-rounded by moe_pack_weights)
+ *   w_router  [E,d]      packed: FP32 router rows rounded to TF32
+ *   w_pool    [p,d]      packed: FP16 (BF16 configs) or TF32-rounded FP32
  *   g_pool    [p]        FP32 gain of the pooled-input norm
- *   w13       packed gate/up rows of every expert, written by moe_pack_weights
- *   w2        [E,p,I]    down projections (expert dtype; F32: TF32-rounded)
+ *   w13       packed gate/up rows of every expert: FP16 or TF32-rounded FP32
+ *   w2        [E,p,I]    down projections: the BF16 checkpoint tensor as given, or (FP32
+ *                        configs) a packed TF32-rounded copy
  *   g_exp     [E,p]      FP32 per-expert output-norm gains
- *   w_unpool  [d,p]      unpooler (act dtype; F32: TF32-rounded)               */
+ *   w_unpool  [d,p]      packed: FP16 or TF32-rounded FP32
+ * BF16 configurations run the pooler, gate/up and unpooler GEMMs on FP16 operands: the
+ * activations they read (h, u, c) are RMS-normalised, hence bounded by
+ * sqrt(width) * max|gain|, and FP16 keeps 3 more significand bits than BF16 at the same
+ * tensor-core rate.  The down GEMM reads s = silu(a) * b, which has no such bound, in
+ * BF16.  The BF16 -> FP16 weight copies are exact for |w| >= 2^-17.                   */
 typedef struct {
   const float* g_in;
   const float* w_router;
@@ -133,7 +140,7 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Bytes of the packed buffers moe_pack_weights writes.  which: 0 = w_router (TF32
  * copy), 1 = w13, 2 = w2, 3 = w_pool, 4 = w_unpool.  Returns 0 for a buffer this
- * config does not need packed (BF16 w2 / w_pool / w_unpool are used as given). */
+ * config does not need packed (a BF16 w2 is used as given). */
 size_t moe_packed_bytes(const moe_config_t* cfg, int which);
 
 /* Prepares weights for moe_forward ("SGLang and Miles Add Day-0 Support for Muse Spark
@@ -142,9 +149,10 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which);
  *  - w_router_out [E,d] FP32: w_router rounded to TF32 (ties away), the router's
  *    operand precision (the vLLM page's "Nvidia" section: TF32 router GEMM).
  *  - w13_out: gate and up rows interleaved in blocks of G rows (G = 128), so one
- *    256-row tile of the gate/up GEMM holds gate rows i..i+G and the matching up rows.
- *  - w2_out, w_pool_out, w_unpool_out: F32 configs only, TF32-rounded copies; pass
- *    NULL for BF16 configs (those tensors are then used as given).
+ *    256-row tile of the gate/up GEMM holds gate rows i..i+G and the matching up rows;
+ *    converted to FP16 (BF16 configs) or rounded to TF32 (FP32 configs).
+ *  - w_pool_out, w_unpool_out: FP16 copies (BF16 configs) or TF32-rounded copies.
+ *  - w2_out: FP32 configs only, a TF32-rounded copy; pass NULL for BF16 configs.
  * Output buffers are caller-allocated with moe_packed_bytes; none may alias a source. */
 moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weights_t* src,
                               float* w_router_out, void* w13_out, void* w2_out,
@@ -185,10 +193,11 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally);
 
 /* Byte offsets, inside the workspace of this config, of the intermediates a test may
  * inspect after a call (the buffers stay valid until the next call on the workspace):
- *   0 h32 [T,d] FP32 (TF32-rounded)   1 h16 [T,d] BF16     2 ids [T,k] int32
+ *   0 h32 [T,d] FP32 (TF32-rounded)   1 h16 [T,d] FP16     2 ids [T,k] int32
  *   3 w [T,k] FP32                    4 pooled [T,p] FP32   5 row_off [E+1] int32
  *   6 src [T*k] int32 (dispatched row -> t*k+j)              7 inv [T*k] int32
- *   8 A_perm [T*k,p]  9 s [T*k,I]  10 y [T*k,p] (expert dtype)  11 c [T,p] (act dtype)
+ *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (BF16 / FP32)   10 y [T*k,p] FP32
+ *  11 c [T,p] (FP16 / FP32)
  * Writes min(n, 12) offsets and returns how many it wrote (0 for an invalid config). */
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n);
 

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -171,8 +172,8 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 // Instruction descriptor, dense MMA with FP32 accumulation, both operands K-major:
-//   bits 4-5 D format (1 = F32); bits 7-9 / 10-12 A / B format (kind::f16: 1 = BF16;
-//   kind::tf32: 2 = TF32); bits 17-22 N >> 3; bits 24-28 M >> 4.
+//   bits 4-5 D format (1 = F32); bits 7-9 / 10-12 A / B format (kind::f16: 0 = F16,
+//   1 = BF16; kind::tf32: 2 = TF32); bits 17-22 N >> 3; bits 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t ab_format, uint32_t m,
                                                     uint32_t n) {
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((n >> 3) << 17) |
@@ -222,6 +223,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -2,10 +2,11 @@
 // both operands K-major, fed by TMA, for every projection of the latent-MoE block:
 //
 //   router  h32 [T,d] x W_r [E,d]          TF32, epilogue = top-k + renormalised softmax
-//   pooler  h16 [T,d] x W_pool [p,d]        BF16, epilogue = FP32 store
-//   gate/up A_perm [Tk,p] x W13_e [2I,p]    BF16, grouped by expert, epilogue = SwiGLU
-//   down    s [Tk,I] x W2_e [p,I]           BF16, grouped by expert, epilogue = store
-//   unpool  c [T,p] x W_unpool [d,p]        BF16, epilogue = store
+//   pooler  h16 [T,d] x W_pool [p,d]        FP16, epilogue = FP32 store
+//   gate/up A_perm [Tk,p] x W13_e [2I,p]    FP16, grouped by expert, epilogue = SwiGLU
+//   down    s [Tk,I] x W2_e [p,I]           BF16, grouped by expert, epilogue = FP32 store
+//   unpool  c [T,p] x W_unpool [d,p]        FP16, epilogue = store
+// (FP32 configurations run every projection on TF32 operands.)
 //
 // ("SGLang and Miles Add Day-0 Support for Muse Spark Open": section "MoE with Pooler,
 // Unpooler and Per-Expert Normalization" for the steps; "Kernel Optimizations" for the
@@ -38,6 +39,8 @@ constexpr int ROUTER_MAX_K = 8;
 
 enum EpiKind : int { EPI_ROUTER = 0, EPI_STORE = 1, EPI_SWIGLU = 2 };
 enum OutFmt : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_TF32 = 2 };
+// Operand kinds; the values are the instruction-descriptor format codes.
+enum OpKind : int { OP_F16 = 0, OP_BF16 = 1, OP_TF32 = 2 };
 
 struct GemmParams {
   int M;        // dense: rows of A and of the output
@@ -231,7 +234,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
   }
 }
 
-template <bool TF32, int EPI>
+template <int KIND, int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const GemmParams P) {
@@ -275,6 +278,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   const uint32_t tmem_base = S->tmem_base;
   const int num_tiles = gemm_num_tiles(P, S);
+  constexpr bool TF32 = KIND == OP_TF32;
   const int kblocks = P.K / (TF32 ? 32 : 64);   // one 128-byte slice per stage
   const uint64_t limit = P.timeout_ns;
   volatile int* abort_flag = &S->abort_flag;
@@ -318,7 +322,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = idesc_f32acc(TF32 ? 2u : 1u, GEMM_BM, P.bn);
+    const uint32_t idesc = idesc_f32acc(static_cast<uint32_t>(KIND), GEMM_BM, P.bn);
     int stage = 0;
     uint32_t phase = 0;
     int it = 0;

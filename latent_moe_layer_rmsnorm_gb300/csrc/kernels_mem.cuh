@@ -1,13 +1,14 @@
 // kernels_mem.cuh -- the memory-bound steps of the latent-MoE block:
 //   norm_in        full-width RMSNorm of x -> h32 (TF32-rounded FP32, router operand)
-//                  and h16 (BF16, pooler operand)
+//                  and h16 (FP16, pooler operand)
 //   dispatch       histogram of expert ids -> per-expert row offsets -> stable
 //                  counting-sort positions (token-major order) and the inverse map
 //   pool_permute   RMSNorm of the pooled row, cast, written to the k permuted rows
 //                  of the expert GEMM input
 //   combine        per-expert RMSNorm of each selected expert output, times its route
 //                  weight, summed in FP32 in slot order
-//   pack           gate/up interleave and TF32 rounding of weights
+//   pack           gate/up interleave and weight conversion (BF16 -> FP16, or TF32
+//                  rounding for FP32 configurations)
 // ("SGLang and Miles Add Day-0 Support for Muse Spark Open": section "MoE with Pooler,
 // Unpooler and Per-Expert Normalization"; "The Fused Post-per-expert Norm" for the
 // combine; "Kernel Optimizations" for the norm fused into the boundary kernel and the
@@ -36,11 +37,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // ---- full-width RMSNorm ---------------------------------------------------------------
 // One block per token.  Pass 1 sums squares; pass 2 re-reads the row (L1-resident) and
-// writes h = x * rsqrt(mean(x^2) + eps) * g twice: TF32-rounded FP32 and BF16.
+// writes h = x * rsqrt(mean(x^2) + eps) * g twice: TF32-rounded FP32 and FP16.  FP16 is
+// safe for h: |h_i| <= sqrt(d) * max|g| (e.g. 91 * 1.5 at d = 8192).
 template <bool ACT_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     norm_in_kernel(const void* __restrict__ x, const float* __restrict__ g,
-                   float* __restrict__ h32, __nv_bfloat16* __restrict__ h16, int d, float eps) {
+                   float* __restrict__ h32, __half* __restrict__ h16, int d, float eps) {
   __shared__ float red[32];
   const size_t t = blockIdx.x;
   const int nchunk = d >> 3;  // 8 elements per chunk
@@ -89,8 +91,8 @@ __global__ void __launch_bounds__(MEM_THREADS)
     o32[1] = make_float4(tf32_rna(h[4]), tf32_rna(h[5]), tf32_rna(h[6]), tf32_rna(h[7]));
     if constexpr (!ACT_F32) {
       uint4 o;
-      o.x = pack_bf16x2(h[0], h[1]); o.y = pack_bf16x2(h[2], h[3]);
-      o.z = pack_bf16x2(h[4], h[5]); o.w = pack_bf16x2(h[6], h[7]);
+      o.x = pack_f16x2(h[0], h[1]); o.y = pack_f16x2(h[2], h[3]);
+      o.z = pack_f16x2(h[4], h[5]); o.w = pack_f16x2(h[6], h[7]);
       reinterpret_cast<uint4*>(h16 + t * d)[c] = o;
     }
   }
@@ -210,7 +212,8 @@ __global__ void __launch_bounds__(32)
 
 // ---- pooled-input RMSNorm + cast + permute ---------------------------------------------
 // One block per token: u = pooled * rsqrt(mean(pooled^2) + eps) * g_pool, written in the
-// GEMM operand format to the token's k dispatched rows.
+// GEMM operand format (FP16, or TF32-rounded FP32) to the token's k dispatched rows.
+// FP16 is safe for u: |u_i| <= sqrt(p) * max|g_pool|.
 template <bool OUT_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     pool_permute_kernel(const float* __restrict__ pooled, const float* __restrict__ g,
@@ -260,12 +263,12 @@ __global__ void __launch_bounds__(MEM_THREADS)
         }
       } else {
         uint4 o;
-        o.x = pack_bf16x2(u[0], u[1]); o.y = pack_bf16x2(u[2], u[3]);
-        o.z = pack_bf16x2(u[4], u[5]); o.w = pack_bf16x2(u[6], u[7]);
+        o.x = pack_f16x2(u[0], u[1]); o.y = pack_f16x2(u[2], u[3]);
+        o.z = pack_f16x2(u[4], u[5]); o.w = pack_f16x2(u[6], u[7]);
         for (int s = 0; s < k; ++s) {
           const int r = rows[s];
           if (r < 0) continue;
-          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a_perm) + size_t(r) * p)[c] = o;
+          reinterpret_cast<uint4*>(static_cast<__half*>(a_perm) + size_t(r) * p)[c] = o;
         }
       }
     }
@@ -275,7 +278,8 @@ __global__ void __launch_bounds__(MEM_THREADS)
 // ---- combine -----------------------------------------------------------------------
 // One block per token.  Pass 1: sum of squares of each selected expert output row (the
 // values as stored).  Pass 2: c = sum_j w_j * y_j * rsqrt(mean(y_j^2) + eps) * g_exp[e_j]
-// accumulated in FP32 in slot order j = 0..k-1.
+// accumulated in FP32 in slot order j = 0..k-1, stored as the unpooler's operand: FP16
+// (|c_i| <= sum_j |w_j| * sqrt(p) * max|g_exp|), or TF32-rounded FP32.
 template <bool Y_F32, bool C_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     combine_kernel(const void* __restrict__ y, const int* __restrict__ inv,
@@ -361,26 +365,48 @@ __global__ void __launch_bounds__(MEM_THREADS)
       dst[1] = make_float4(tf32_rna(acc[4]), tf32_rna(acc[5]), tf32_rna(acc[6]), tf32_rna(acc[7]));
     } else {
       uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]); o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]); o.w = pack_bf16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(c_out) + t * p)[c] = o;
+      o.x = pack_f16x2(acc[0], acc[1]); o.y = pack_f16x2(acc[2], acc[3]);
+      o.z = pack_f16x2(acc[4], acc[5]); o.w = pack_f16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4*>(static_cast<__half*>(c_out) + t * p)[c] = o;
     }
   }
 }
 
 // ---- weight preparation ----------------------------------------------------------------
-__global__ void round_tf32_kernel(const float* __restrict__ src, float* __restrict__ dst,
-                                  size_t n4) {
-  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n4;
-       i += size_t(gridDim.x) * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(src)[i];
-    reinterpret_cast<float4*>(dst)[i] = make_float4(tf32_rna(a.x), tf32_rna(a.y), tf32_rna(a.z), tf32_rna(a.w));
+// Element conversion applied while packing a weight: FP32 -> TF32 (ties away) for FP32
+// configurations, BF16 -> FP16 for BF16 ones (exact for |w| >= 2^-17; smaller values
+// round to the FP16 subnormal grid, 2^-24 apart).
+enum PackConv : int { CONV_TF32 = 0, CONV_BF16_TO_F16 = 1 };
+
+template <int CONV>
+__device__ __forceinline__ uint4 pack_convert(uint4 v) {
+  if constexpr (CONV == CONV_TF32) {
+    v.x = __float_as_uint(tf32_rna(__uint_as_float(v.x)));
+    v.y = __float_as_uint(tf32_rna(__uint_as_float(v.y)));
+    v.z = __float_as_uint(tf32_rna(__uint_as_float(v.z)));
+    v.w = __float_as_uint(tf32_rna(__uint_as_float(v.w)));
+  } else {
+    float2 f;
+    f = unpack_bf16x2(v.x); v.x = pack_f16x2(f.x, f.y);
+    f = unpack_bf16x2(v.y); v.y = pack_f16x2(f.x, f.y);
+    f = unpack_bf16x2(v.z); v.z = pack_f16x2(f.x, f.y);
+    f = unpack_bf16x2(v.w); v.w = pack_f16x2(f.x, f.y);
   }
+  return v;
+}
+
+// Converted copy of n bytes (a multiple of 16) of a weight tensor.
+template <int CONV>
+__global__ void convert_copy_kernel(const void* __restrict__ src, void* __restrict__ dst,
+                                    size_t n16) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n16;
+       i += size_t(gridDim.x) * blockDim.x)
+    reinterpret_cast<uint4*>(dst)[i] = pack_convert<CONV>(reinterpret_cast<const uint4*>(src)[i]);
 }
 
 // One block per destination row of w13 [E, 2I, p]: rows are interleaved in blocks of G:
 // dst[e][2G*b + i] = gate[e][G*b + i], dst[e][2G*b + G + i] = up[e][G*b + i].
-template <bool ROUND_TF32>
+template <int CONV>
 __global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __restrict__ up,
                                 void* __restrict__ dst, int I, int p, int G, int elem_bytes) {
   const size_t drow = blockIdx.x;         // e * 2I + r
@@ -393,16 +419,8 @@ __global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __res
   const uint8_t* s = static_cast<const uint8_t*>(is_up ? up : gate) + srow * p * elem_bytes;
   uint8_t* o = static_cast<uint8_t*>(dst) + drow * p * elem_bytes;
   const int n16 = p * elem_bytes / 16;
-  for (int c = threadIdx.x; c < n16; c += blockDim.x) {
-    uint4 v = reinterpret_cast<const uint4*>(s)[c];
-    if constexpr (ROUND_TF32) {
-      v.x = __float_as_uint(tf32_rna(__uint_as_float(v.x)));
-      v.y = __float_as_uint(tf32_rna(__uint_as_float(v.y)));
-      v.z = __float_as_uint(tf32_rna(__uint_as_float(v.z)));
-      v.w = __float_as_uint(tf32_rna(__uint_as_float(v.w)));
-    }
-    reinterpret_cast<uint4*>(o)[c] = v;
-  }
+  for (int c = threadIdx.x; c < n16; c += blockDim.x)
+    reinterpret_cast<uint4*>(o)[c] = pack_convert<CONV>(reinterpret_cast<const uint4*>(s)[c]);
 }
 
 __global__ void clear_status_kernel(int* status) {

@@ -46,21 +46,24 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major [rows, inner] operand, tiles of box_rows x 128 bytes, 128-byte swizzle,
-// zero fill outside the tensor.
-bool make_tmap(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t rows,
+// Row-major [rows, inner] operand of the given kind, tiles of box_rows x 128 bytes,
+// 128-byte swizzle, zero fill outside the tensor.  TF32 operands are plain FP32 words
+// (already rounded), so the copy moves their bits unchanged.
+bool make_tmap(CUtensorMap* m, const void* base, int kind, uint64_t inner, uint64_t rows,
                uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const uint32_t es = f32 ? 4 : 2;
+  const uint32_t es = kind == OP_TF32 ? 4 : 2;
+  const CUtensorMapDataType dt = kind == OP_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : kind == OP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * es};
   cuuint32_t box[2] = {128u / es, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ---- per-device cache -------------------------------------------------------------------
@@ -71,9 +74,9 @@ struct DevInfo {
 DevInfo g_dev[64];
 std::mutex g_mu;
 
-template <bool TF32, int EPI>
+template <int KIND, int EPI>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(gemm_tcgen05_kernel<TF32, EPI>,
+  return cudaFuncSetAttribute(gemm_tcgen05_kernel<KIND, EPI>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(gemm_smem_bytes()));
 }
@@ -87,11 +90,12 @@ moe_status_t device_ready(int* sms) {
     if (cudaDeviceGetAttribute(&D.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return MOE_ERR_CUDA;
     cudaError_t e = cudaSuccess;
-    if (e == cudaSuccess) e = set_smem_attr<true, EPI_ROUTER>();
-    if (e == cudaSuccess) e = set_smem_attr<true, EPI_STORE>();
-    if (e == cudaSuccess) e = set_smem_attr<false, EPI_STORE>();
-    if (e == cudaSuccess) e = set_smem_attr<true, EPI_SWIGLU>();
-    if (e == cudaSuccess) e = set_smem_attr<false, EPI_SWIGLU>();
+    if (e == cudaSuccess) e = set_smem_attr<OP_TF32, EPI_ROUTER>();
+    if (e == cudaSuccess) e = set_smem_attr<OP_TF32, EPI_STORE>();
+    if (e == cudaSuccess) e = set_smem_attr<OP_TF32, EPI_SWIGLU>();
+    if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_STORE>();
+    if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_SWIGLU>();
+    if (e == cudaSuccess) e = set_smem_attr<OP_BF16, EPI_STORE>();
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     D.ready = true;
   }
@@ -152,7 +156,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.inv = take(T * k * 4);
   L.a_perm = take(T * k * p * ee);
   L.s = take(T * k * I * ee);
-  L.y = take(T * k * p * ee);
+  L.y = take(T * k * p * 4);     // expert outputs stay FP32 until the per-expert norm
   L.c = take(T * p * ea);
   L.total = off;
   return L;
@@ -179,11 +183,11 @@ inline moe_status_t last_launch() {
 
 inline int bn_for(int n) { return (n % 256 == 0) ? 256 : 128; }
 
-template <bool TF32, int EPI>
+template <int KIND, int EPI>
 moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& P,
                          int grid, cudaStream_t st) {
   if (grid <= 0) return MOE_OK;
-  gemm_tcgen05_kernel<TF32, EPI><<<grid, GEMM_THREADS, gemm_smem_bytes(), st>>>(ta, tb, P);
+  gemm_tcgen05_kernel<KIND, EPI><<<grid, GEMM_THREADS, gemm_smem_bytes(), st>>>(ta, tb, P);
   return last_launch();
 }
 
@@ -234,9 +238,14 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   uint8_t* base = static_cast<uint8_t*>(ws);
   int* status = reinterpret_cast<int*>(base + L.status);
   float* h32 = reinterpret_cast<float*>(base + L.h32);
-  __nv_bfloat16* h16 = reinterpret_cast<__nv_bfloat16*>(base + L.h16);
+  __half* h16 = reinterpret_cast<__half*>(base + L.h16);
   const bool act_f32 = c.act == MOE_F32;
   const bool exp_f32 = c.expert == MOE_F32;
+  // operand kinds: FP32 configurations run on TF32; BF16 ones keep the norm-bounded
+  // operands (h, u, c) and the weights they meet in FP16, and s / W2 in BF16
+  const int k_proj = act_f32 ? OP_TF32 : OP_F16;      // pooler, unpooler
+  const int k_up = exp_f32 ? OP_TF32 : OP_F16;        // gate/up GEMM
+  const int k_down = exp_f32 ? OP_TF32 : OP_BF16;     // down GEMM
   const int T = c.T, d = c.d, p = c.p, E_ = c.E, k = c.top_k, I = c.I;
   const int rows = T * k;
   const int mtiles = (T + GEMM_BM - 1) / GEMM_BM;
@@ -255,13 +264,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   if (internal_route) {
     const int bn = (E_ + 15) / 16 * 16;
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, h32, true, d, T, GEMM_BM) ||
-        !make_tmap(&tb, W->w_router, true, d, E_, bn))
+    if (!make_tmap(&ta, h32, OP_TF32, d, T, GEMM_BM) ||
+        !make_tmap(&tb, W->w_router, OP_TF32, d, E_, bn))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = bn; P.K = d; P.bn = bn; P.groups = 0;
     P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
-    MOE_TRY((launch_gemm<true, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st)));
+    MOE_TRY((launch_gemm<OP_TF32, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st)));
   } else {
     ids = const_cast<int32_t*>(ids_in);
     wts = const_cast<float*>(w_in);
@@ -274,15 +283,15 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
-    if (!make_tmap(&ta, act_f32 ? static_cast<const void*>(h32) : h16, act_f32, d, T, GEMM_BM) ||
-        !make_tmap(&tb, W->w_pool, act_f32, d, p, bn))
+    if (!make_tmap(&ta, act_f32 ? static_cast<const void*>(h32) : h16, k_proj, d, T, GEMM_BM) ||
+        !make_tmap(&tb, W->w_pool, k_proj, d, p, bn))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = p; P.K = d; P.bn = bn; P.groups = 0;
     P.out = pooled; P.ld_out = p; P.out_fmt = OUT_F32;
     const int grid = std::min(sms, mtiles * (p / bn));
-    if (act_f32) MOE_TRY((launch_gemm<true, EPI_STORE>(ta, tb, P, grid, st)));
-    else MOE_TRY((launch_gemm<false, EPI_STORE>(ta, tb, P, grid, st)));
+    if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
   }
   E.mark(3);
 
@@ -311,8 +320,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   const int max_mt = (rows + GEMM_BM - 1) / GEMM_BM + E_;
   {
     CUtensorMap ta, tb;
-    if (!make_tmap(&ta, a_perm, exp_f32, p, rows, GEMM_BM) ||
-        !make_tmap(&tb, W->w13, exp_f32, p, static_cast<uint64_t>(E_) * 2 * I, 2 * W13_GROUP))
+    if (!make_tmap(&ta, a_perm, k_up, p, rows, GEMM_BM) ||
+        !make_tmap(&tb, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, 2 * W13_GROUP))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = 2 * I; P.K = p; P.bn = 2 * W13_GROUP; P.groups = E_;
@@ -320,8 +329,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
     const int grid = std::min(sms, max_mt * (2 * I / P.bn));
-    if (exp_f32) MOE_TRY((launch_gemm<true, EPI_SWIGLU>(ta, tb, P, grid, st)));
-    else MOE_TRY((launch_gemm<false, EPI_SWIGLU>(ta, tb, P, grid, st)));
+    if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_SWIGLU>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<OP_F16, EPI_SWIGLU>(ta, tb, P, grid, st)));
   }
   E.mark(5);
 
@@ -330,32 +339,25 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
-    if (!make_tmap(&ta, s_buf, exp_f32, I, rows, GEMM_BM) ||
-        !make_tmap(&tb, W->w2, exp_f32, I, static_cast<uint64_t>(E_) * p, bn))
+    if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
+        !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, bn))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = bn; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt_off;
-    P.out = y_buf; P.ld_out = p; P.out_fmt = exp_f32 ? OUT_F32 : OUT_BF16;
+    P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32;
     const int grid = std::min(sms, max_mt * (p / bn));
-    if (exp_f32) MOE_TRY((launch_gemm<true, EPI_STORE>(ta, tb, P, grid, st)));
-    else MOE_TRY((launch_gemm<false, EPI_STORE>(ta, tb, P, grid, st)));
+    if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<OP_BF16, EPI_STORE>(ta, tb, P, grid, st)));
   }
   E.mark(6);
 
   // ---- stage: per-expert RMSNorm + FP32 weighted sum -------------------------------------
   void* c_buf = base + L.c;
-  if (exp_f32) {
-    if (act_f32)
-      combine_kernel<true, true><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
-    else
-      combine_kernel<true, false><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
-  } else {
-    if (act_f32)
-      combine_kernel<false, true><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
-    else
-      combine_kernel<false, false><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
-  }
+  if (act_f32)
+    combine_kernel<true, true><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+  else
+    combine_kernel<true, false><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
   MOE_TRY(last_launch());
   E.mark(7);
 
@@ -363,15 +365,15 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   {
     CUtensorMap ta, tb;
     const int bn = bn_for(d);
-    if (!make_tmap(&ta, c_buf, act_f32, p, T, GEMM_BM) ||
-        !make_tmap(&tb, W->w_unpool, act_f32, p, d, bn))
+    if (!make_tmap(&ta, c_buf, k_proj, p, T, GEMM_BM) ||
+        !make_tmap(&tb, W->w_unpool, k_proj, p, d, bn))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = d; P.K = p; P.bn = bn; P.groups = 0;
     P.out = out; P.ld_out = d; P.out_fmt = c.out == MOE_F32 ? OUT_F32 : OUT_BF16;
     const int grid = std::min(sms, mtiles * (d / bn));
-    if (act_f32) MOE_TRY((launch_gemm<true, EPI_STORE>(ta, tb, P, grid, st)));
-    else MOE_TRY((launch_gemm<false, EPI_STORE>(ta, tb, P, grid, st)));
+    if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
+    else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
   }
   E.mark(8);
   return MOE_OK;
@@ -402,8 +404,8 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which) {
     case 0: return size_t(c.E) * c.d * 4;
     case 1: return size_t(c.E) * 2 * c.I * c.p * ee;
     case 2: return c.expert == MOE_F32 ? size_t(c.E) * c.p * c.I * ee : 0;
-    case 3: return c.act == MOE_F32 ? size_t(c.p) * c.d * ea : 0;
-    case 4: return c.act == MOE_F32 ? size_t(c.d) * c.p * ea : 0;
+    case 3: return size_t(c.p) * c.d * ea;
+    case 4: return size_t(c.d) * c.p * ea;
     default: return 0;
   }
 }
@@ -414,35 +416,33 @@ moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weigh
   MOE_TRY(validate(cfg));
   const moe_config_t& c = *cfg;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (!src || !src->w_router || !src->w_gate || !src->w_up || !w_router_out || !w13_out)
-    return MOE_ERR_INVALID_ARG;
-  const void* ptrs[] = {src->w_router, src->w_gate, src->w_up, w_router_out, w13_out};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
   const bool act_f32 = c.act == MOE_F32, exp_f32 = c.expert == MOE_F32;
-  if (exp_f32 && (!src->w_down || !w2_out || !aligned16(w2_out))) return MOE_ERR_INVALID_ARG;
-  if (act_f32 && (!src->w_pool || !src->w_unpool || !w_pool_out || !w_unpool_out ||
-                  !aligned16(w_pool_out) || !aligned16(w_unpool_out)))
+  if (!src) return MOE_ERR_INVALID_ARG;
+  const void* need[] = {src->w_router, src->w_gate, src->w_up, src->w_pool, src->w_unpool,
+                        w_router_out, w13_out, w_pool_out, w_unpool_out};
+  for (const void* p : need)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (exp_f32 && (!src->w_down || !w2_out || !aligned16(src->w_down) || !aligned16(w2_out)))
     return MOE_ERR_INVALID_ARG;
-  auto round = [&](const void* s, void* d, size_t n) {
-    const size_t n4 = n / 4;
-    const int grid = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 4096));
-    round_tf32_kernel<<<grid, 256, 0, st>>>(static_cast<const float*>(s), static_cast<float*>(d), n4);
+  auto copy = [&](const void* s, void* d, size_t bytes, bool tf32) {
+    const size_t n16 = bytes / 16;
+    const int grid = static_cast<int>(std::min<size_t>((n16 + 255) / 256, 8192));
+    if (tf32) convert_copy_kernel<CONV_TF32><<<grid, 256, 0, st>>>(s, d, n16);
+    else convert_copy_kernel<CONV_BF16_TO_F16><<<grid, 256, 0, st>>>(s, d, n16);
     return last_launch();
   };
-  MOE_TRY(round(src->w_router, w_router_out, size_t(c.E) * c.d));
+  MOE_TRY(copy(src->w_router, w_router_out, size_t(c.E) * c.d * 4, true));
   const int es = exp_f32 ? 4 : 2;
   const unsigned rows13 = static_cast<unsigned>(c.E) * 2u * c.I;
   if (exp_f32)
-    pack_w13_kernel<true><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
+    pack_w13_kernel<CONV_TF32><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
   else
-    pack_w13_kernel<false><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
+    pack_w13_kernel<CONV_BF16_TO_F16><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
   MOE_TRY(last_launch());
-  if (exp_f32) MOE_TRY(round(src->w_down, w2_out, size_t(c.E) * c.p * c.I));
-  if (act_f32) {
-    MOE_TRY(round(src->w_pool, w_pool_out, size_t(c.p) * c.d));
-    MOE_TRY(round(src->w_unpool, w_unpool_out, size_t(c.d) * c.p));
-  }
+  if (exp_f32) MOE_TRY(copy(src->w_down, w2_out, size_t(c.E) * c.p * c.I * 4, true));
+  const size_t ea = act_f32 ? 4 : 2;
+  MOE_TRY(copy(src->w_pool, w_pool_out, size_t(c.p) * c.d * ea, act_f32));
+  MOE_TRY(copy(src->w_unpool, w_unpool_out, size_t(c.d) * c.p * ea, act_f32));
   return MOE_OK;
 }
 

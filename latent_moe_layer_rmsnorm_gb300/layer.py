@@ -57,10 +57,11 @@ class LatentMoE:
             es = torch.tensor([], dtype=dtype).element_size()
             return torch.empty(n // es, dtype=dtype, device=dev)
 
-        act = _TORCH[shape.act]
+        # packed operand dtypes: FP16 for BF16 configurations, FP32 (TF32-rounded) else
+        op = torch.float32 if shape.act == "f32" else torch.float16
         self.w_router = buf(L.PACK_ROUTER, torch.float32)
-        self.w13 = buf(L.PACK_W13, act)
-        w2p, poolp, unpoolp = buf(L.PACK_W2, act), buf(L.PACK_POOL, act), buf(L.PACK_UNPOOL, act)
+        self.w13 = buf(L.PACK_W13, op)
+        w2p, poolp, unpoolp = buf(L.PACK_W2, op), buf(L.PACK_POOL, op), buf(L.PACK_UNPOOL, op)
         src = L.moe_canonical_weights_t(
             w_router=_ptr(w["w_router"]), w_pool=_ptr(w["w_pool"]), w_gate=_ptr(w["w_gate"]),
             w_up=_ptr(w["w_up"]), w_down=_ptr(w["w_down"]), w_unpool=_ptr(w["w_unpool"]))
@@ -140,13 +141,15 @@ class LatentMoE:
     def intermediate(self, name: str, T: int) -> torch.Tensor:
         """Copy of one workspace intermediate after a call with T tokens (for tests)."""
         sh, k = self.shape, self.shape.top_k
-        act, exp = _TORCH[sh.act], _TORCH[sh.expert]
-        spec = {"h32": ((T, sh.d), torch.float32), "h16": ((T, sh.d), torch.bfloat16),
+        f32 = sh.act == "f32"
+        op = torch.float32 if f32 else torch.float16
+        spec = {"h32": ((T, sh.d), torch.float32), "h16": ((T, sh.d), torch.float16),
                 "ids": ((T, k), torch.int32), "w": ((T, k), torch.float32),
                 "pooled": ((T, sh.p), torch.float32), "row_off": ((sh.E + 1,), torch.int32),
                 "src": ((T * k,), torch.int32), "inv": ((T * k,), torch.int32),
-                "a_perm": ((T * k, sh.p), exp), "s": ((T * k, sh.I), exp),
-                "y": ((T * k, sh.p), exp), "c": ((T, sh.p), act)}
+                "a_perm": ((T * k, sh.p), op),
+                "s": ((T * k, sh.I), torch.float32 if f32 else torch.bfloat16),
+                "y": ((T * k, sh.p), torch.float32), "c": ((T, sh.p), op)}
         shape, dtype = spec[name]
         off = L.moe_workspace_offsets(self.config(T))[name] + self.ws_off
         n = 1

@@ -4,10 +4,10 @@ Only `tests/`, the package smoke check and the benchmark's CPU-baseline leg may
 import this package; the library never does.
 """
 from .moe_oracle import (moe_forward, route, rmsnorm, router_logits, topk_route,
-                         route_margin, expert_swiglu, expert_down, silu,
-                         storage_kinds)
+                         route_margin, expert_swiglu, expert_down, silu, pool, unpool,
+                         combine, storage_kinds, store)
 from . import formats
 
 __all__ = ["moe_forward", "route", "rmsnorm", "router_logits", "topk_route",
-           "route_margin", "expert_swiglu", "expert_down", "silu", "storage_kinds",
-           "formats"]
+           "route_margin", "expert_swiglu", "expert_down", "silu", "pool", "unpool",
+           "combine", "storage_kinds", "store", "formats"]

@@ -12,6 +12,8 @@ Definitions followed:
   GPU path converts with round-to-nearest, ties AWAY from zero (`cvt.rna.tf32.f32`),
   which is the rounding the oracle mirrors.
 * FP32: IEEE binary32, round to nearest even (numpy's cast).
+* FP16: IEEE binary16 (11 significant bits, subnormals 2^-24 apart below 2^-14),
+  round to nearest even (numpy's cast from float64).
 * E2M1 (FP4): sign + 2-bit exponent + 1-bit mantissa, magnitudes
   {0, 0.5, 1, 1.5, 2, 3, 4, 6}; NVFP4 encodes by round-to-nearest-even on that
   grid, saturating at 6.  ("SGLang and Miles Add Day-0 Support for Muse Spark
@@ -52,6 +54,11 @@ def bf16(x) -> np.ndarray:
 def fp32(x) -> np.ndarray:
     """Round to IEEE binary32 (nearest even)."""
     return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float64)
+
+
+def fp16(x) -> np.ndarray:
+    """Round to IEEE binary16 (nearest even)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
 
 
 def tf32_rna(x) -> np.ndarray:

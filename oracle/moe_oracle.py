@@ -32,11 +32,13 @@ Two modes:
   norm's FP32 output, and the routing decision must be taken in the precision
   the kernel uses.
 * chain=True ("precision chain", the parity gate): float64 arithmetic, with every
-  value rounded where the GPU path stores it (see `_store`): h (FP32 for the
-  router, BF16 or TF32 for the pooler), pooled (FP32), u, s, y, c (BF16, or
-  TF32/FP32 in FP32 mode) and out.  The page fixes the FP32 route-weighted sum
-  and the BF16 values the per-expert norm is taken on; the other storage types
-  are the kernel's.
+  value rounded where the GPU path stores it (see `storage_kinds`): h (FP32 for
+  the router; FP16, or TF32 in FP32 mode, for the pooler), pooled (FP32), u and c
+  (FP16 / TF32), s (BF16 / TF32), y (FP32: the expert outputs only feed the
+  per-expert norm, so they keep accumulator precision) and out; the weights meet
+  the GEMMs in the same formats (FP16 copies of the pooler, gate/up and unpooler
+  weights).  The page fixes the FP32 route-weighted sum; the storage types are the
+  kernel's.
 
 Readings of points the pages leave open (each is also listed with the design
 notes): softmax over all E logits, top-k, renormalised (= softmax over the k
@@ -64,9 +66,14 @@ def _store(v: np.ndarray, kind: str) -> np.ndarray:
         return F.fp32(v)
     if kind == "bf16":
         return F.bf16(v)
+    if kind == "f16":
+        return F.fp16(v)
     if kind == "tf32":          # FP32 storage, pre-rounded for a TF32 MMA operand
         return F.tf32_rna(F.fp32(v))
     raise ValueError(kind)
+
+
+store = _store
 
 
 def as_f64(a) -> np.ndarray:
@@ -139,25 +146,53 @@ def expert_down(s: np.ndarray, w_down_e) -> np.ndarray:
     return s @ as_f64(w_down_e).T
 
 
+def pool(h: np.ndarray, w_pool) -> np.ndarray:
+    """pooled = W_pool h for rows h [n, d]; W_pool is [p, d] (the pooler, 8192 -> 4096)."""
+    return as_f64(h) @ as_f64(w_pool).T
+
+
+def unpool(c: np.ndarray, w_unpool) -> np.ndarray:
+    """out = W_unpool c for rows c [n, p]; W_unpool is [d, p] (the unpooler)."""
+    return as_f64(c) @ as_f64(w_unpool).T
+
+
+def combine(y: np.ndarray, ids: np.ndarray, wts: np.ndarray, g_exp, eps: float) -> np.ndarray:
+    """c_t = sum_j w_tj * RMSNorm_{g_exp[e_tj]}(y_tj), summed in slot order j = 0..k-1.
+
+    y is [n, k, p] (slot j of token t = output of expert ids[t, j]).  Each expert
+    output is normalised with its own gain before the weighting (the page's
+    per-expert RMSNorm before the routing-weighted sum).
+    """
+    g_exp = as_f64(g_exp)
+    n, k, p = y.shape
+    c = np.zeros((n, p))
+    for j in range(k):
+        c = c + as_f64(wts)[:, j: j + 1] * rmsnorm(y[:, j], g_exp[np.asarray(ids)[:, j]], eps)
+    return c
+
+
 # ---- the layer ---------------------------------------------------------------------
 
 def storage_kinds(act: str, expert: str, out: str, chain: bool) -> dict:
     """Where the GPU path stores each intermediate, as `_store` kinds."""
     if not chain:
         return dict(h_pool="f64", pooled="f64", u="f64", s="f64", y="f64", c="f64",
-                    out="f64", w_proj="f64", w_exp="f64")
+                    out="f64", w_proj="f64", w_gate_up="f64", w_down="f64")
     tc = act == "f32"            # FP32 activations run their GEMMs on TF32 operands
     te = expert == "f32"
+    # BF16 configurations: the norm-bounded GEMM operands h, u, c (and the weights they
+    # meet: pooler, gate/up, unpooler) are FP16; s and the down weights stay BF16.
     return dict(
-        h_pool="tf32" if tc else "bf16",
+        h_pool="tf32" if tc else "f16",
         pooled="f32",
-        u="tf32" if te else "bf16",
+        u="tf32" if te else "f16",
         s="tf32" if te else "bf16",
-        y="f32" if te else "bf16",
-        c="tf32" if tc else "bf16",
+        y="f32",                              # expert outputs are kept in FP32
+        c="tf32" if tc else "f16",
         out=out,
-        w_proj="tf32" if tc else "f64",      # BF16 weights are exact as given
-        w_exp="tf32" if te else "f64",
+        w_proj="tf32" if tc else "f16",
+        w_gate_up="tf32" if te else "f16",
+        w_down="tf32" if te else "f64",       # BF16 weights are exact as given
     )
 
 
@@ -195,7 +230,7 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
 
     h_pool = _store(F.fp32(h) if chain else h, st["h_pool"])
     w_pool = _store(as_f64(inp["w_pool"]), st["w_proj"])
-    pooled = _store(h_pool @ w_pool.T, st["pooled"])
+    pooled = _store(pool(h_pool, w_pool), st["pooled"])
     u = _store(rmsnorm(pooled, inp["g_pool"], eps), st["u"])
 
     p = u.shape[1]
@@ -204,9 +239,9 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
     s_all = None
     for e in np.unique(ids):
         rows, slots = np.nonzero(ids == e)
-        wg = _store(as_f64(inp["w_gate"][e]), st["w_exp"])
-        wu = _store(as_f64(inp["w_up"][e]), st["w_exp"])
-        wd = _store(as_f64(inp["w_down"][e]), st["w_exp"])
+        wg = _store(as_f64(inp["w_gate"][e]), st["w_gate_up"])
+        wu = _store(as_f64(inp["w_up"][e]), st["w_gate_up"])
+        wd = _store(as_f64(inp["w_down"][e]), st["w_down"])
         s = _store(expert_swiglu(u[rows], wg, wu), st["s"])
         if return_parts:
             if s_all is None:
@@ -214,18 +249,16 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
             s_all[rows, slots] = s
         y_all[rows, slots] = _store(expert_down(s, wd), st["y"])
 
-    c = np.zeros((n, p))
     if not norm_after_sum:
-        for j in range(top_k):     # the route-weighted sum, in slot order
-            yn = rmsnorm(y_all[:, j], g_exp[ids[:, j]], eps)
-            c = c + wts[:, j: j + 1] * yn
+        c = combine(y_all, ids, wts, g_exp, eps)
     else:
+        c = np.zeros((n, p))
         for j in range(top_k):
             c = c + wts[:, j: j + 1] * y_all[:, j]
         c = rmsnorm(c, np.ones(p), eps)
     c = _store(c, st["c"])
     w_unpool = _store(as_f64(inp["w_unpool"]), st["w_proj"])
-    res = _store(c @ w_unpool.T, st["out"])
+    res = _store(unpool(c, w_unpool), st["out"])
     if not return_parts:
         return res
     return dict(out=res, h=h, logits=logits, ids=ids, w=wts, pooled=pooled, u=u,

@@ -71,3 +71,15 @@ def test_ue4m3_rounding():
     assert F.ue4m3_encode(np.array([1.07]))[0] == 0x39
     assert F.ue4m3_encode(np.array([1e9]))[0] == 0x7E
     assert F.ue4m3_encode(np.array([-1.0]))[0] == 0
+
+
+def test_fp16_matches_torch_cast():
+    rng = np.random.default_rng(3)
+    v = np.concatenate([rng.normal(size=20000) * 10.0 ** rng.integers(-9, 4, 20000),
+                        [0.0, 1.0, 65504.0, 2.0 ** -24, 3 * 2.0 ** -26]]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.float16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(F.fp16(v.astype(np.float64)), ref.astype(np.float64))
+    # bf16 values of ordinary magnitude are exact in fp16 (3 more significand bits)
+    b = F.bf16(rng.normal(size=5000) * 0.02)
+    big = np.abs(b) >= 2.0 ** -17
+    np.testing.assert_array_equal(F.fp16(b)[big], b[big])

@@ -17,16 +17,40 @@ from latent_moe_layer_rmsnorm_gb300 import synth
 
 pytestmark = pytest.mark.gpu
 
-# BF16 storage: outputs agree with the rounding-chain oracle to a few BF16 units of
-# the intermediates; 1e-2 is the benchmark spec's bound.  Measured values are printed.
+# ---- tolerances, each derived from the arithmetic ------------------------------------
+#
+# Both sides round at the same storage points, so a stored GPU value equals the
+# oracle's unless an FP32-vs-FP64 accumulation difference (~1e-6 relative) puts the
+# two on different sides of a rounding boundary: the values then differ by exactly
+# one unit of the storage format (BF16: 2^-8 of the value, TF32: 2^-11), for a small
+# fraction of elements.  Stage-wise checks (each stage fed the GPU's own input) use
+# exactly that criterion.
+#
+# End to end, those one-unit flips propagate.  The largest effect is a flipped
+# element of c going through the unpooler: it moves an output by up to
+# max|W_unpool| * unit(c) ~ (4/sqrt(p)) * 2^-8 * max|c|.  At p >= 1024 a handful of
+# such flips stays well inside the benchmark spec's bound 1e-2 * rms(out); at the narrow
+# test widths (p = 128, 256) one flip alone is 4e-3 .. 6e-3 of rms, so those shapes
+# get 3e-2.
 TOL_BF16 = 1e-2
-# FP32 storage with TF32 GEMM operands (both sides round at the same points): the
-# residual is FP32-vs-FP64 accumulation plus rare TF32 rounding flips, ~1e-4.
-TOL_F32 = 2e-3
+TOL_NARROW = 3e-2
+# FP32 storage with TF32 operands: one TF32 unit is 2^-10 of a value (ties-away
+# rounding moves by a full unit); stored values reach ~5x rms: 5e-3.
+TOL_F32 = 5e-3
+# FP32-stored results of one GEMM (pooled, FP32 out): only the summation order
+# differs; |error| <= sqrt(K) * 2^-24 * |terms| in practice, far below 5e-5 * rms.
+TOL_F32_SUM = 5e-5
+# Route weights: one TF32 flip of a router operand element moves a logit by
+# 2^-10 * |h_i| * |W_r[e,i]| <= 2^-10 * 6 * 0.25 (d = 256) and a weight by at most a
+# quarter of that: 4e-4.  Routing decisions have 1e-3 margins, above that noise.
+TOL_W = 5e-4
+MAX_FLIP_FRACTION = 0.01
 
 TINY_BF16 = synth.TINY_F32.replace(name="tiny_bf16", act="bf16", expert="bf16")
-MID_BF16 = synth.Shape("mid_bf16", T=300, d=512, p=256, E=16, top_k=4, I=384)
-SHAPES = {"tiny_f32": synth.TINY_F32, "tiny_bf16": TINY_BF16, "mid_bf16": MID_BF16}
+NARROW_BF16 = synth.Shape("narrow_bf16", T=300, d=512, p=256, E=16, top_k=4, I=384)
+MID_BF16 = synth.Shape("mid_bf16", T=300, d=1024, p=1024, E=16, top_k=4, I=512)
+SHAPES = {"tiny_f32": synth.TINY_F32, "tiny_bf16": TINY_BF16, "narrow_bf16": NARROW_BF16,
+          "mid_bf16": MID_BF16}
 
 
 def need_gpu():
@@ -49,7 +73,47 @@ def gpu_layer(shape, inp, out="f32"):
 
 
 def tol_for(shape):
-    return TOL_F32 if shape.act == "f32" else TOL_BF16
+    if shape.act == "f32":
+        return TOL_F32
+    return TOL_BF16 if shape.p >= 1024 else TOL_NARROW
+
+
+def unit(v, kind):
+    """One unit in the last place of the storage format at |v| (v != 0)."""
+    bits = {"bf16": 7, "tf32": 10, "f16": 10}[kind]
+    a = np.maximum(np.abs(np.asarray(v, np.float64)), 1e-30)
+    u = np.exp2(np.floor(np.log2(a)) - bits)
+    if kind == "f16":
+        u = np.maximum(u, 2.0 ** -24)      # subnormal spacing
+    return u
+
+
+# Values near zero that come out of a cancellation (silu(a) * b with a ~ 0) carry
+# the FP32 accumulation noise of their GEMM in absolute terms: ~sqrt(K) * 2^-24 of
+# the accumulated magnitudes, below 3e-5 of the stage's rms.
+ATOL_NOISE = 3e-5
+
+
+def assert_one_unit(name, gpu, ref, kind):
+    """Equal, or one storage unit apart (plus the accumulation-noise floor), and
+    rarely apart."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    d = np.abs(gpu - ref)
+    u = unit(np.maximum(np.abs(gpu), np.abs(ref)), kind)
+    floor = ATOL_NOISE * float(np.sqrt(np.mean(ref * ref)))
+    bad = d > u * (1 + 1e-9) + floor
+    assert not np.any(bad), (name, int(bad.sum()), float(d[bad].max()))
+    frac = float(np.mean(d > 0))
+    assert frac <= MAX_FLIP_FRACTION, (name, frac)
+    return frac
+
+
+def assert_sum_close(name, gpu, ref):
+    ref = np.asarray(ref, np.float64)
+    e = rel_err(gpu, ref)
+    assert e <= TOL_F32_SUM, (name, e)
+    return e
 
 
 def check_dispatch(layer, T, ids):
@@ -72,13 +136,57 @@ def check_dispatch(layer, T, ids):
     return src
 
 
+def check_stagewise(layer, view, shape, T, ids, w, out):
+    """Each stage recomputed by the oracle from the GPU's own stored input of that stage."""
+    k = shape.top_k
+    f32 = shape.act == "f32"
+    st = oracle.storage_kinds(shape.act, shape.expert, "f32", True)
+
+    def wconv(a, kind):
+        return oracle.store(np.asarray(a, np.float64), kind)
+    src = layer.intermediate("src", T).cpu().numpy().astype(np.int64)
+    inv = layer.intermediate("inv", T).cpu().numpy().astype(np.int64).reshape(T, k)
+    h_in = to_np(layer.intermediate("h32" if f32 else "h16", T))
+    pooled = to_np(layer.intermediate("pooled", T))
+    u = to_np(layer.intermediate("a_perm", T))
+    s = to_np(layer.intermediate("s", T))
+    y = to_np(layer.intermediate("y", T))
+    c = to_np(layer.intermediate("c", T))
+    rep = {}
+    rep["pooled"] = assert_sum_close(
+        "pooled", pooled,
+        oracle.store(oracle.pool(h_in, wconv(view["w_pool"], st["w_proj"])), "f32"))
+    u_ref = oracle.store(oracle.rmsnorm(pooled, view["g_pool"], shape.eps), st["u"])
+    rep["u"] = assert_one_unit("u", u, u_ref[src // k], st["u"])
+    e_of_row = ids.reshape(-1)[src]
+    s_ref = np.zeros(s.shape)
+    y_ref = np.zeros(y.shape)
+    for e in np.unique(e_of_row):
+        rows = np.nonzero(e_of_row == e)[0]
+        s_ref[rows] = oracle.store(
+            oracle.expert_swiglu(u[rows].astype(np.float64), wconv(view["w_gate"][e], st["w_gate_up"]),
+                                 wconv(view["w_up"][e], st["w_gate_up"])), st["s"])
+        y_ref[rows] = oracle.store(
+            oracle.expert_down(s[rows].astype(np.float64), wconv(view["w_down"][e], st["w_down"])),
+            st["y"])
+    rep["s"] = assert_one_unit("s", s, s_ref, st["s"])
+    rep["y"] = assert_sum_close("y", y, y_ref)             # y is stored in FP32
+    y_slots = y[inv].astype(np.float64)                    # [T, k, p]
+    c_ref = oracle.store(oracle.combine(y_slots, ids, np.asarray(w, np.float64), view["g_exp"],
+                                        shape.eps), st["c"])
+    rep["c"] = assert_one_unit("c", c, c_ref, st["c"])
+    rep["out"] = assert_sum_close(
+        "out", to_np(out), oracle.store(oracle.unpool(c, wconv(view["w_unpool"], st["w_proj"])), "f32"))
+    return rep
+
+
 @pytest.mark.parametrize("name", list(SHAPES))
 def test_layer_matches_oracle(name):
     need_gpu()
     shape = SHAPES[name]
     inp = make_case(shape)
-    ref = oracle.moe_forward(oracle_view(inp), **oracle_kwargs(shape, "f32"), chain=True,
-                             return_parts=True)
+    view = oracle_view(inp)
+    ref = oracle.moe_forward(view, **oracle_kwargs(shape, "f32"), chain=True, return_parts=True)
     layer, dev = gpu_layer(shape, inp, out="f32")
     T, k = shape.T, shape.top_k
     out = layer.forward(dev["x"])
@@ -86,24 +194,18 @@ def test_layer_matches_oracle(name):
     assert layer.read_status() == (0, 0)
 
     ids = layer.intermediate("ids", T).cpu().numpy()
+    w = to_np(layer.intermediate("w", T))
     np.testing.assert_array_equal(ids, ref["ids"])
-    np.testing.assert_allclose(to_np(layer.intermediate("w", T)), ref["w"], rtol=0, atol=2e-6)
-    src = check_dispatch(layer, T, ids)
-    tok, slot = src // k, src % k
-
-    errs = {}
-    errs["pooled"] = rel_err(to_np(layer.intermediate("pooled", T)), ref["pooled"])
-    errs["u"] = rel_err(to_np(layer.intermediate("a_perm", T)), ref["u"][tok])
-    errs["s"] = rel_err(to_np(layer.intermediate("s", T)), ref["s"][tok, slot])
-    errs["y"] = rel_err(to_np(layer.intermediate("y", T)), ref["y"][tok, slot])
-    errs["c"] = rel_err(to_np(layer.intermediate("c", T)), ref["c"])
-    errs["out"] = rel_err(to_np(out), ref["out"])
-    print(name, {k_: f"{v:.2e}" for k_, v in errs.items()})
-    for stage, e in errs.items():
-        assert e <= tol_for(shape), (stage, e, errs)
+    np.testing.assert_allclose(w, ref["w"], rtol=0, atol=TOL_W)
+    np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-6)
+    check_dispatch(layer, T, ids)
+    stages = check_stagewise(layer, view, shape, T, ids, w, out)
+    e2e = rel_err(to_np(out), ref["out"])
+    print(name, "stage-wise", {k_: f"{v:.1e}" for k_, v in stages.items()}, f"e2e {e2e:.2e}")
+    assert e2e <= tol_for(shape), e2e
 
 
-@pytest.mark.parametrize("name", ["tiny_bf16", "mid_bf16", "tiny_f32"])
+@pytest.mark.parametrize("name", ["tiny_bf16", "narrow_bf16", "tiny_f32"])
 @pytest.mark.parametrize("T", [1, 63, 65, 129])
 def test_ragged_token_counts(name, T):
     need_gpu()
@@ -117,8 +219,9 @@ def test_ragged_token_counts(name, T):
     torch.cuda.synchronize()
     assert layer.read_status() == (0, 0)
     np.testing.assert_array_equal(ids.cpu().numpy(), ref["ids"])
-    np.testing.assert_allclose(to_np(w), ref["w"], rtol=0, atol=2e-6)
+    np.testing.assert_allclose(to_np(w), ref["w"], rtol=0, atol=TOL_W)
     assert out.shape == (T, shape.d)      # the pooler keeps the token count
+    check_stagewise(layer, oracle_view(inp), shape, T, ids.cpu().numpy(), to_np(w), out)
     assert rel_err(to_np(out), ref["out"]) <= tol_for(shape)
 
 
@@ -133,7 +236,7 @@ def test_bf16_output_mode():
     out = to_np(layer.forward(dev["x"]))
     rms = np.sqrt(np.mean(ref ** 2))
     ulp = np.abs(ref) * 2.0 ** -7
-    assert np.all(np.abs(out - ref) <= TOL_BF16 * rms + ulp)
+    assert np.all(np.abs(out - ref) <= tol_for(shape) * rms + ulp)
 
 
 def test_routing_replay_and_determinism():
@@ -165,7 +268,9 @@ def test_external_routes_match_oracle():
                              ids=ids.numpy(), weights=w.numpy().astype(np.float64))
     layer, dev = gpu_layer(shape, inp)
     out = layer.forward(dev["x"], ids=ids.cuda(), w=w.cuda())
-    assert rel_err(to_np(out), ref) <= TOL_BF16
+    torch.cuda.synchronize()
+    check_stagewise(layer, oracle_view(inp), shape, shape.T, ids.numpy(), w.numpy(), out)
+    assert rel_err(to_np(out), ref) <= tol_for(shape)
 
 
 def test_relabelling_is_bit_exact():
@@ -244,5 +349,7 @@ def test_empty_and_crowded_experts():
                              ids=ids.numpy(), weights=w.numpy().astype(np.float64))
     layer, dev = gpu_layer(shape, inp)
     out = layer.forward(dev["x"], ids=ids.cuda(), w=w.cuda())
-    assert rel_err(to_np(out), ref) <= TOL_BF16
+    torch.cuda.synchronize()
     check_dispatch(layer, T, ids.numpy())
+    check_stagewise(layer, oracle_view(inp), shape, T, ids.numpy(), w.numpy(), out)
+    assert rel_err(to_np(out), ref) <= tol_for(shape)
