@@ -167,6 +167,27 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* W, const vo
                        int32_t* ids, float* w, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
 
+/* moe_route for callers that cannot allocate device memory at all -- code running where
+ * no allocator is reachable, such as an engine that reserves all of its memory at start-up,
+ * a plugin host that forbids device allocations, or a replayed CUDA graph that must not
+ * grow its memory pool.  It takes no workspace: its scratch (status word, h32 and h16)
+ * lives in a fixed 12 MiB + 256 B array inside the library, which every GPU that loads the
+ * library holds until the process exits.  The pages describe nothing like it; it is an
+ * addition of this library.
+ *   Same arguments and results as moe_route, minus the workspace.
+ *   Limit: T * d <= 2^21 (e.g. T <= 256 at d = 8192); larger calls return
+ *   MOE_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address (once per device,
+ *   with that device current); make that first call before any stream capture.
+ *   No cudaMalloc, cudaFree or allocating library routine is called.
+ *   All calls share the one array, which keeps the previous call's contents (each call
+ *   clears the status word it needs at zero): calls that overlap on the GPU -- on
+ *   different streams, or from different threads -- race, so serialise them.
+ *   Device-side wait failures of these calls are recorded only in the array's status
+ *   word, which moe_read_status cannot reach. */
+moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                               int32_t* ids, float* w, moe_stream_t stream);
+
 /* The whole block for T tokens.
  *   x    [T,d] act dtype (device)
  *   ids, w  NULL: route internally.  Otherwise [T,k] int32 ids (each in [0,E)) and

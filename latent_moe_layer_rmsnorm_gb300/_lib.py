@@ -30,7 +30,8 @@ PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL = range(5)
 
 # every symbol the header declares
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_packed_bytes", "moe_pack_weights",
-           "moe_route", "moe_forward", "moe_forward_profiled", "moe_num_stages",
+           "moe_route", "moe_route_noalloc", "moe_forward", "moe_forward_profiled",
+           "moe_num_stages",
            "moe_stage_name", "moe_forward_launches", "moe_workspace_offsets",
            "moe_read_status", "moe_status_string")
 
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
     L.moe_pack_weights.restype = i32
     L.moe_route.argtypes = [cfgp, wp, vp, vp, vp, vp, sz, vp]
     L.moe_route.restype = i32
+    L.moe_route_noalloc.argtypes = [cfgp, wp, vp, vp, vp, vp]
+    L.moe_route_noalloc.restype = i32
     L.moe_forward.argtypes = [cfgp, wp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_forward.restype = i32
     L.moe_forward_profiled.argtypes = [cfgp, wp, vp, vp, vp, vp, vp, sz, vp,
@@ -137,6 +140,10 @@ def moe_pack_weights(cfg, src: moe_canonical_weights_t, w_router_out, w13_out, w
 
 def moe_route(cfg, W: moe_weights_t, x, ids, w, ws, ws_bytes, stream) -> int:
     return int(lib().moe_route(ctypes.byref(cfg), _ref(W), x, ids, w, ws, ws_bytes, stream))
+
+
+def moe_route_noalloc(cfg, W: moe_weights_t, x, ids, w, stream) -> int:
+    return int(lib().moe_route_noalloc(ctypes.byref(cfg), _ref(W), x, ids, w, stream))
 
 
 def moe_forward(cfg, W: moe_weights_t, x, ids, w, out, ws, ws_bytes, stream) -> int:

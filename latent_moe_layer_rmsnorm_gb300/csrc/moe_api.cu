@@ -379,6 +379,44 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   return MOE_OK;
 }
 
+// ---- routing without caller-provided scratch ---------------------------------------------
+// Some callers cannot hand the library a workspace: code that runs where no allocator is
+// reachable (an engine whose memory is fully reserved up front, a plugin host that
+// forbids device allocations after start-up, a replayed CUDA graph that must not grow
+// its pool).  moe_route_noalloc serves them from this file-scope array instead.  Every
+// GPU that loads the library keeps it until the process exits, so it is kept small:
+// status word, then h32 [T,d] FP32 and h16 [T,d] FP16 for T * d <= NOALLOC_MAX_ELEMS.
+constexpr size_t NOALLOC_MAX_ELEMS = size_t(1) << 21;   // e.g. T = 256 at d = 8192
+constexpr size_t NOALLOC_H32_OFF = 256;
+constexpr size_t NOALLOC_H16_OFF = NOALLOC_H32_OFF + NOALLOC_MAX_ELEMS * 4;
+constexpr size_t NOALLOC_BYTES = NOALLOC_H16_OFF + NOALLOC_MAX_ELEMS * 2;   // 12 MiB + 256
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+struct NoAllocDev {
+  void* ptr = nullptr;
+  bool ready = false;
+};
+NoAllocDev g_noalloc_dev[64];
+std::mutex g_noalloc_mu;
+
+// Device address of the array on the current device, looked up once per device.  In host
+// code the array's name only stands for it; the kernels must get this address.
+moe_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocDev& D = g_noalloc_dev[dev];
+  if (!D.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    D.ptr = p;
+    D.ready = true;
+  }
+  *out = D.ptr;
+  return MOE_OK;
+}
+
 }  // namespace
 
 // =====================================================================================
@@ -451,6 +489,43 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* W, const vo
                        moe_stream_t stream) {
   return run_layer(cfg, W, x, nullptr, nullptr, nullptr, ids, w, true, ws, ws_bytes,
                    reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
+}
+
+moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
+                               int32_t* ids, float* w, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config_t& c = *cfg;
+  if (static_cast<size_t>(c.T) * c.d > NOALLOC_MAX_ELEMS) return MOE_ERR_WORKSPACE;
+  MOE_TRY(check_weights(c, W, true, true));
+  if (!x || !aligned16(x) || !ids || !w) return MOE_ERR_INVALID_ARG;
+  if (c.T == 0) return MOE_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int sms = 0;
+  MOE_TRY(device_ready(&sms));
+  void* scratch = nullptr;
+  MOE_TRY(noalloc_scratch(&scratch));
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  int* status = reinterpret_cast<int*>(base);
+  float* h32 = reinterpret_cast<float*>(base + NOALLOC_H32_OFF);
+  __half* h16 = reinterpret_cast<__half*>(base + NOALLOC_H16_OFF);
+  // the array keeps the previous call's contents: the status word must start at zero
+  clear_status_kernel<<<1, 32, 0, st>>>(status);
+  MOE_TRY(last_launch());
+  if (c.act == MOE_F32)
+    norm_in_kernel<true><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, c.d, c.eps);
+  else
+    norm_in_kernel<false><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, h16, c.d, c.eps);
+  MOE_TRY(last_launch());
+  const int bn = (c.E + 15) / 16 * 16;
+  CUtensorMap ta, tb;
+  if (!make_tmap(&ta, h32, OP_TF32, c.d, c.T, GEMM_BM) ||
+      !make_tmap(&tb, W->w_router, OP_TF32, c.d, c.E, bn))
+    return MOE_ERR_CUDA;
+  GemmParams P = base_params(status, c.flags);
+  P.M = c.T; P.N = bn; P.K = c.d; P.bn = bn; P.groups = 0;
+  P.E = c.E; P.top_k = c.top_k; P.ids = ids; P.wts = w;
+  const int mtiles = (c.T + GEMM_BM - 1) / GEMM_BM;
+  return launch_gemm<OP_TF32, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st);
 }
 
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
