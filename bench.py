@@ -74,7 +74,7 @@ def bytes_per_token(s, act_bytes=2) -> dict:
     return {
         "norm": s.d * act_bytes + s.d * 4 + s.d * act_bytes,            # x in; h32, h16 out
         "dispatch": s.p * 4 + k * s.p * act_bytes + 16 * k,             # pooled in; k rows out
-        "combine": k * s.p * act_bytes + s.p * act_bytes + 8 * k,       # k rows in; c out
+        "combine": k * s.p * 4 + s.p * act_bytes + 8 * k,               # k FP32 rows in; c out
     }
 
 
@@ -152,6 +152,24 @@ def recorded_traffic(workload: str, kernel: str):
     return float(m.group(1))
 
 
+# ---- ranks ----------------------------------------------------------------------------------
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling over independent token batches)."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(v: float, device) -> float:
+    """The job's elapsed time is the slowest rank's (no-op for one process)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---- our arm -----------------------------------------------------------------------------
 
 def run_ours(args):
@@ -174,7 +192,7 @@ def run_ours(args):
     shape = synth.WORKLOADS[args.workload]
     if shape.expert == "nvfp4":
         raise SystemExit("the NVFP4 workload is not available in this build")
-    seed = args.seed + 1000 * rank             # each rank: its own batch
+    seed = rank_seed(args.seed, rank)
     inp = synth.make_inputs(shape, seed=seed, device="cuda")
     out_kind = "bf16" if shape.act == "bf16" else "f32"
     layer = LatentMoE(shape, inp, out=out_kind, keep_canonical=False)
@@ -218,11 +236,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), "cuda")
     st = layer.read_status()
     if st != (0, 0):
         raise SystemExit(f"device status after the timed steps: {st}")
@@ -258,11 +272,7 @@ def run_ours(args):
             ho.copy_(out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            tt = torch.tensor([e2e_ms], device="cuda", dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), "cuda")
         e2e = {"value": T * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": x.numel() * x.element_size(),
                "d2h_bytes_per_step": out.numel() * out.element_size(),
@@ -329,47 +339,56 @@ def _oracle_cores():
         return os.cpu_count() or 1
 
 
-def cpu_baseline_from_gpu_inputs(shape, layer, x, seed, n_tokens=4):
-    """Time the oracle, as it stands, on n_tokens of the benchmark's own batch.  The
-    inputs (dense weights and the routed experts' matrices) are staged on the host
-    before the clock starts; the oracle's float64 conversion is timed."""
+def cpu_baseline_from_gpu_inputs(shape, layer, x, seed, n_groups=6, group=4):
+    """Time the oracle, as it stands, on n_groups x group tokens of the benchmark's own
+    batch.  Each group's inputs (dense weights and its routed experts' matrices) are
+    staged on the host before its clock starts, so host memory holds one group's
+    experts at a time; the oracle's float64 work (conversion included) is timed."""
     import numpy as np
     import torch
 
     import oracle
     from latent_moe_layer_rmsnorm_gb300 import synth
 
-    toks = list(range(0, shape.T, shape.T // n_tokens))[:n_tokens]
+    n_tok = n_groups * group
+    toks = [int(t) for t in np.linspace(0, shape.T - 1, n_tok).round()]
     dense = synth.make_dense(shape, seed=seed, device="cuda")
     view = {k: v.float().cpu().numpy() for k, v in dense.items()}
-    view["x"] = x[toks].float().cpu().numpy()
-    ids, _ = layer.route(x[toks].contiguous())
-    need = sorted(set(ids.cpu().numpy().reshape(-1).tolist()))
-    experts = {e: {k: v.float().cpu().numpy() for k, v in
-                   synth.make_expert(shape, seed, e, device="cuda").items()} for e in need}
+    del dense
+    total, n_exp = 0.0, 0
+    for g0 in range(0, n_tok, group):
+        tg = toks[g0: g0 + group]
+        view["x"] = x[tg].float().cpu().numpy()
+        ids, _ = layer.route(x[tg].contiguous())
+        need = sorted(set(ids.cpu().numpy().reshape(-1).tolist()))
+        n_exp += len(need)
+        experts = {e: {k: v.float().cpu().numpy() for k, v in
+                       synth.make_expert(shape, seed, e, device="cuda").items()} for e in need}
 
-    class Sparse:
-        def __init__(self, key):
-            self.key = key
+        class Sparse:
+            def __init__(self, key):
+                self.key = key
 
-        def __getitem__(self, e):
-            e = int(e)
-            if e not in experts:     # the oracle routed a token elsewhere than the GPU
-                experts[e] = {k: v.float().cpu().numpy() for k, v in
-                              synth.make_expert(shape, seed, e, device="cuda").items()}
-            return experts[e][self.key]
+            def __getitem__(self, e):
+                e = int(e)
+                if e not in experts:     # the oracle routed a token elsewhere than the GPU
+                    experts[e] = {k: v.float().cpu().numpy() for k, v in
+                                  synth.make_expert(shape, seed, e, device="cuda").items()}
+                return experts[e][self.key]
 
-    for key in ("w_gate", "w_up", "w_down"):
-        view[key] = Sparse(key)
-    t0 = time.perf_counter()
-    oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act=shape.act,
-                       expert=shape.expert, out="bf16", chain=True)
-    dt = time.perf_counter() - t0
-    del np
-    return {"value": round(len(toks) / dt, 4), "unit": "tokens/s", "cores": _oracle_cores(),
+        for key in ("w_gate", "w_up", "w_down"):
+            view[key] = Sparse(key)
+        t0 = time.perf_counter()
+        oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act=shape.act,
+                           expert=shape.expert, out="bf16", chain=True)
+        total += time.perf_counter() - t0
+        del experts
+    del np, torch
+    return {"value": round(n_tok / total, 4), "unit": "tokens/s", "cores": _oracle_cores(),
             "kind": "oracle",
-            "sample": f"{len(toks)} tokens of the {shape.name} batch ({len(need)} experts), "
-                      f"float64 numpy, {dt:.1f} s"}
+            "sample": f"{n_tok} tokens of the {shape.name} batch in groups of {group} "
+                      f"({n_exp} routed expert matrices staged per group), float64 numpy, "
+                      f"{total:.1f} s of oracle time"}
 
 
 def run_reference(args):

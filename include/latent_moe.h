@@ -2,9 +2,9 @@
  * latent_moe.h -- C ABI of the latent mixture-of-experts block on one GB300 (sm_103a).
  *
  * The block (from "SGLang and Miles Add Day-0 Support for Muse Spark Open", section
- * "MoE with Pooler, Unpooler and Per-Expert Normalization"; widths from "Muse Spark
- * Open Day-0 on vLLM", section "潜空间 MoE"; router precision from the same page's
- * "Nvidia" section):
+ * "MoE with Pooler, Unpooler and Per-Expert Normalization"; widths from "vLLM 对 Muse
+ * Spark Open 的 Day 0 支持" (vLLM Day-0 support), section "潜空间 MoE"; router precision
+ * from the same page's "Nvidia" section):
  *
  *   h_t   = RMSNorm_{g_in}(x_t)                         full-width norm        [T,d]
  *   l_t   = W_r h_t  (TF32 operands, FP32 accumulate)   router logits          [T,E]
@@ -147,7 +147,8 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which);
  * Open", section "Reading TensorRT-LLM's weights", describes the same need: the expert
  * GEMM reads gate and up rows of one tile together; this library uses its own layout).
  *  - w_router_out [E,d] FP32: w_router rounded to TF32 (ties away), the router's
- *    operand precision (the vLLM page's "Nvidia" section: TF32 router GEMM).
+ *    operand precision ("vLLM 对 Muse Spark Open 的 Day 0 支持", section "Nvidia":
+ *    a TF32 router GEMM fed by the norm's FP32 output).
  *  - w13_out: gate and up rows interleaved in blocks of G rows (G = 128), so one
  *    256-row tile of the gate/up GEMM holds gate rows i..i+G and the matching up rows;
  *    converted to FP16 (BF16 configs) or rounded to TF32 (FP32 configs).

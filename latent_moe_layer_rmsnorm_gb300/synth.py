@@ -7,7 +7,7 @@ step of the computation.
 
 Workloads follow the MoE-block description of "SGLang and Miles Add Day-0 Support
 for Muse Spark Open" (section "MoE with Pooler, Unpooler and Per-Expert
-Normalization") and the dimensions of "Muse Spark Open Day-0 on vLLM" (section
+Normalization") and the dimensions of "vLLM 对 Muse Spark Open 的 Day 0 支持" (vLLM Day-0 support for Muse Spark Open) (section
 "潜空间 MoE": pooler 8192 x 4096, 256 experts per layer):
 
 * activations x ~ N(0, 1)
@@ -60,8 +60,13 @@ PREFILL_NVFP4 = Shape("prefill_nvfp4", T=16384, d=8192, p=4096, E=256, top_k=8, 
 SKEWED_BF16 = Shape("skewed_bf16", T=8192, d=8192, p=4096, E=256, top_k=8, I=4096,
                     zipf_s=1.2)
 
+# A 1/16 slice of the prefill chunk with the same per-expert load (512 rows per expert)
+# and widths: small enough (~2 GB on the device) for full profiler captures.
+PREFILL_SLICE_BF16 = Shape("prefill_slice_bf16", T=1024, d=8192, p=4096, E=16, top_k=8,
+                           I=4096)
+
 WORKLOADS = {s.name: s for s in (TINY_F32, PREFILL_BF16, DECODE_BF16, PREFILL_NVFP4,
-                                 SKEWED_BF16)}
+                                 SKEWED_BF16, PREFILL_SLICE_BF16)}
 
 
 def storage_dtype(kind: str) -> torch.dtype:

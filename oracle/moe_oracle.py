@@ -6,7 +6,7 @@ this module imports nothing from the library.
 
 What it computes is the plain definition of the block, taken from "SGLang and Miles
 Add Day-0 Support for Muse Spark Open", section "MoE with Pooler, Unpooler and
-Per-Expert Normalization", with the widths of "Muse Spark Open Day-0 on vLLM",
+Per-Expert Normalization", with the widths of "vLLM 对 Muse Spark Open 的 Day 0 支持" (vLLM Day-0 support for Muse Spark Open),
 section "潜空间 MoE", and the router precision of the same page's "Nvidia" section:
 
     h_t   = RMSNorm_{g_in}(x_t)                       full-width norm
@@ -92,7 +92,7 @@ def rmsnorm(v: np.ndarray, g, eps: float) -> np.ndarray:
 def router_logits(h: np.ndarray, w_router) -> np.ndarray:
     """logits[t, e] = sum_i tf32(h[t, i]) * tf32(W_r[e, i]).
 
-    The Nvidia section of the vLLM page: the router GEMM is TF32, fed by the
+    "vLLM 对 Muse Spark Open 的 Day 0 支持", section "Nvidia": the router GEMM is TF32, fed by the
     norm's FP32 output.  h is first stored as FP32, then both operands are
     rounded to TF32; products and the sum are float64.
     """

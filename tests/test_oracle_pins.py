@@ -5,7 +5,7 @@ Muse Spark Open", section "MoE with Pooler, Unpooler and Per-Expert
 Normalization" (router on the full-width vector; pooled input normalised; every
 selected expert output normalised before its routing weight and the sum; the
 combined vector unpooled; the pooler keeps the token count; normalising the sum
-instead would change the result) and "Muse Spark Open Day-0 on vLLM", sections
+instead would change the result) and "vLLM 对 Muse Spark Open 的 Day 0 支持" (vLLM Day-0 support for Muse Spark Open), sections
 "潜空间 MoE" (shared pooler/unpooler, 8192 <-> 4096) and "Nvidia" (TF32 router GEMM
 on the norm's FP32 output).  Closed forms, invariances, brute force and library
 routines (scipy) supply the expected values.
