@@ -54,6 +54,7 @@ from __future__ import annotations
 import numpy as np
 
 from . import formats as F
+from . import nvfp4 as Q
 
 
 # ---- storage rounding --------------------------------------------------------------
@@ -196,6 +197,20 @@ def storage_kinds(act: str, expert: str, out: str, chain: bool) -> dict:
     )
 
 
+def nvfp4_expert_weights(w_gate_e, w_up_e, w_down_e):
+    """Quantise one expert as the library does: gate and up share one global scale
+    (they form one gate/up matrix), down has its own.  Returns dequantised float64
+    matrices and the quantised codes."""
+    gu = np.concatenate([as_f64(w_gate_e), as_f64(w_up_e)], axis=0).astype(np.float32)
+    g13 = Q.global_scale(np.max(np.abs(gu)))
+    q13, sf13 = Q.quantize_blocks(gu, g13)
+    d13 = Q.dequantize(q13, sf13, g13)
+    I = d13.shape[0] // 2
+    q2, sf2, g2 = Q.quantize_tensor(as_f64(w_down_e))
+    return dict(gate=d13[:I], up=d13[I:], down=Q.dequantize(q2, sf2, g2), q13=q13, sf13=sf13,
+                g13=g13, q2=q2, sf2=sf2, g2=g2)
+
+
 def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
                 expert: str = "bf16", out: str = "f32", chain: bool = True,
                 tokens=None, ids=None, weights=None, norm_after_sum: bool = False,
@@ -211,7 +226,15 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
     can show the two orders differ.
     Returns out [n, d] (float64 holding values of the output storage type), or a
     dict of every intermediate with return_parts.
+
+    expert="nvfp4": expert weights are quantised to NVFP4 (nvfp4.py) and used
+    dequantised; the expert input u is quantised per token on the fly and the SwiGLU
+    output s is requantised with the static per-expert global scale inp["gs_act2"][e]
+    (the page gives no rule for that scale; see the design notes), as the kernels do.
     """
+    if expert == "nvfp4":
+        return _forward_nvfp4(inp, top_k=top_k, eps=eps, out=out, tokens=tokens, ids=ids,
+                              weights=weights, return_parts=return_parts)
     st = storage_kinds(act, expert, out, chain)
     x = as_f64(inp["x"])
     if tokens is not None:
@@ -273,3 +296,46 @@ def route(inp: dict, *, top_k: int, eps: float, tokens=None):
     logits = router_logits(rmsnorm(x, inp["g_in"], eps), inp["w_router"])
     ids, w = topk_route(logits, top_k)
     return ids, w, logits
+
+
+def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts):
+    """The block with NVFP4 experts; storage points as in the BF16 chain except the
+    expert operands: u and s are NVFP4 (u quantised from its FP32 value), y FP32."""
+    st = storage_kinds("bf16", "bf16", out, True)
+    x = as_f64(inp["x"])
+    if tokens is not None:
+        x = x[np.asarray(tokens)]
+    n = x.shape[0]
+    h = rmsnorm(x, inp["g_in"], eps)
+    if ids is None:
+        ids, wts = topk_route(router_logits(h, inp["w_router"]), top_k)
+    else:
+        ids = np.asarray(ids, dtype=np.int32)
+        wts = as_f64(weights)
+        top_k = ids.shape[1]
+    h_pool = _store(F.fp32(h), st["h_pool"])
+    pooled = _store(pool(h_pool, _store(as_f64(inp["w_pool"]), st["w_proj"])), st["pooled"])
+    u32 = F.fp32(rmsnorm(pooled, inp["g_pool"], eps))
+    qu, sfu, alpha = Q.quantize_rows(u32)
+    u = Q.dequantize(qu, sfu, alpha)
+    p = u.shape[1]
+    gs2 = as_f64(inp["gs_act2"])
+    y_all = np.zeros((n, top_k, p))
+    s_all = None
+    for e in np.unique(ids):
+        rows, slots = np.nonzero(ids == e)
+        wq = nvfp4_expert_weights(inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
+        s = F.fp32(expert_swiglu(u[rows], wq["gate"], wq["up"]))
+        qs, sfs = Q.quantize_static(s, gs2[e])
+        s_deq = Q.dequantize(qs, sfs, np.float32(gs2[e]))
+        if return_parts:
+            if s_all is None:
+                s_all = np.zeros((n, top_k, s.shape[1]))
+            s_all[rows, slots] = s
+        y_all[rows, slots] = F.fp32(expert_down(s_deq, wq["down"]))
+    c = _store(combine(y_all, ids, wts, inp["g_exp"], eps), st["c"])
+    res = _store(unpool(c, _store(as_f64(inp["w_unpool"]), st["w_proj"])), st["out"])
+    if not return_parts:
+        return res
+    return dict(out=res, h=h, ids=ids, w=wts, pooled=pooled, u32=u32, u=u, alpha=alpha,
+                s=s_all, y=y_all, c=c)

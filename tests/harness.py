@@ -70,7 +70,8 @@ def fix_margins(inp: dict, shape: synth.Shape, seed: int, min_gap: float = 1e-3,
         bad = rows[oracle.route_margin(logits, shape.top_k) < min_gap]
         if len(bad) == 0:
             return redraws
-        synth.redraw_rows(inp["x"], bad, seed=seed * 1000003 + 7 * r + 1)
+        synth.redraw_rows(inp["x"], bad, seed=seed * 1000003 + 7 * r + 1, shape=shape,
+                          base_seed=seed)
         redraws += len(bad)
         rows = bad
     raise RuntimeError("router margins could not be repaired")

@@ -91,3 +91,36 @@ def test_decode_batch():
     touched = len(np.unique(ids))
     print(f"decode: {touched} experts touched, out err {err:.2e}")
     assert err <= TOL
+
+
+def test_skewed_routing():
+    """Zipf-skewed routing (T=8192): the busiest expert spans tens of 128-row tiles,
+    many experts are empty.  Ids of all tokens exactly; sampled tokens in full,
+    including tokens of the busiest and of the least-loaded non-empty expert."""
+    need_gpu()
+    shape = synth.SKEWED_BF16
+    inp, layer, out, ids, w = run_full(shape, seed=2)
+    x = to_np(inp["x"])
+    h = oracle.rmsnorm(x, to_np(inp["g_in"]), shape.eps)
+    logits = oracle.router_logits(h, to_np(inp["w_router"]))
+    del x, h
+    rid, rw = oracle.topk_route(logits, shape.top_k)
+    np.testing.assert_array_equal(ids, rid)
+    np.testing.assert_allclose(w, rw, rtol=0, atol=TOL_W)
+    counts = np.bincount(ids.reshape(-1), minlength=shape.E)
+    ratio = counts.max() / counts.mean()
+    empty = float(np.mean(counts == 0))
+    print(f"skewed load: max/mean {ratio:.1f}, empty experts {empty:.2f}")
+    assert ratio >= 10 and empty >= 0.05
+    busiest = int(np.argmax(counts))
+    nonempty = np.nonzero(counts)[0]
+    rarest = int(nonempty[np.argmin(counts[nonempty])])
+    tok = [0, 4095, 8191]
+    tok += [int(t) for t in np.nonzero((ids == busiest).any(1))[0][[0, -1]]]
+    tok.append(int(np.nonzero((ids == rarest).any(1))[0][0]))
+    tok = sorted(set(tok))
+    ref = oracle_rows(inp, shape, tok)
+    got = to_np(out[torch.as_tensor(tok, device=out.device)])
+    err = rel_err(got, ref["out"])
+    print(f"skewed sampled tokens {tok}: out err {err:.2e}")
+    assert err <= TOL
