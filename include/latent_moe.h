@@ -75,7 +75,8 @@ typedef enum {
  *   eps    RMSNorm epsilon (added to mean(v^2) inside the square root)
  *   act    MOE_BF16 or MOE_F32: dtype of x, w_pool, w_unpool and the stored
  *          activations between the GEMMs
- *   expert MOE_BF16 or MOE_F32 (must equal act in this version)
+ *   expert MOE_BF16 or MOE_F32 (equal to act), or MOE_NVFP4 with act = MOE_BF16
+ *          (then p and I must be multiples of 256)
  *   out    MOE_BF16 or MOE_F32: dtype of the layer output
  *   flags  0, or MOE_FLAG_TEST_TIMEOUT (other bits must be zero)                  */
 /* Test hook for the error path: the gate/up GEMM never issues its first operand load,
@@ -114,6 +115,22 @@ typedef struct {
   const void* w2;
   const float* g_exp;
   const void* w_unpool;
+  /* NVFP4 experts only (NULL otherwise), all written by moe_quantize_nvfp4 except gs_act2:
+   *   w13 / w2 then hold E2M1 codes (two per byte, even K element in the low nibble):
+   *     w13 [E, 2I, p/2] with gate/up rows interleaved in blocks of 64,
+   *     w2  [E, p, I/2];
+   *   sf13, sf2  UE4M3 block scales (one per 16 elements along K) in the chunked layout:
+   *     512-byte chunks indexed (row / 128, k / 64), chunk-row-major; inside a chunk the
+   *     scale of (row, 16-block g) is at byte (row % 32) * 16 + ((row % 128) / 32) * 4
+   *     + g % 4 -- the 4 x 32 arrangement the block-scaled MMA reads from tensor memory;
+   *   gs13, gs2  [E] FP32 global scales (amax / (6 * 448) of each expert's W13 / W2);
+   *   gs_act2    [E] FP32 static global scale of the requantised SwiGLU output (caller
+   *              supplied, calibrated: the pages give no rule for it). */
+  const uint8_t* sf13;
+  const uint8_t* sf2;
+  const float* gs13;
+  const float* gs2;
+  const float* gs_act2;
 } moe_weights_t;
 
 /* Canonical (unpacked) weights, as a checkpoint stores them (device pointers):
@@ -138,9 +155,10 @@ size_t moe_workspace_size(const moe_config_t* cfg);
  * (before its first use); moe_read_status clears it again after each read. */
 moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Bytes of the packed buffers moe_pack_weights writes.  which: 0 = w_router (TF32
- * copy), 1 = w13, 2 = w2, 3 = w_pool, 4 = w_unpool.  Returns 0 for a buffer this
- * config does not need packed (a BF16 w2 is used as given). */
+/* Bytes of the packed buffers moe_pack_weights / moe_quantize_nvfp4 write.  which:
+ * 0 = w_router (TF32 copy), 1 = w13, 2 = w2, 3 = w_pool, 4 = w_unpool, and for NVFP4
+ * configs 5 = sf13, 6 = sf2, 7 = gs13, 8 = gs2.  Returns 0 for a buffer this config does
+ * not need packed (a BF16 w2 is used as given). */
 size_t moe_packed_bytes(const moe_config_t* cfg, int which);
 
 /* Prepares weights for moe_forward ("SGLang and Miles Add Day-0 Support for Muse Spark
@@ -154,10 +172,23 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which);
  *    converted to FP16 (BF16 configs) or rounded to TF32 (FP32 configs).
  *  - w_pool_out, w_unpool_out: FP16 copies (BF16 configs) or TF32-rounded copies.
  *  - w2_out: FP32 configs only, a TF32-rounded copy; pass NULL for BF16 configs.
+ *  - NVFP4 configs: w13_out and w2_out must be NULL (moe_quantize_nvfp4 writes them);
+ *    src->w_gate / w_up / w_down are not read.
  * Output buffers are caller-allocated with moe_packed_bytes; none may alias a source. */
 moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weights_t* src,
                               float* w_router_out, void* w13_out, void* w2_out,
                               void* w_pool_out, void* w_unpool_out, moe_stream_t stream);
+
+/* NVFP4 expert weights from BF16 gate [E,I,p], up [E,I,p], down [E,p,I] (device):
+ * per expert one FP32 global scale g = amax / (6 * 448) for gate+up together and one
+ * for down; per 16 elements along K a UE4M3 scale sf = rne(bmax / (6 g)) (saturating at
+ * 448); codes e2m1 = rne(x * (1 / sf) * (1 / g)) (saturating at 6) ("SGLang and Miles
+ * Add Day-0 Support for Muse Spark Open", section "NVFP4 as a third MMA kind").  Output
+ * layouts are those of moe_weights_t's NVFP4 fields; sizes from moe_packed_bytes. */
+moe_status_t moe_quantize_nvfp4(const moe_config_t* cfg, const void* w_gate, const void* w_up,
+                                const void* w_down, uint8_t* w13_out, uint8_t* sf13_out,
+                                float* gs13_out, uint8_t* w2_out, uint8_t* sf2_out,
+                                float* gs2_out, moe_stream_t stream);
 
 /* Router only: full-width RMSNorm, TF32 router GEMM and top-k.
  *   x    [T,d] act dtype (device)
@@ -220,7 +251,11 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally);
  *   6 src [T*k] int32 (dispatched row -> t*k+j)              7 inv [T*k] int32
  *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (BF16 / FP32)   10 y [T*k,p] FP32
  *  11 c [T,p] (FP16 / FP32)
- * Writes min(n, 12) offsets and returns how many it wrote (0 for an invalid config). */
+ * NVFP4 configs: dispatched rows start at a 128-row boundary per expert (R rows in all,
+ * R = 128 * (ceil(T*k/128) + E)); 8 A_perm [R, p/2] E2M1 codes, 9 s [R, I/2] codes,
+ * 10 y [R, p] FP32, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
+ * FP32 per-row scales.  All configs: 15 row_cnt [E+1] int32 rows per expert.
+ * Writes min(n, 16) offsets and returns how many it wrote (0 for an invalid config). */
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n);
 
 /* Synchronises `stream`, returns the device-side status of every call since the last

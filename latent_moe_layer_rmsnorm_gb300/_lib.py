@@ -26,17 +26,19 @@ MOE_NVFP4 = 2
 
 MOE_FLAG_TEST_TIMEOUT = 0x80000000
 
-PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL = range(5)
+PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL, PACK_SF13, PACK_SF2, PACK_GS13, \
+    PACK_GS2 = range(9)
 
 # every symbol the header declares
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_packed_bytes", "moe_pack_weights",
-           "moe_route", "moe_route_noalloc", "moe_forward", "moe_forward_profiled",
+           "moe_quantize_nvfp4", "moe_route", "moe_route_noalloc", "moe_forward",
+           "moe_forward_profiled",
            "moe_num_stages",
            "moe_stage_name", "moe_forward_launches", "moe_workspace_offsets",
            "moe_read_status", "moe_status_string")
 
 OFFSET_NAMES = ("h32", "h16", "ids", "w", "pooled", "row_off", "src", "inv", "a_perm", "s",
-                "y", "c")
+                "y", "c", "sf_u", "sf_s", "alpha", "row_cnt")
 
 
 class MoeError(RuntimeError):
@@ -56,7 +58,9 @@ class moe_weights_t(ctypes.Structure):
     _fields_ = [("g_in", ctypes.c_void_p), ("w_router", ctypes.c_void_p),
                 ("w_pool", ctypes.c_void_p), ("g_pool", ctypes.c_void_p),
                 ("w13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("g_exp", ctypes.c_void_p),
-                ("w_unpool", ctypes.c_void_p)]
+                ("w_unpool", ctypes.c_void_p), ("sf13", ctypes.c_void_p),
+                ("sf2", ctypes.c_void_p), ("gs13", ctypes.c_void_p), ("gs2", ctypes.c_void_p),
+                ("gs_act2", ctypes.c_void_p)]
 
 
 class moe_canonical_weights_t(ctypes.Structure):
@@ -89,6 +93,8 @@ def lib() -> ctypes.CDLL:
     L.moe_pack_weights.argtypes = [cfgp, ctypes.POINTER(moe_canonical_weights_t), vp, vp, vp,
                                    vp, vp, vp]
     L.moe_pack_weights.restype = i32
+    L.moe_quantize_nvfp4.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_quantize_nvfp4.restype = i32
     L.moe_route.argtypes = [cfgp, wp, vp, vp, vp, vp, sz, vp]
     L.moe_route.restype = i32
     L.moe_route_noalloc.argtypes = [cfgp, wp, vp, vp, vp, vp]
@@ -136,6 +142,12 @@ def moe_pack_weights(cfg, src: moe_canonical_weights_t, w_router_out, w13_out, w
                      w_pool_out, w_unpool_out, stream) -> int:
     return int(lib().moe_pack_weights(ctypes.byref(cfg), ctypes.byref(src), w_router_out,
                                       w13_out, w2_out, w_pool_out, w_unpool_out, stream))
+
+
+def moe_quantize_nvfp4(cfg, w_gate, w_up, w_down, w13_out, sf13_out, gs13_out, w2_out,
+                       sf2_out, gs2_out, stream) -> int:
+    return int(lib().moe_quantize_nvfp4(ctypes.byref(cfg), w_gate, w_up, w_down, w13_out,
+                                        sf13_out, gs13_out, w2_out, sf2_out, gs2_out, stream))
 
 
 def moe_route(cfg, W: moe_weights_t, x, ids, w, ws, ws_bytes, stream) -> int:

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -118,6 +120,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Untiled bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completing `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // ---- tcgen05: tensor memory ---------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -198,6 +209,46 @@ __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint6
   }
 }
 
+// Block-scaled FP4 MMA (NVFP4: E2M1 operands, one UE4M3 scale per 16 elements of K):
+// scale_a / scale_b are the TMEM addresses of this K=64 step's scales (A row r: lane r,
+// column scale_a + r/32; B column n: lane n%32, column scale_b + n/32; 4 bytes = the 4
+// blocks of 16), as laid down by tcgen05.cp .32x128b.warpx4 from 4x32 chunks.
+__device__ __forceinline__ void mma_issue_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t scale_a, uint32_t scale_b,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(scale_a), "r"(scale_b), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of the block-scaled kind: A/B format E2M1 (1), scale format
+// UE4M3 (bit 23 = 0), scale-data ids 0, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_nvf4(uint32_t m, uint32_t n) {
+  return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Shared-memory descriptor of an unswizzled operand: 8-row x 16-byte core matrices,
+// `lbo` bytes apart along the 16-byte dimension and `sbo` bytes apart along rows.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(lbo >> 4) << 16;
+  d |= static_cast<uint64_t>(sbo >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  return d;
+}
+
+// Copy one 4x32 scale chunk (512 B: 32 rows of 16 bytes, byte 4j + b of row i = scale b
+// of operand row 32j + i) into 4 TMEM columns of all four lane quadrants.
+__device__ __forceinline__ void tmem_cp_scales(uint32_t taddr, const void* chunk) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
+               "l"(sdesc_plain(smem_u32(chunk), 16, 128))
+               : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -229,6 +280,64 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two FP32 values -> two E2M1 codes (round to nearest even, saturating at 6), `lo` in
+// bits 0-3 (the even K element), `hi` in bits 4-7.
+__device__ __forceinline__ uint32_t pack_e2m1x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1,
+                                                        cudaRoundNearest));
+}
+
+// Non-negative FP32 -> UE4M3 code (round to nearest even, saturating at 448).
+__device__ __forceinline__ uint32_t encode_ue4m3(float v) {
+  return static_cast<uint32_t>(
+             __nv_cvt_float2_to_fp8x2(make_float2(v, 0.0f), __NV_SATFINITE, __NV_E4M3)) &
+         0xFFu;
+}
+
+// UE4M3 code -> value, from the format: bias 7, 3 mantissa bits, subnormals m * 2^-9.
+// Built from the FP32 bit fields (exact).
+__device__ __forceinline__ float decode_ue4m3(uint32_t c) {
+  const uint32_t e = (c >> 3) & 15u, m = c & 7u;
+  return e == 0 ? static_cast<float>(m) * 0.001953125f
+                : __uint_as_float(((e + 120u) << 23) | (m << 20));
+}
+
+// 1 / scale for a UE4M3 code (IEEE division), 0 for the zero code and the NaN codes.
+__device__ __forceinline__ float recip_ue4m3(uint32_t c) {
+  c &= 0xFFu;
+  return (c == 0 || (c & 0x7Fu) == 0x7Fu || c > 0x7Fu) ? 0.0f : 1.0f / decode_ue4m3(c);
+}
+
+// NVFP4 quantisation of one block of 16 FP32 values with global scale g (six_g =
+// 6*g and inv_g = 1/g in FP32, both 0 when g == 0): returns the scale code and writes
+// 8 bytes of E2M1 codes (element 2i in the low nibble of byte i).  The op order is
+// the reference order: sf = ue4m3(bmax / six_g); r = recip(sf) * inv_g;
+// code = e2m1(x * r).
+__device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float six_g, float inv_g,
+                                               uint2& codes, const float* recip_tab) {
+  float bmax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
+  const uint32_t sf = encode_ue4m3(six_g > 0.f ? bmax / six_g : 0.f);
+  const float r = (recip_tab ? recip_tab[sf] : recip_ue4m3(sf)) * inv_g;
+  uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w0 |= pack_e2m1x2(x[2 * i] * r, x[2 * i + 1] * r) << (8 * i);
+    w1 |= pack_e2m1x2(x[8 + 2 * i] * r, x[8 + 2 * i + 1] * r) << (8 * i);
+  }
+  codes = make_uint2(w0, w1);
+  return sf;
+}
+
+// Byte offset of scale (row r, 16-element block g) in the chunked scale layout of a
+// matrix with K columns: chunk = (r / 128, g / 4), 512 B each, chunks row-block-major;
+// inside a chunk byte (r % 32) * 16 + ((r % 128) / 32) * 4 + g % 4.
+__device__ __forceinline__ size_t sf_offset(size_t r, int g, int K) {
+  const size_t chunk = (r >> 7) * static_cast<size_t>(K >> 6) + (g >> 2);
+  return chunk * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (g & 3);
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {

@@ -1,0 +1,264 @@
+// gemm_nvf4.cuh -- grouped expert GEMMs on NVFP4 operands with tcgen05 block-scaled MMA
+// ("SGLang and Miles Add Day-0 Support for Muse Spark Open", "NVFP4 as a third MMA kind":
+// E2M1 operands, UE4M3 scale per 16 elements, per-token FP32 input scales applied to the
+// first GEMM's accumulators; "The NVFP4 requantization reciprocal table": the SwiGLU
+// output is requantised to NVFP4 between the two GEMMs with a 256-entry FP32 table of
+// scale reciprocals in shared memory).
+//
+//   gate/up  u [rows, p] x W13_e [2I, p] (gate/up rows interleaved in blocks of 64)
+//            epilogue: a, b = acc * alpha[row] * beta13[e]; s = silu(a) * b; s -> NVFP4
+//            with the static global scale gamma[e] (codes + chunked scales)
+//   down     s [rows, I] x W2_e [p, I]; epilogue y = acc * gamma[e] * beta2[e] (FP32)
+//
+// Same pipeline as gemm_tcgen05.cuh (TMA producer warp, one MMA-issuing thread, four
+// epilogue warps, double-buffered TMEM accumulators, bounded waits), with per-stage
+// scale tiles: the producer bulk-copies the 4 scale chunks (512 B each) of the A and B
+// tiles next to the operand tiles; the MMA thread moves them to TMEM with tcgen05.cp
+// (.32x128b.warpx4) and issues 4 block-scaled MMAs (K = 64 each) per 128-byte K slice.
+// TMEM: accumulators in columns [0, 256), a ring of per-stage scale columns after them.
+// A rows are 128-aligned per expert (padded dispatch), so a tile's scales are whole chunks.
+#pragma once
+
+#include "gemm_tcgen05.cuh"
+
+namespace lmoe {
+
+constexpr int NV_BN = 128;
+constexpr int NV_STAGES = 5;
+constexpr int NV_A_STAGE = GEMM_BM * 128;    // 128 rows x 256 FP4
+constexpr int NV_B_STAGE = NV_BN * 128;
+constexpr int NV_SF_STAGE = 4 * 512;         // 4 scale chunks per operand per stage
+constexpr int NV_SF_COL0 = 256;
+constexpr int NV_SF_COLS = 32;               // per stage: 16 (A) + 16 (B)
+
+enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_F32 = 1 };
+
+struct NvSmem {
+  GemmSmem g;                // barriers and schedule (its `full`/`empty` sized for GEMM_STAGES)
+  uint64_t full[NV_STAGES];
+  uint64_t empty[NV_STAGES];
+  float recip[256];
+};
+
+constexpr size_t nvf4_smem_bytes() {
+  return 1024 + size_t(NV_STAGES) * (NV_A_STAGE + NV_B_STAGE + 2 * NV_SF_STAGE) + sizeof(NvSmem);
+}
+
+template <int EPI>
+__device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoord& tc,
+                                              uint32_t taddr, int r, const float* recip) {
+  const bool row_ok = r < tc.valid;
+  const size_t row = static_cast<size_t>(tc.a_row + r);
+  if constexpr (EPI == NV_EPI_SWIGLU_Q) {
+    // columns [0, 64) gate, [64, 128) up of output features n_blk*64 ..
+    const float sc = P.row_scale[row] * P.grp_scale[tc.e];
+    const float gam = P.out_scale[tc.e];
+    const float six_g = 6.0f * gam;
+    const float inv_g = gam > 0.f ? 1.0f / gam : 0.f;
+    const int I = P.ld_out;
+    uint8_t* codes = static_cast<uint8_t*>(P.out) + row * (I / 2);
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      uint32_t g[16], u[16];
+      tmem_ld16(taddr + c0, g);
+      tmem_ld16(taddr + 64 + c0, u);
+      tmem_ld_wait();
+      float s[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a = __uint_as_float(g[i]) * sc;
+        const float b = __uint_as_float(u[i]) * sc;
+        s[i] = a / (1.0f + __expf(-a)) * b;     // silu(a) * b
+      }
+      uint2 q;
+      const uint32_t code = quantize16(s, six_g, inv_g, q, recip);
+      if (row_ok) {
+        const int col = tc.n_blk * 64 + c0;
+        *reinterpret_cast<uint2*>(codes + col / 2) = q;
+        P.out_sf[sf_offset(row, col / 16, I)] = static_cast<uint8_t>(code);
+      }
+    }
+  } else {
+    const float sc = P.grp_scale[tc.e] * P.out_scale[tc.e];
+    const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * NV_BN;
+#pragma unroll 1
+    for (int c0 = 0; c0 < NV_BN; c0 += 32) {
+      uint32_t a[16], b[16];
+      tmem_ld16(taddr + c0, a);
+      tmem_ld16(taddr + c0 + 16, b);
+      tmem_ld_wait();
+      float va[16], vb[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        va[i] = __uint_as_float(a[i]) * sc;
+        vb[i] = __uint_as_float(b[i]) * sc;
+      }
+      if (row_ok) {
+        store16(P.out, base + c0, OUT_F32, va);
+        store16(P.out, base + c0 + 16, OUT_F32, vb);
+      }
+    }
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const GemmParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + NV_STAGES * NV_A_STAGE;
+  uint8_t* sSA = sB + NV_STAGES * NV_B_STAGE;
+  uint8_t* sSB = sSA + NV_STAGES * NV_SF_STAGE;
+  NvSmem* N = reinterpret_cast<NvSmem*>(sSB + NV_STAGES * NV_SF_STAGE);
+  GemmSmem* S = &N->g;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NV_STAGES; ++s) {
+      mbar_init(&N->full[s], 1);
+      mbar_init(&N->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&S->tfull[a], 1);
+      mbar_init(&S->tempty[a], 4);
+    }
+    mbar_init(&S->drain, 1);
+    S->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  for (int i = threadIdx.x; i <= P.groups; i += blockDim.x) {
+    S->mt_off[i] = P.mt_off[i];
+    S->row_off[i] = P.row_off[i];
+    S->row_cnt[i] = P.row_cnt[i];
+  }
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) N->recip[i] = recip_ue4m3(i);
+  if (warp == 2) tmem_alloc(&S->tmem_base, GEMM_TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = S->tmem_base;
+  const int num_tiles = gemm_num_tiles(P, S);
+  const int kblocks = P.K / 256;               // 256 FP4 = 128 bytes per stage
+  const int kchunks = P.K / 64;                // scale chunks per 128-row block
+  const uint64_t limit = P.timeout_ns;
+  volatile int* abort_flag = &S->abort_flag;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    const uint32_t bytes = NV_A_STAGE + NV_B_STAGE + 2 * NV_SF_STAGE;
+    int stage = 0;
+    uint32_t phase = 0;
+    int last_phase[NV_STAGES];
+#pragma unroll
+    for (int s = 0; s < NV_STAGES; ++s) last_phase[s] = -1;
+    for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+      const TileCoord tc = gemm_tile(P, S, t);
+      const uint8_t* sfa = P.sf_a + (static_cast<size_t>(tc.a_row >> 7) * kchunks) * 512;
+      const uint8_t* sfb = P.sf_b + (static_cast<size_t>(tc.b_row >> 7) * kchunks) * 512;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&N->empty[stage], phase ^ 1, abort_flag, P.status,
+                               WAIT_PRODUCER_EMPTY, limit))
+          goto producer_done;
+        mbar_arrive_expect_tx(&N->full[stage], bytes);
+        tma_load_2d(sA + stage * NV_A_STAGE, &tmA, &N->full[stage], kb * 128, tc.a_row);
+        tma_load_2d(sB + stage * NV_B_STAGE, &tmB, &N->full[stage], kb * 128, tc.b_row);
+        bulk_load(sSA + stage * NV_SF_STAGE, sfa + kb * NV_SF_STAGE, NV_SF_STAGE, &N->full[stage]);
+        bulk_load(sSB + stage * NV_SF_STAGE, sfb + kb * NV_SF_STAGE, NV_SF_STAGE, &N->full[stage]);
+        last_phase[stage] = static_cast<int>(phase);
+        if (++stage == NV_STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  producer_done:
+    if (*abort_flag) {
+      volatile int never = 0;
+      for (int s = 0; s < NV_STAGES; ++s)
+        if (last_phase[s] >= 0)
+          mbar_wait_bounded(&N->full[s], static_cast<uint32_t>(last_phase[s]), &never, nullptr,
+                            WAIT_DRAIN, limit);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = idesc_nvf4(GEMM_BM, NV_BN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_bounded(&S->tempty[acc], acc_phase ^ 1, abort_flag, P.status,
+                             WAIT_MMA_TMEM_EMPTY, limit))
+        break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * NV_BN;
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&N->full[stage], phase, abort_flag, P.status, WAIT_MMA_FULL,
+                               limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sf_col = tmem_base + NV_SF_COL0 + stage * NV_SF_COLS;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          tmem_cp_scales(sf_col + 4 * j, sSA + stage * NV_SF_STAGE + 512 * j);
+          tmem_cp_scales(sf_col + 16 + 4 * j, sSB + stage * NV_SF_STAGE + 512 * j);
+        }
+        const uint32_t a0 = smem_u32(sA + stage * NV_A_STAGE);
+        const uint32_t b0 = smem_u32(sB + stage * NV_B_STAGE);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mma_issue_nvf4(d_tmem, sdesc_sw128(a0 + 32 * j), sdesc_sw128(b0 + 32 * j), idesc,
+                         sf_col + 4 * j, sf_col + 16 + 4 * j, (kb | j) != 0);
+        }
+        mma_commit(&N->empty[stage]);
+        if (++stage == NV_STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      mma_commit(&S->tfull[acc]);
+    }
+    mma_commit(&S->drain);
+    {
+      volatile int never = 0;
+      mbar_wait_bounded(&S->drain, 0, &never, P.status, WAIT_DRAIN, limit);
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_bounded(&S->tfull[acc], acc_phase, abort_flag, P.status,
+                             WAIT_EPI_TMEM_FULL, limit))
+        break;
+      tc_fence_after();
+      const TileCoord tc = gemm_tile(P, S, t);
+      const uint32_t taddr = tmem_base + acc * NV_BN + (static_cast<uint32_t>(q * 32) << 16);
+      nvf4_epilogue<EPI>(P, tc, taddr, r, N->recip);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S->tempty[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, GEMM_TMEM_COLS);
+  }
+}
+
+}  // namespace lmoe

@@ -39,8 +39,9 @@ constexpr int ROUTER_MAX_K = 8;
 
 enum EpiKind : int { EPI_ROUTER = 0, EPI_STORE = 1, EPI_SWIGLU = 2 };
 enum OutFmt : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_TF32 = 2 };
-// Operand kinds; the values are the instruction-descriptor format codes.
-enum OpKind : int { OP_F16 = 0, OP_BF16 = 1, OP_TF32 = 2 };
+// Operand kinds; the values of the first three are the instruction-descriptor format
+// codes of kind::f16 / kind::tf32.  OP_NVF4: packed E2M1 operands (gemm_nvf4.cuh).
+enum OpKind : int { OP_F16 = 0, OP_BF16 = 1, OP_TF32 = 2, OP_NVF4 = 3 };
 
 struct GemmParams {
   int M;        // dense: rows of A and of the output
@@ -50,6 +51,7 @@ struct GemmParams {
   int groups;   // 0 = dense; > 0 = grouped over this many experts
   const int* row_off;  // grouped: [groups+1] first A row of each expert (device)
   const int* mt_off;   // grouped: [groups+1] prefix sum of 128-row tiles (device)
+  const int* row_cnt;  // grouped: [groups] rows of each expert (device)
   int* status;
   unsigned long long timeout_ns;
   int debug_skip_first_load;  // test hook: never issue the first TMA load
@@ -60,6 +62,14 @@ struct GemmParams {
   int E, top_k;         // router
   int32_t* ids;
   float* wts;
+  // NVFP4 operands: chunked scale arrays of A and B, and FP32 scales applied to the
+  // accumulator: row_scale[row] * grp_scale[e] (gate/up) or grp_scale[e] * out_scale[e]
+  const uint8_t* sf_a;
+  const uint8_t* sf_b;
+  const float* row_scale;
+  const float* grp_scale;
+  const float* out_scale;   // requantisation global scale (gate/up) / extra factor (down)
+  uint8_t* out_sf;          // requantised output: chunked scales (codes go to `out`)
 };
 
 struct GemmSmem {
@@ -72,6 +82,7 @@ struct GemmSmem {
   int abort_flag;
   int mt_off[GEMM_MAX_GROUPS + 1];
   int row_off[GEMM_MAX_GROUPS + 1];
+  int row_cnt[GEMM_MAX_GROUPS + 1];
 };
 
 constexpr size_t gemm_smem_bytes() {
@@ -84,6 +95,7 @@ struct TileCoord {
   int b_row;   // first B row
   int valid;   // rows of the tile that belong to it (<= 128)
   int n_blk;   // tile index along N
+  int e;       // expert (grouped), 0 for dense
 };
 
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& P, const GemmSmem* S) {
@@ -103,6 +115,7 @@ __device__ __forceinline__ TileCoord gemm_tile(const GemmParams& P, const GemmSm
     c.a_row = m_blk * GEMM_BM;
     c.b_row = c.n_blk * P.bn;
     c.valid = min(GEMM_BM, P.M - c.a_row);
+    c.e = 0;
     return c;
   }
   // largest e with mt_off[e] * nb <= t (experts with no rows have empty ranges)
@@ -118,7 +131,8 @@ __device__ __forceinline__ TileCoord gemm_tile(const GemmParams& P, const GemmSm
   const int m_blk = local - c.n_blk * mt_e;
   c.a_row = S->row_off[e] + m_blk * GEMM_BM;
   c.b_row = e * P.N + c.n_blk * P.bn;
-  c.valid = min(GEMM_BM, S->row_off[e + 1] - c.a_row);
+  c.valid = min(GEMM_BM, S->row_cnt[e] - m_blk * GEMM_BM);
+  c.e = e;
   return c;
 }
 
@@ -269,6 +283,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int i = threadIdx.x; i <= P.groups; i += blockDim.x) {
       S->mt_off[i] = P.mt_off[i];
       S->row_off[i] = P.row_off[i];
+      S->row_cnt[i] = P.row_cnt[i];
     }
   }
   if (warp == 2) tmem_alloc(&S->tmem_base, GEMM_TMEM_COLS);

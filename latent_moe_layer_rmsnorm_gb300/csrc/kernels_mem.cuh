@@ -144,10 +144,13 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
   return warp_prefix + x - v;
 }
 
-// 2) one block: chunk bases per expert, expert row offsets and 128-row tile offsets.
+// 2) one block: chunk bases per expert, expert row offsets, row counts and 128-row tile
+// offsets.  padded != 0 starts every expert's rows on a 128-row boundary (row_off[e] =
+// 128 * mt_off[e]), so no 128-row tile spans two experts.
 __global__ void __launch_bounds__(256)
     dispatch_scan_kernel(int* __restrict__ chunk_counts, int nchunks, int E,
-                         int* __restrict__ row_off, int* __restrict__ mt_off) {
+                         int* __restrict__ row_off, int* __restrict__ mt_off,
+                         int* __restrict__ row_cnt, int padded) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
   int running = 0;
@@ -163,14 +166,17 @@ __global__ void __launch_bounds__(256)
   const int mt = (e < E) ? (running + 127) / 128 : 0;
   int mt_total;
   const int mto = block_excl_scan(mt, sh, &mt_total);
+  const int start = padded ? mto * 128 : off;
   if (e < E) {
-    row_off[e] = off;
+    row_off[e] = start;
     mt_off[e] = mto;
-    for (int c = 0; c < nchunks; ++c) chunk_counts[c * E + e] += off;
+    row_cnt[e] = running;
+    for (int c = 0; c < nchunks; ++c) chunk_counts[c * E + e] += start;
   }
   if (e == 0) {
-    row_off[E] = total;
+    row_off[E] = padded ? mt_total * 128 : total;
     mt_off[E] = mt_total;
+    row_cnt[E] = total;
   }
 }
 
@@ -421,6 +427,173 @@ __global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __res
   const int n16 = p * elem_bytes / 16;
   for (int c = threadIdx.x; c < n16; c += blockDim.x)
     reinterpret_cast<uint4*>(o)[c] = pack_convert<CONV>(reinterpret_cast<const uint4*>(s)[c]);
+}
+
+// ---- NVFP4 ------------------------------------------------------------------------------
+// ("SGLang and Miles Add Day-0 Support for Muse Spark Open", "NVFP4 as a third MMA kind":
+// E2M1 values, UE4M3 scale per 16 elements, FP32 global scale per tensor / per token.)
+constexpr float NVFP4_AMAX_DIV = 2688.0f;   // 6 (largest E2M1) * 448 (largest UE4M3)
+
+// amax of |x| over `n` BF16 values at src + blockIdx.y * stride_y, merged into
+// amax_bits[blockIdx.y] (FP32 bits of a non-negative value order like integers, so
+// atomicMax is exact and order independent).
+__global__ void amax_bf16_kernel(const __nv_bfloat16* __restrict__ src, size_t n,
+                                 size_t stride_y, unsigned* __restrict__ amax_bits) {
+  __shared__ float red[32];
+  const __nv_bfloat16* p = src + blockIdx.y * stride_y;
+  float m = 0.f;
+  for (size_t i = (blockIdx.x * size_t(blockDim.x) + threadIdx.x) * 8; i < n;
+       i += size_t(gridDim.x) * blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    m = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (threadIdx.x == 0) atomicMax(amax_bits + blockIdx.y, __float_as_uint(m));
+  }
+}
+
+__global__ void zero_u32_kernel(unsigned* p, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0;
+}
+
+// g[e] = amax[e] / 2688 (the NVFP4 global scale of one expert's tensor).
+__global__ void global_scale_kernel(const unsigned* __restrict__ amax_bits, float* __restrict__ g,
+                                    int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) g[i] = __uint_as_float(amax_bits[i]) / NVFP4_AMAX_DIV;
+}
+
+// One block per destination row of a quantised expert matrix [E * rows, K]:
+//   gate/up (interleaved in blocks of G rows, like the BF16 packing) when `up` is set,
+//   a plain matrix otherwise.  Codes: [row][K/2] bytes; scales: chunked layout.
+__global__ void quantize_weight_kernel(const __nv_bfloat16* __restrict__ gate,
+                                       const __nv_bfloat16* __restrict__ up,
+                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                                       const float* __restrict__ g, int rows_per_expert, int K,
+                                       int G) {
+  const size_t drow = blockIdx.x;
+  const size_t e = drow / rows_per_expert;
+  const int r = static_cast<int>(drow - e * rows_per_expert);
+  const __nv_bfloat16* src;
+  if (up != nullptr) {     // interleaved: dst rows [2G*b, 2G*b+G) gate, then up
+    const int half_rows = rows_per_expert / 2;
+    const int b = r / (2 * G), i = r - b * 2 * G;
+    const size_t srow = e * half_rows + size_t(b) * G + (i >= G ? i - G : i);
+    src = (i >= G ? up : gate) + srow * K;
+  } else {
+    src = gate + drow * K;
+  }
+  const float ge = g[e];
+  const float six_g = 6.0f * ge;
+  const float inv_g = ge > 0.f ? 1.0f / ge : 0.f;
+  for (int grp = threadIdx.x; grp < K / 16; grp += blockDim.x) {
+    const uint4 a = reinterpret_cast<const uint4*>(src)[2 * grp];
+    const uint4 b = reinterpret_cast<const uint4*>(src)[2 * grp + 1];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float x[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = unpack_bf16x2(w[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
+    }
+    uint2 q;
+    const uint32_t code = quantize16(x, six_g, inv_g, q, nullptr);
+    reinterpret_cast<uint2*>(codes + drow * (K / 2))[grp] = q;
+    sf[sf_offset(drow, grp, K)] = static_cast<uint8_t>(code);
+  }
+}
+
+// Pooled-input RMSNorm fused with the per-token NVFP4 quantiser: one block per token;
+// u = pooled * rsqrt(mean(pooled^2) + eps) * g_pool in FP32, alpha = max|u| / 2688,
+// then E2M1 codes + UE4M3 scales written to each of the token's k dispatched rows
+// (alpha too, per row, for the gate/up GEMM's accumulators).  p <= 8192.
+__global__ void __launch_bounds__(MEM_THREADS)
+    pool_quant_kernel(const float* __restrict__ pooled, const float* __restrict__ g,
+                      const int* __restrict__ inv, uint8_t* __restrict__ codes,
+                      uint8_t* __restrict__ sf, float* __restrict__ alpha_rows, int p, int k,
+                      float eps) {
+  __shared__ float red[32];
+  __shared__ int rows[MAX_TOPK];
+  const size_t t = blockIdx.x;
+  if (threadIdx.x < k) rows[threadIdx.x] = inv[t * k + threadIdx.x];
+  constexpr int GPT = 2;                 // 16-element groups per thread: p <= 8192
+  const int ngrp = p >> 4;
+  float v[GPT][16];
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int grp = threadIdx.x + j * MEM_THREADS;
+    if (grp < ngrp) {
+      const float4* s4 = reinterpret_cast<const float4*>(pooled + t * p) + 4 * grp;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 a = s4[q];
+        v[j][4 * q] = a.x; v[j][4 * q + 1] = a.y; v[j][4 * q + 2] = a.z; v[j][4 * q + 3] = a.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss = fmaf(v[j][i], v[j][i], ss);
+    }
+  }
+  const float total = block_sum(ss, red);
+  const float rs = rsqrtf(total / static_cast<float>(p) + eps);
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int grp = threadIdx.x + j * MEM_THREADS;
+    if (grp < ngrp) {
+      const float4* g4 = reinterpret_cast<const float4*>(g) + 4 * grp;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 gg = g4[q];
+        v[j][4 * q] = v[j][4 * q] * rs * gg.x;
+        v[j][4 * q + 1] = v[j][4 * q + 1] * rs * gg.y;
+        v[j][4 * q + 2] = v[j][4 * q + 2] * rs * gg.z;
+        v[j][4 * q + 3] = v[j][4 * q + 3] * rs * gg.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+    }
+  }
+  // block max (after block_sum's barriers the reduction buffer is free again)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = (threadIdx.x & 31) < (blockDim.x >> 5) ? red[threadIdx.x & 31] : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float a = amax / NVFP4_AMAX_DIV;
+  const float six_a = 6.0f * a;
+  const float inv_a = a > 0.f ? 1.0f / a : 0.f;
+#pragma unroll
+  for (int j = 0; j < GPT; ++j) {
+    const int grp = threadIdx.x + j * MEM_THREADS;
+    if (grp < ngrp) {
+      uint2 q;
+      const uint32_t code = quantize16(v[j], six_a, inv_a, q, nullptr);
+      for (int sl = 0; sl < k; ++sl) {
+        const int r = rows[sl];
+        if (r < 0) continue;
+        reinterpret_cast<uint2*>(codes + size_t(r) * (p / 2))[grp] = q;
+        sf[sf_offset(size_t(r), grp, p)] = static_cast<uint8_t>(code);
+      }
+    }
+  }
+  if (threadIdx.x < k && rows[threadIdx.x] >= 0) alpha_rows[rows[threadIdx.x]] = a;
 }
 
 __global__ void clear_status_kernel(int* status) {

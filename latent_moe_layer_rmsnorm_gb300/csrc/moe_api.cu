@@ -5,6 +5,7 @@
 
 #include "../../include/latent_moe.h"
 #include "common.cuh"
+#include "gemm_nvf4.cuh"
 #include "gemm_tcgen05.cuh"
 #include "kernels_mem.cuh"
 
@@ -53,9 +54,10 @@ bool make_tmap(CUtensorMap* m, const void* base, int kind, uint64_t inner, uint6
                uint32_t box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
-  const uint32_t es = kind == OP_TF32 ? 4 : 2;
+  const uint32_t es = kind == OP_TF32 ? 4 : kind == OP_NVF4 ? 1 : 2;
   const CUtensorMapDataType dt = kind == OP_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : kind == OP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : kind == OP_NVF4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * es};
@@ -96,6 +98,14 @@ moe_status_t device_ready(int* sms) {
     if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_STORE>();
     if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_SWIGLU>();
     if (e == cudaSuccess) e = set_smem_attr<OP_BF16, EPI_STORE>();
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_SWIGLU_Q>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(nvf4_smem_bytes()));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_F32>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(nvf4_smem_bytes()));
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     D.ready = true;
   }
@@ -114,7 +124,12 @@ moe_status_t validate(const moe_config_t* c) {
   if (c->out != MOE_BF16 && c->out != MOE_F32) return MOE_ERR_INVALID_ARG;
   if (c->expert != MOE_BF16 && c->expert != MOE_F32 && c->expert != MOE_NVFP4)
     return MOE_ERR_INVALID_ARG;
-  if (c->expert != c->act) return MOE_ERR_UNSUPPORTED;
+  if (c->expert == MOE_NVFP4) {
+    if (c->act != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (c->p % 256 || c->I % 256) return MOE_ERR_UNSUPPORTED;
+  } else if (c->expert != c->act) {
+    return MOE_ERR_UNSUPPORTED;
+  }
   if ((c->flags & ~MOE_FLAG_TEST_TIMEOUT) != 0) return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED;
   if (c->d % 128 || c->p % 128 || c->I % 128) return MOE_ERR_UNSUPPORTED;
@@ -126,9 +141,10 @@ moe_status_t validate(const moe_config_t* c) {
 }
 
 struct WsLayout {
-  size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, src, inv, a_perm, s, y,
-      c, total;
+  size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, row_cnt, src, inv, a_perm,
+      s, y, c, sf_u, sf_s, alpha, total;
   int nchunks;
+  size_t rows;    // dispatched rows (NVFP4: 128-aligned per expert)
 };
 
 WsLayout ws_layout(const moe_config_t& c) {
@@ -142,7 +158,10 @@ WsLayout ws_layout(const moe_config_t& c) {
   const size_t T = c.T, d = c.d, p = c.p, E = c.E, k = c.top_k, I = c.I;
   const size_t ea = c.act == MOE_F32 ? 4 : 2;
   const size_t ee = c.expert == MOE_F32 ? 4 : 2;
+  const bool q = c.expert == MOE_NVFP4;
   L.nchunks = static_cast<int>((T * k + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
+  L.rows = q ? 128 * ((T * k + 127) / 128 + E) : T * k;
+  const size_t R = L.rows;
   L.status = take(256);
   L.h32 = take(T * d * 4);
   L.h16 = take(c.act == MOE_BF16 ? T * d * 2 : 0);
@@ -152,12 +171,16 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.chunk = take(size_t(L.nchunks) * E * 4);
   L.row_off = take((E + 1) * 4);
   L.mt_off = take((E + 1) * 4);
-  L.src = take(T * k * 4);
+  L.row_cnt = take((E + 1) * 4);
+  L.src = take(R * 4);
   L.inv = take(T * k * 4);
-  L.a_perm = take(T * k * p * ee);
-  L.s = take(T * k * I * ee);
-  L.y = take(T * k * p * 4);     // expert outputs stay FP32 until the per-expert norm
+  L.a_perm = take(q ? R * p / 2 : R * p * ee);
+  L.s = take(q ? R * I / 2 : R * I * ee);
+  L.y = take(R * p * 4);     // expert outputs stay FP32 until the per-expert norm
   L.c = take(T * p * ea);
+  L.sf_u = take(q ? R * p / 16 : 0);
+  L.sf_s = take(q ? R * I / 16 : 0);
+  L.alpha = take(q ? R * 4 : 0);
   L.total = off;
   return L;
 }
@@ -174,6 +197,11 @@ moe_status_t check_weights(const moe_config_t& c, const moe_weights_t* W, bool r
   const void* more[] = {W->w_pool, W->g_pool, W->w13, W->w2, W->g_exp, W->w_unpool};
   for (const void* p : more)
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (c.expert == MOE_NVFP4) {
+    const void* q[] = {W->sf13, W->sf2, W->gs13, W->gs2, W->gs_act2};
+    for (const void* p : q)
+      if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  }
   return MOE_OK;
 }
 
@@ -296,19 +324,29 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   E.mark(3);
 
   // ---- stage: dispatch (counting sort) + pooled RMSNorm + permute ---------------------
+  const bool nvf4 = c.expert == MOE_NVFP4;
   int* chunk = reinterpret_cast<int*>(base + L.chunk);
   int* row_off = reinterpret_cast<int*>(base + L.row_off);
   int* mt_off = reinterpret_cast<int*>(base + L.mt_off);
+  int* row_cnt = reinterpret_cast<int*>(base + L.row_cnt);
   int* src = reinterpret_cast<int*>(base + L.src);
   int* inv = reinterpret_cast<int*>(base + L.inv);
   void* a_perm = base + L.a_perm;
+  uint8_t* sf_u = base + L.sf_u;
+  uint8_t* sf_s = base + L.sf_s;
+  float* alpha = reinterpret_cast<float*>(base + L.alpha);
   dispatch_hist_kernel<<<L.nchunks, MEM_THREADS, 0, st>>>(ids, rows, E_, chunk, status);
   MOE_TRY(last_launch());
-  dispatch_scan_kernel<<<1, 256, 0, st>>>(chunk, L.nchunks, E_, row_off, mt_off);
+  dispatch_scan_kernel<<<1, 256, 0, st>>>(chunk, L.nchunks, E_, row_off, mt_off, row_cnt,
+                                          nvf4 ? 1 : 0);
   MOE_TRY(last_launch());
   dispatch_scatter_kernel<<<L.nchunks, 32, 0, st>>>(ids, rows, E_, chunk, inv, src);
   MOE_TRY(last_launch());
-  if (exp_f32)
+  if (nvf4)
+    pool_quant_kernel<<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv,
+                                                 static_cast<uint8_t*>(a_perm), sf_u, alpha, p,
+                                                 k, c.eps);
+  else if (exp_f32)
     pool_permute_kernel<true><<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv, a_perm, p, k, c.eps);
   else
     pool_permute_kernel<false><<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv, a_perm, p, k, c.eps);
@@ -318,14 +356,29 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   // ---- stage: grouped gate/up GEMM + SwiGLU -------------------------------------------
   void* s_buf = base + L.s;
   const int max_mt = (rows + GEMM_BM - 1) / GEMM_BM + E_;
-  {
+  const int R = static_cast<int>(L.rows);
+  if (nvf4) {
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, a_perm, OP_NVF4, p / 2, R, GEMM_BM) ||
+        !make_tmap(&tb, W->w13, OP_NVF4, p / 2, static_cast<uint64_t>(E_) * 2 * I, NV_BN))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.N = 2 * I; P.K = p; P.bn = NV_BN; P.groups = E_;
+    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
+    P.out = s_buf; P.ld_out = I;
+    P.sf_a = sf_u; P.sf_b = W->sf13; P.row_scale = alpha; P.grp_scale = W->gs13;
+    P.out_scale = W->gs_act2; P.out_sf = sf_s;
+    const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
+    gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    MOE_TRY(last_launch());
+  } else {
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, a_perm, k_up, p, rows, GEMM_BM) ||
         !make_tmap(&tb, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, 2 * W13_GROUP))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = 2 * I; P.K = p; P.bn = 2 * W13_GROUP; P.groups = E_;
-    P.row_off = row_off; P.mt_off = mt_off;
+    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
     P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
     const int grid = std::min(sms, max_mt * (2 * I / P.bn));
@@ -336,7 +389,20 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
 
   // ---- stage: grouped down GEMM -> y ------------------------------------------------------
   void* y_buf = base + L.y;
-  {
+  if (nvf4) {
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, s_buf, OP_NVF4, I / 2, R, GEMM_BM) ||
+        !make_tmap(&tb, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, NV_BN))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.N = p; P.K = I; P.bn = NV_BN; P.groups = E_;
+    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
+    P.out = y_buf; P.ld_out = p;
+    P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
+    const int grid = std::min(sms, max_mt * (p / NV_BN));
+    gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    MOE_TRY(last_launch());
+  } else {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
     if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
@@ -344,7 +410,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = bn; P.groups = E_;
-    P.row_off = row_off; P.mt_off = mt_off;
+    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
     P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32;
     const int grid = std::min(sms, max_mt * (p / bn));
     if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
@@ -438,12 +504,18 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which) {
   const moe_config_t& c = *cfg;
   const size_t ea = c.act == MOE_F32 ? 4 : 2;
   const size_t ee = c.expert == MOE_F32 ? 4 : 2;
+  const bool q = c.expert == MOE_NVFP4;
   switch (which) {
     case 0: return size_t(c.E) * c.d * 4;
-    case 1: return size_t(c.E) * 2 * c.I * c.p * ee;
-    case 2: return c.expert == MOE_F32 ? size_t(c.E) * c.p * c.I * ee : 0;
+    case 1: return q ? size_t(c.E) * 2 * c.I * c.p / 2 : size_t(c.E) * 2 * c.I * c.p * ee;
+    case 2: return q ? size_t(c.E) * c.p * c.I / 2
+                     : (c.expert == MOE_F32 ? size_t(c.E) * c.p * c.I * ee : 0);
     case 3: return size_t(c.p) * c.d * ea;
     case 4: return size_t(c.d) * c.p * ea;
+    case 5: return q ? size_t(c.E) * 2 * c.I * c.p / 16 : 0;
+    case 6: return q ? size_t(c.E) * c.p * c.I / 16 : 0;
+    case 7: return q ? size_t(c.E) * 4 : 0;
+    case 8: return q ? size_t(c.E) * 4 : 0;
     default: return 0;
   }
 }
@@ -456,10 +528,15 @@ moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weigh
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool act_f32 = c.act == MOE_F32, exp_f32 = c.expert == MOE_F32;
   if (!src) return MOE_ERR_INVALID_ARG;
-  const void* need[] = {src->w_router, src->w_gate, src->w_up, src->w_pool, src->w_unpool,
-                        w_router_out, w13_out, w_pool_out, w_unpool_out};
+  const bool nvf4 = c.expert == MOE_NVFP4;
+  if (nvf4 && (w13_out || w2_out)) return MOE_ERR_INVALID_ARG;
+  const void* need[] = {src->w_router, src->w_pool, src->w_unpool, w_router_out, w_pool_out,
+                        w_unpool_out};
   for (const void* p : need)
     if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  if (!nvf4 && (!src->w_gate || !src->w_up || !w13_out || !aligned16(src->w_gate) ||
+                !aligned16(src->w_up) || !aligned16(w13_out)))
+    return MOE_ERR_INVALID_ARG;
   if (exp_f32 && (!src->w_down || !w2_out || !aligned16(src->w_down) || !aligned16(w2_out)))
     return MOE_ERR_INVALID_ARG;
   auto copy = [&](const void* s, void* d, size_t bytes, bool tf32) {
@@ -472,16 +549,54 @@ moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weigh
   MOE_TRY(copy(src->w_router, w_router_out, size_t(c.E) * c.d * 4, true));
   const int es = exp_f32 ? 4 : 2;
   const unsigned rows13 = static_cast<unsigned>(c.E) * 2u * c.I;
-  if (exp_f32)
-    pack_w13_kernel<CONV_TF32><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
-  else
-    pack_w13_kernel<CONV_BF16_TO_F16><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
-  MOE_TRY(last_launch());
+  if (!nvf4) {
+    if (exp_f32)
+      pack_w13_kernel<CONV_TF32><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
+    else
+      pack_w13_kernel<CONV_BF16_TO_F16><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
+    MOE_TRY(last_launch());
+  }
   if (exp_f32) MOE_TRY(copy(src->w_down, w2_out, size_t(c.E) * c.p * c.I * 4, true));
   const size_t ea = act_f32 ? 4 : 2;
   MOE_TRY(copy(src->w_pool, w_pool_out, size_t(c.p) * c.d * ea, act_f32));
   MOE_TRY(copy(src->w_unpool, w_unpool_out, size_t(c.d) * c.p * ea, act_f32));
   return MOE_OK;
+}
+
+moe_status_t moe_quantize_nvfp4(const moe_config_t* cfg, const void* w_gate, const void* w_up,
+                                const void* w_down, uint8_t* w13_out, uint8_t* sf13_out,
+                                float* gs13_out, uint8_t* w2_out, uint8_t* sf2_out,
+                                float* gs2_out, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  const moe_config_t& c = *cfg;
+  if (c.expert != MOE_NVFP4) return MOE_ERR_INVALID_ARG;
+  const void* need[] = {w_gate, w_up, w_down, w13_out, sf13_out, gs13_out, w2_out, sf2_out,
+                        gs2_out};
+  for (const void* p : need)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const size_t E = c.E, I = c.I, p = c.p;
+  // global scales: the outputs first hold each expert's amax (FP32 bits), then g
+  unsigned* a13 = reinterpret_cast<unsigned*>(gs13_out);
+  unsigned* a2 = reinterpret_cast<unsigned*>(gs2_out);
+  zero_u32_kernel<<<1, 256, 0, st>>>(a13, c.E);
+  zero_u32_kernel<<<1, 256, 0, st>>>(a2, c.E);
+  MOE_TRY(last_launch());
+  const dim3 grid(64, c.E);
+  amax_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w_gate), I * p, I * p, a13);
+  amax_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w_up), I * p, I * p, a13);
+  amax_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(w_down), p * I, p * I, a2);
+  MOE_TRY(last_launch());
+  global_scale_kernel<<<(c.E + 255) / 256, 256, 0, st>>>(a13, gs13_out, c.E);
+  global_scale_kernel<<<(c.E + 255) / 256, 256, 0, st>>>(a2, gs2_out, c.E);
+  MOE_TRY(last_launch());
+  quantize_weight_kernel<<<static_cast<unsigned>(E * 2 * I), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(w_gate), static_cast<const __nv_bfloat16*>(w_up),
+      w13_out, sf13_out, gs13_out, static_cast<int>(2 * I), c.p, NV_BN / 2);
+  MOE_TRY(last_launch());
+  quantize_weight_kernel<<<static_cast<unsigned>(E * p), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(w_down), nullptr, w2_out, sf2_out, gs2_out, c.p, c.I, 0);
+  return last_launch();
 }
 
 moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
@@ -560,9 +675,9 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally) {
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n) {
   if (validate(cfg) != MOE_OK || !offsets || n <= 0) return 0;
   const WsLayout L = ws_layout(*cfg);
-  const size_t all[12] = {L.h32, L.h16, L.ids, L.wts, L.pooled, L.row_off,
-                          L.src, L.inv, L.a_perm, L.s, L.y, L.c};
-  const int m = n < 12 ? n : 12;
+  const size_t all[16] = {L.h32, L.h16, L.ids, L.wts, L.pooled, L.row_off, L.src, L.inv,
+                          L.a_perm, L.s, L.y, L.c, L.sf_u, L.sf_s, L.alpha, L.row_cnt};
+  const int m = n < 16 ? n : 16;
   for (int i = 0; i < m; ++i) offsets[i] = all[i];
   return m;
 }

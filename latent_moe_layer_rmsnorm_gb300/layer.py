@@ -12,7 +12,7 @@ from . import _lib as L
 from .synth import Shape
 
 _DT = {"bf16": L.MOE_BF16, "f32": L.MOE_F32, "nvfp4": L.MOE_NVFP4}
-_TORCH = {"bf16": torch.bfloat16, "f32": torch.float32}
+_TORCH = {"bf16": torch.bfloat16, "f32": torch.float32, "nvfp4": torch.bfloat16}
 
 
 def make_config(shape: Shape, T: int | None = None, out: str = "bf16",
@@ -59,14 +59,29 @@ class LatentMoE:
 
         # packed operand dtypes: FP16 for BF16 configurations, FP32 (TF32-rounded) else
         op = torch.float32 if shape.act == "f32" else torch.float16
+        nvf4 = shape.expert == "nvfp4"
         self.w_router = buf(L.PACK_ROUTER, torch.float32)
-        self.w13 = buf(L.PACK_W13, op)
-        w2p, poolp, unpoolp = buf(L.PACK_W2, op), buf(L.PACK_POOL, op), buf(L.PACK_UNPOOL, op)
+        if nvf4:
+            self.w13, w2p = buf(L.PACK_W13, torch.uint8), buf(L.PACK_W2, torch.uint8)
+            self.sf13, self.sf2 = buf(L.PACK_SF13, torch.uint8), buf(L.PACK_SF2, torch.uint8)
+            self.gs13, self.gs2 = buf(L.PACK_GS13, torch.float32), buf(L.PACK_GS2, torch.float32)
+            self.gs_act2 = w["gs_act2"].float().contiguous()
+        else:
+            self.w13, w2p = buf(L.PACK_W13, op), buf(L.PACK_W2, op)
+            self.sf13 = self.sf2 = self.gs13 = self.gs2 = self.gs_act2 = None
+        poolp, unpoolp = buf(L.PACK_POOL, op), buf(L.PACK_UNPOOL, op)
         src = L.moe_canonical_weights_t(
             w_router=_ptr(w["w_router"]), w_pool=_ptr(w["w_pool"]), w_gate=_ptr(w["w_gate"]),
             w_up=_ptr(w["w_up"]), w_down=_ptr(w["w_down"]), w_unpool=_ptr(w["w_unpool"]))
-        L.check(L.moe_pack_weights(cfg, src, _ptr(self.w_router), _ptr(self.w13), _ptr(w2p),
-                                   _ptr(poolp), _ptr(unpoolp), _stream()), "moe_pack_weights")
+        L.check(L.moe_pack_weights(cfg, src, _ptr(self.w_router),
+                                   None if nvf4 else _ptr(self.w13),
+                                   None if nvf4 else _ptr(w2p), _ptr(poolp), _ptr(unpoolp),
+                                   _stream()), "moe_pack_weights")
+        if nvf4:
+            L.check(L.moe_quantize_nvfp4(cfg, _ptr(w["w_gate"]), _ptr(w["w_up"]),
+                                         _ptr(w["w_down"]), _ptr(self.w13), _ptr(self.sf13),
+                                         _ptr(self.gs13), _ptr(w2p), _ptr(self.sf2),
+                                         _ptr(self.gs2), _stream()), "moe_quantize_nvfp4")
         self.w2 = w2p if w2p is not None else w["w_down"]
         self.w_pool = poolp if poolp is not None else w["w_pool"]
         self.w_unpool = unpoolp if unpoolp is not None else w["w_unpool"]
@@ -76,7 +91,9 @@ class LatentMoE:
         self.W = L.moe_weights_t(g_in=_ptr(self.g_in), w_router=_ptr(self.w_router),
                                  w_pool=_ptr(self.w_pool), g_pool=_ptr(self.g_pool),
                                  w13=_ptr(self.w13), w2=_ptr(self.w2), g_exp=_ptr(self.g_exp),
-                                 w_unpool=_ptr(self.w_unpool))
+                                 w_unpool=_ptr(self.w_unpool), sf13=_ptr(self.sf13),
+                                 sf2=_ptr(self.sf2), gs13=_ptr(self.gs13), gs2=_ptr(self.gs2),
+                                 gs_act2=_ptr(self.gs_act2))
         if keep_canonical:
             self.canonical = w
         self.ws = None
@@ -143,13 +160,22 @@ class LatentMoE:
         sh, k = self.shape, self.shape.top_k
         f32 = sh.act == "f32"
         op = torch.float32 if f32 else torch.float16
+        if sh.expert == "nvfp4":
+            R = 128 * ((T * k + 127) // 128 + sh.E)
+            rows = {"src": ((R,), torch.int32), "a_perm": ((R, sh.p // 2), torch.uint8),
+                    "s": ((R, sh.I // 2), torch.uint8), "y": ((R, sh.p), torch.float32),
+                    "sf_u": ((R * sh.p // 16,), torch.uint8),
+                    "sf_s": ((R * sh.I // 16,), torch.uint8), "alpha": ((R,), torch.float32)}
+        else:
+            rows = {"src": ((T * k,), torch.int32), "a_perm": ((T * k, sh.p), op),
+                    "s": ((T * k, sh.I), torch.float32 if f32 else torch.bfloat16),
+                    "y": ((T * k, sh.p), torch.float32)}
         spec = {"h32": ((T, sh.d), torch.float32), "h16": ((T, sh.d), torch.float16),
                 "ids": ((T, k), torch.int32), "w": ((T, k), torch.float32),
                 "pooled": ((T, sh.p), torch.float32), "row_off": ((sh.E + 1,), torch.int32),
-                "src": ((T * k,), torch.int32), "inv": ((T * k,), torch.int32),
-                "a_perm": ((T * k, sh.p), op),
-                "s": ((T * k, sh.I), torch.float32 if f32 else torch.bfloat16),
-                "y": ((T * k, sh.p), torch.float32), "c": ((T, sh.p), op)}
+                "row_cnt": ((sh.E + 1,), torch.int32), "inv": ((T * k,), torch.int32),
+                "c": ((T, sh.p), op)}
+        spec.update(rows)
         shape, dtype = spec[name]
         off = L.moe_workspace_offsets(self.config(T))[name] + self.ws_off
         n = 1

@@ -101,9 +101,9 @@ def e2m1_encode(v) -> np.ndarray:
     dist = np.abs(a[..., None] - E2M1_MAGNITUDES)
     nearest = dist == dist.min(axis=-1, keepdims=True)
     best = np.argmin(np.where(nearest, np.arange(8) & 1, 2), axis=-1)
-    # a value that rounds to zero is encoded as +0
-    sign = (v < 0) & (best > 0)
-    return (best | np.where(sign, 8, 0)).astype(np.uint8)
+    # the sign bit follows the input's sign, also when the magnitude rounds to zero
+    # (as for IEEE conversions: -0.1 -> -0)
+    return (best | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
 
 
 # ---- UE4M3 (block scale) ----------------------------------------------------------

@@ -50,7 +50,8 @@ def test_e2m1_ties_and_saturation():
         assert F.e2m1_decode(F.e2m1_encode(np.array([-v])))[0] == -want, v
     assert F.e2m1_decode(F.e2m1_encode(np.array([100.0])))[0] == 6.0
     assert F.e2m1_decode(F.e2m1_encode(np.array([-7.0])))[0] == -6.0
-    assert F.e2m1_encode(np.array([-0.1]))[0] == 0
+    assert F.e2m1_encode(np.array([-0.1]))[0] == 8          # -0 keeps its sign
+    assert F.e2m1_encode(np.array([0.1]))[0] == 0
 
 
 def test_ue4m3_table_and_round_trip():

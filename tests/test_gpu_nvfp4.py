@@ -1,0 +1,185 @@
+"""NVFP4 experts on the GPU against the oracle ("SGLang and Miles Add Day-0 Support for
+Muse Spark Open", section "NVFP4 as a third MMA kind"; "The NVFP4 requantization
+reciprocal table").
+
+* weight quantiser: codes, block scales and global scales bit-exact (integer output;
+  both sides decide in the same FP32 op order);
+* stage-wise: the activation quantiser, the block-scaled gate/up GEMM with its SwiGLU +
+  requantisation epilogue and the block-scaled down GEMM, each from the GPU's own input;
+* end to end against the oracle that dequantises the same NVFP4 weights and emulates
+  the activation quantisation: max|gpu - ref| / rms(ref) <= 3e-2 (the NVFP4 bound).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import formats as F
+from oracle import nvfp4 as Q
+from harness import fix_margins, oracle_view, rel_err, to_np
+from latent_moe_layer_rmsnorm_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_NVFP4 = 3e-2
+SMALL = synth.Shape("nvfp4_small", T=200, d=1024, p=512, E=8, top_k=4, I=512, expert="nvfp4")
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from latent_moe_layer_rmsnorm_gb300 import build
+    build.build()
+
+
+def unchunk_sf(sf: np.ndarray, rows: int, K: int) -> np.ndarray:
+    """Chunked scale layout (see latent_moe.h) -> [rows, K/16]."""
+    r = np.arange(rows)[:, None]
+    g = np.arange(K // 16)[None, :]
+    off = ((r // 128) * (K // 64) + g // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + g % 4
+    return sf[off]
+
+
+def unpack_codes(b: np.ndarray) -> np.ndarray:
+    """[rows, K/2] bytes -> [rows, K] E2M1 codes (even element in the low nibble)."""
+    out = np.empty((b.shape[0], b.shape[1] * 2), dtype=np.uint8)
+    out[:, 0::2] = b & 15
+    out[:, 1::2] = b >> 4
+    return out
+
+
+def w13_row_map(I: int) -> np.ndarray:
+    """Packed gate/up row -> row of [gate; up] (interleaved in blocks of 64)."""
+    r = np.arange(2 * I)
+    b, i = r // 128, r % 128
+    return np.where(i < 64, b * 64 + i, I + b * 64 + (i - 64))
+
+
+def build(shape, seed):
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+    inp = synth.make_inputs(shape, seed=seed, device="cpu")
+    fix_margins(inp, shape, seed=seed)
+    dev = {k: v.cuda() for k, v in inp.items()}
+    return inp, dev, LatentMoE(shape, dev, out="f32")
+
+
+def test_weight_quantizer_bit_exact():
+    need_gpu()
+    shape = SMALL
+    inp, dev, layer = build(shape, 0)
+    torch.cuda.synchronize()
+    E, I, p = shape.E, shape.I, shape.p
+    codes13 = layer.w13.cpu().numpy().reshape(E, 2 * I, p // 2)
+    sf13 = layer.sf13.cpu().numpy()
+    codes2 = layer.w2.cpu().numpy().reshape(E, p, I // 2)
+    sf2 = layer.sf2.cpu().numpy()
+    gs13, gs2 = layer.gs13.cpu().numpy(), layer.gs2.cpu().numpy()
+    view = oracle_view(inp)
+    rmap = w13_row_map(I)
+    sf13_rows = unchunk_sf(sf13, E * 2 * I, p).reshape(E, 2 * I, p // 16)
+    sf2_rows = unchunk_sf(sf2, E * p, I).reshape(E, p, I // 16)
+    for e in range(E):
+        ref = oracle.nvfp4_expert_weights(view["w_gate"][e], view["w_up"][e], view["w_down"][e])
+        assert gs13[e] == ref["g13"] and gs2[e] == ref["g2"], e
+        np.testing.assert_array_equal(unpack_codes(codes13[e]), ref["q13"][rmap])
+        np.testing.assert_array_equal(sf13_rows[e], ref["sf13"][rmap])
+        np.testing.assert_array_equal(unpack_codes(codes2[e]), ref["q2"])
+        np.testing.assert_array_equal(sf2_rows[e], ref["sf2"])
+
+
+def test_nvfp4_stages_and_layer():
+    need_gpu()
+    shape = SMALL
+    inp, dev, layer = build(shape, 1)
+    T, k, E, I, p = shape.T, shape.top_k, shape.E, shape.I, shape.p
+    out = layer.forward(dev["x"])
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    view = oracle_view(inp)
+    ref = oracle.moe_forward(view, top_k=k, eps=shape.eps, act="bf16", expert="nvfp4",
+                             out="f32", return_parts=True)
+    ids = layer.intermediate("ids", T).cpu().numpy()
+    np.testing.assert_array_equal(ids, ref["ids"])
+    row_off = layer.intermediate("row_off", T).cpu().numpy().astype(np.int64)
+    row_cnt = layer.intermediate("row_cnt", T).cpu().numpy().astype(np.int64)
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    np.testing.assert_array_equal(row_cnt[:E], counts)
+    assert np.all(row_off[:E] % 128 == 0)                   # 128-aligned expert rows
+    inv = layer.intermediate("inv", T).cpu().numpy().astype(np.int64).reshape(T, k)
+    pooled = to_np(layer.intermediate("pooled", T))
+    R = 128 * ((T * k + 127) // 128 + E)
+
+    # activation quantiser, from the GPU's pooled rows
+    u_codes = unpack_codes(layer.intermediate("a_perm", T).cpu().numpy())
+    sf_u = unchunk_sf(layer.intermediate("sf_u", T).cpu().numpy(), R, p)
+    alpha = to_np(layer.intermediate("alpha", T))
+    u32 = F.fp32(oracle.rmsnorm(pooled, view["g_pool"], shape.eps))
+    qu, sfu, al = Q.quantize_rows(u32)
+    rows_t = inv.reshape(-1)
+    tok = np.repeat(np.arange(T), k)
+    np.testing.assert_allclose(alpha[rows_t], al[tok], rtol=2e-6)
+    deq_gpu = Q.dequantize(u_codes[rows_t], sf_u[rows_t], alpha[rows_t])
+    deq_ref = Q.dequantize(qu[tok], sfu[tok], al[tok])
+    code_match = float(np.mean(u_codes[rows_t] == qu[tok]))
+    # a value near a rounding boundary may land one E2M1 step (<= 2 x scale) away, and a
+    # block maximum near a UE4M3 boundary may change its block's scale by one step (1/8)
+    scale = np.maximum(F.ue4m3_decode(sfu[tok]), F.ue4m3_decode(sf_u[rows_t]))
+    step = scale.repeat(16, axis=1) * al[tok][:, None] * 2.0
+    assert np.all(np.abs(deq_gpu - deq_ref) <= step * (1 + 1e-6) + 0.13 * np.abs(deq_ref))
+    assert code_match > 0.99, code_match
+
+    # gate/up GEMM + SwiGLU + requantisation, from the GPU's own u
+    s_codes = unpack_codes(layer.intermediate("s", T).cpu().numpy())
+    sf_s = unchunk_sf(layer.intermediate("sf_s", T).cpu().numpy(), R, I)
+    y = to_np(layer.intermediate("y", T))
+    gs_act2 = view["gs_act2"]
+    s_match, s_total, y_err = 0, 0, 0.0
+    for e in range(E):
+        rows = np.arange(row_off[e], row_off[e] + row_cnt[e])
+        if len(rows) == 0:
+            continue
+        wq = oracle.nvfp4_expert_weights(view["w_gate"][e], view["w_up"][e], view["w_down"][e])
+        u_deq = Q.dequantize(u_codes[rows], sf_u[rows], alpha[rows])
+        s_ref = F.fp32(oracle.expert_swiglu(u_deq, wq["gate"], wq["up"]))
+        qs, sfs = Q.quantize_static(s_ref, gs_act2[e])
+        s_match += int(np.sum(s_codes[rows] == qs))
+        s_total += qs.size
+        d_gpu = Q.dequantize(s_codes[rows], sf_s[rows], np.float32(gs_act2[e]))
+        d_ref = Q.dequantize(qs, sfs, np.float32(gs_act2[e]))
+        stp = np.maximum(F.ue4m3_decode(sfs), F.ue4m3_decode(sf_s[rows])).repeat(16, axis=1)
+        assert np.all(np.abs(d_gpu - d_ref)
+                      <= 2.0 * stp * gs_act2[e] * (1 + 1e-6) + 0.13 * np.abs(d_ref) + 1e-12)
+        # down GEMM, from the GPU's own s
+        y_ref = oracle.expert_down(d_gpu, wq["down"])
+        y_err = max(y_err, rel_err(y[rows], y_ref))
+    assert s_match / s_total > 0.97, s_match / s_total
+    assert y_err < 2e-5, y_err
+
+    e2e = rel_err(to_np(out), ref["out"])
+    print(f"nvfp4: u codes {code_match:.4f} equal, s codes {s_match / s_total:.4f} equal, "
+          f"y {y_err:.1e}, end to end {e2e:.2e}")
+    assert e2e <= TOL_NVFP4
+
+
+@pytest.mark.slow
+def test_nvfp4_prefill_chunk_sampled():
+    """The NVFP4 prefill chunk at full size: ids of all tokens exactly, sampled tokens in
+    full against the NVFP4 oracle."""
+    need_gpu()
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+    shape = synth.PREFILL_NVFP4
+    inp = synth.make_inputs(shape, seed=3, device="cuda")
+    fix_margins(inp, shape, seed=3)
+    layer = LatentMoE(shape, inp, out="f32")
+    out = layer.forward(inp["x"])
+    ids, _ = layer.route(inp["x"])
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    tok = [0, 4097, 9000, 16383]
+    view = oracle_view(inp, lazy=True)
+    ref = oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act="bf16",
+                             expert="nvfp4", out="f32", tokens=tok, return_parts=True)
+    np.testing.assert_array_equal(ids.cpu().numpy()[tok], ref["ids"])
+    err = rel_err(to_np(out[torch.as_tensor(tok, device=out.device)]), ref["out"])
+    print(f"nvfp4 prefill sampled {tok}: {err:.2e}")
+    assert err <= TOL_NVFP4
