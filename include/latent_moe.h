@@ -78,11 +78,17 @@ typedef enum {
  *   expert MOE_BF16 or MOE_F32 (equal to act), or MOE_NVFP4 with act = MOE_BF16
  *          (then p and I must be multiples of 256)
  *   out    MOE_BF16 or MOE_F32: dtype of the layer output
- *   flags  0, or MOE_FLAG_TEST_TIMEOUT (other bits must be zero)                  */
+ *   flags  0, MOE_FLAG_TEST_TIMEOUT, MOE_FLAG_WEIGHT_TILES (other bits must be zero) */
 /* Test hook for the error path: the gate/up GEMM never issues its first operand load,
  * so its MMA wait runs out after 20 ms; the call's kernels then end early and
  * moe_read_status reports MOE_ERR_TIMEOUT.  Outputs are undefined.  Tests only. */
 #define MOE_FLAG_TEST_TIMEOUT 0x80000000u
+/* Run the BF16 / FP32 expert GEMMs with weight rows on the MMA's M side and each
+ * expert's tokens on N (tiles shrink to the tokens present, in steps of 16) instead of
+ * the default 128-token tiles on M.  Same results.  It removes the partly empty last
+ * tile of each expert, but on a GB300 the expert GEMMs are bound by operand delivery
+ * into shared memory, not by MMA work, and the default is faster at prefill sizes. */
+#define MOE_FLAG_WEIGHT_TILES 0x40000000u
 typedef struct {
   int32_t T, d, p, E, top_k, I;
   float eps;

@@ -25,6 +25,7 @@ MOE_BF16 = 1
 MOE_NVFP4 = 2
 
 MOE_FLAG_TEST_TIMEOUT = 0x80000000
+MOE_FLAG_WEIGHT_TILES = 0x40000000
 
 PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL, PACK_SF13, PACK_SF2, PACK_GS13, \
     PACK_GS2 = range(9)

@@ -49,6 +49,9 @@ struct GemmParams {
   int K;        // reduction length in elements
   int bn;       // tile width: multiple of 16, <= 256
   int groups;   // 0 = dense; > 0 = grouped over this many experts
+  int ksplit;   // dense only: K is split into this many slices (1 = no split); slice s
+                // writes its FP32 partial at out + s * split_stride
+  size_t split_stride;
   const int* row_off;  // grouped: [groups+1] first A row of each expert (device)
   const int* mt_off;   // grouped: [groups+1] prefix sum of 128-row tiles (device)
   const int* row_cnt;  // grouped: [groups] rows of each expert (device)
@@ -96,11 +99,12 @@ struct TileCoord {
   int valid;   // rows of the tile that belong to it (<= 128)
   int n_blk;   // tile index along N
   int e;       // expert (grouped), 0 for dense
+  int split;   // K slice (dense split-K), 0 otherwise
 };
 
 __device__ __forceinline__ int gemm_num_tiles(const GemmParams& P, const GemmSmem* S) {
   const int nb = P.N / P.bn;
-  if (P.groups == 0) return ((P.M + GEMM_BM - 1) / GEMM_BM) * nb;
+  if (P.groups == 0) return ((P.M + GEMM_BM - 1) / GEMM_BM) * nb * P.ksplit;
   return S->mt_off[P.groups] * nb;
 }
 
@@ -110,14 +114,17 @@ __device__ __forceinline__ TileCoord gemm_tile(const GemmParams& P, const GemmSm
   const int nb = P.N / P.bn;
   TileCoord c;
   if (P.groups == 0) {
-    const int m_blk = t / nb;
-    c.n_blk = t - m_blk * nb;
+    c.split = t % P.ksplit;          // consecutive tiles: the slices of one output tile
+    const int o = t / P.ksplit;
+    const int m_blk = o / nb;
+    c.n_blk = o - m_blk * nb;
     c.a_row = m_blk * GEMM_BM;
     c.b_row = c.n_blk * P.bn;
     c.valid = min(GEMM_BM, P.M - c.a_row);
     c.e = 0;
     return c;
   }
+  c.split = 0;
   // largest e with mt_off[e] * nb <= t (experts with no rows have empty ranges)
   int lo = 0, hi = P.groups - 1;
   while (lo < hi) {
@@ -180,18 +187,20 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == EPI_STORE) {
-    const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * P.bn;
-    for (int c0 = 0; c0 < P.bn; c0 += 32) {
+    const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * P.bn +
+                        static_cast<size_t>(tc.split) * P.split_stride;
+    for (int c0 = 0; c0 < P.bn; c0 += 32) {    // bn is a multiple of 16
+      const bool two = c0 + 16 < P.bn;          // uniform across the warp
       uint32_t a[16], b[16];
       tmem_ld16(taddr + c0, a);
-      tmem_ld16(taddr + c0 + 16, b);
+      if (two) tmem_ld16(taddr + c0 + 16, b);
       tmem_ld_wait();
       float va[16], vb[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) { va[i] = __uint_as_float(a[i]); vb[i] = __uint_as_float(b[i]); }
       if (row_ok) {
         store16(P.out, base + c0, P.out_fmt, va);
-        store16(P.out, base + c0 + 16, P.out_fmt, vb);
+        if (two) store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
@@ -294,7 +303,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const uint32_t tmem_base = S->tmem_base;
   const int num_tiles = gemm_num_tiles(P, S);
   constexpr bool TF32 = KIND == OP_TF32;
-  const int kblocks = P.K / (TF32 ? 32 : 64);   // one 128-byte slice per stage
+  const int kblocks = P.K / (TF32 ? 32 : 64) / (P.groups == 0 ? P.ksplit : 1);
   const uint64_t limit = P.timeout_ns;
   volatile int* abort_flag = &S->abort_flag;
 
@@ -317,7 +326,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           skip = false;   // test hook: this stage never fills, so the MMA wait runs out
         } else {
           mbar_arrive_expect_tx(&S->full[stage], bytes);
-          const int kc = kb * (TF32 ? 32 : 64);
+          const int kc = (tc.split * kblocks + kb) * (TF32 ? 32 : 64);
           tma_load_2d(sA + stage * GEMM_A_STAGE, &tmA, &S->full[stage], kc, tc.a_row);
           tma_load_2d(sB + stage * GEMM_B_STAGE, &tmB, &S->full[stage], kc, tc.b_row);
           last_phase[stage] = static_cast<int>(phase);

@@ -150,7 +150,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
 __global__ void __launch_bounds__(256)
     dispatch_scan_kernel(int* __restrict__ chunk_counts, int nchunks, int E,
                          int* __restrict__ row_off, int* __restrict__ mt_off,
-                         int* __restrict__ row_cnt, int padded) {
+                         int* __restrict__ mt2_off, int* __restrict__ row_cnt, int padded) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
   int running = 0;
@@ -166,16 +166,21 @@ __global__ void __launch_bounds__(256)
   const int mt = (e < E) ? (running + 127) / 128 : 0;
   int mt_total;
   const int mto = block_excl_scan(mt, sh, &mt_total);
+  const int mt2 = (e < E) ? (running + 255) / 256 : 0;    // 256-row tiles
+  int mt2_total;
+  const int mt2o = block_excl_scan(mt2, sh, &mt2_total);
   const int start = padded ? mto * 128 : off;
   if (e < E) {
     row_off[e] = start;
     mt_off[e] = mto;
+    mt2_off[e] = mt2o;
     row_cnt[e] = running;
     for (int c = 0; c < nchunks; ++c) chunk_counts[c * E + e] += start;
   }
   if (e == 0) {
     row_off[E] = padded ? mt_total * 128 : total;
     mt_off[E] = mt_total;
+    mt2_off[E] = mt2_total;
     row_cnt[E] = total;
   }
 }
@@ -427,6 +432,103 @@ __global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __res
   const int n16 = p * elem_bytes / 16;
   for (int c = threadIdx.x; c < n16; c += blockDim.x)
     reinterpret_cast<uint4*>(o)[c] = pack_convert<CONV>(reinterpret_cast<const uint4*>(s)[c]);
+}
+
+// ---- split-K reductions ----------------------------------------------------------------
+// out[i] = sum over s of part[s * n + i], in slice order (deterministic), written as FP32,
+// BF16 or TF32-rounded FP32.  n % 4 == 0.
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, int ksplit, size_t n,
+                                     void* __restrict__ out, int fmt) {
+  for (size_t i = (blockIdx.x * size_t(blockDim.x) + threadIdx.x) * 4; i < n;
+       i += size_t(gridDim.x) * blockDim.x * 4) {
+    // slices in groups of 4 (loads in flight together), summed in a fixed order
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= ksplit; s += 4) {
+      const float4 v0 = *reinterpret_cast<const float4*>(part + (s + 0) * n + i);
+      const float4 v1 = *reinterpret_cast<const float4*>(part + (s + 1) * n + i);
+      const float4 v2 = *reinterpret_cast<const float4*>(part + (s + 2) * n + i);
+      const float4 v3 = *reinterpret_cast<const float4*>(part + (s + 3) * n + i);
+      acc.x += (v0.x + v1.x) + (v2.x + v3.x);
+      acc.y += (v0.y + v1.y) + (v2.y + v3.y);
+      acc.z += (v0.z + v1.z) + (v2.z + v3.z);
+      acc.w += (v0.w + v1.w) + (v2.w + v3.w);
+    }
+    for (; s < ksplit; ++s) {
+      const float4 v = *reinterpret_cast<const float4*>(part + s * n + i);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    if (fmt == 0) {          // BF16
+      uint2 o;
+      o.x = pack_bf16x2(acc.x, acc.y);
+      o.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + i) = o;
+    } else if (fmt == 2) {   // TF32-rounded FP32
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + i) =
+          make_float4(tf32_rna(acc.x), tf32_rna(acc.y), tf32_rna(acc.z), tf32_rna(acc.w));
+    } else {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = acc;
+    }
+  }
+}
+
+// Router logits from split-K partials [ksplit][T][ld] (sum in slice order), then the
+// top-k (descending, ties to the lower id) and the softmax over the chosen logits.
+// One warp per token; lane l owns experts l, l+32, ...
+__global__ void router_reduce_topk_kernel(const float* __restrict__ part, int ksplit, int T,
+                                          int ld, int E, int k, int32_t* __restrict__ ids,
+                                          float* __restrict__ wts) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (t >= T) return;
+  constexpr int PER = 8;                 // E <= 256
+  float v[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) v[j] = 0.f;
+  // all of this lane's experts per slice: 8 independent loads in flight
+  for (int s = 0; s < ksplit; ++s) {
+    const float* row = part + (size_t(s) * T + t) * ld;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E) v[j] += row[e];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < PER; ++j)
+    if (lane + 32 * j >= E) v[j] = -INFINITY;
+  // k rounds of warp arg-max: larger logit wins, equal logits go to the lower id
+  float chosen[MAX_TOPK];
+  int chosen_id[MAX_TOPK];
+  for (int r = 0; r < k; ++r) {
+    float best = -INFINITY;
+    int bid = 0x7FFFFFFF;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane + 32 * j;
+      if (e < E && (v[j] > best || (v[j] == best && e < bid))) { best = v[j]; bid = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
+      if (ob > best || (ob == best && oi < bid)) { best = ob; bid = oi; }
+    }
+    chosen[r] = best;
+    chosen_id[r] = bid;
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (lane + 32 * j == bid) v[j] = -INFINITY;   // remove it (its id is unique)
+  }
+  if (lane == 0) {
+    float z[MAX_TOPK], sum = 0.f;
+    for (int r = 0; r < k; ++r) { z[r] = __expf(chosen[r] - chosen[0]); sum += z[r]; }
+    const float inv = 1.0f / sum;
+    for (int r = 0; r < k; ++r) {
+      ids[size_t(t) * k + r] = chosen_id[r];
+      wts[size_t(t) * k + r] = z[r] * inv;
+    }
+  }
 }
 
 // ---- NVFP4 ------------------------------------------------------------------------------

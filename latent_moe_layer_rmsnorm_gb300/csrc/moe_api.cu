@@ -6,6 +6,7 @@
 #include "../../include/latent_moe.h"
 #include "common.cuh"
 #include "gemm_nvf4.cuh"
+#include "gemm_swap.cuh"
 #include "gemm_tcgen05.cuh"
 #include "kernels_mem.cuh"
 
@@ -98,6 +99,19 @@ moe_status_t device_ready(int* sms) {
     if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_STORE>();
     if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_SWIGLU>();
     if (e == cudaSuccess) e = set_smem_attr<OP_BF16, EPI_STORE>();
+    const int swap_smem = static_cast<int>(swap_smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_swap_kernel<OP_F16, SWAP_SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, swap_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_swap_kernel<OP_BF16, SWAP_STORE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, swap_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_swap_kernel<OP_TF32, SWAP_SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, swap_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_swap_kernel<OP_TF32, SWAP_STORE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, swap_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_SWIGLU_Q>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -130,7 +144,7 @@ moe_status_t validate(const moe_config_t* c) {
   } else if (c->expert != c->act) {
     return MOE_ERR_UNSUPPORTED;
   }
-  if ((c->flags & ~MOE_FLAG_TEST_TIMEOUT) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_WEIGHT_TILES)) != 0) return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED;
   if (c->d % 128 || c->p % 128 || c->I % 128) return MOE_ERR_UNSUPPORTED;
   if (c->d > 32768 || c->p > 8192 || c->I > 32768) return MOE_ERR_UNSUPPORTED;
@@ -140,9 +154,41 @@ moe_status_t validate(const moe_config_t* c) {
   return MOE_OK;
 }
 
+inline int bn_for(int n) { return (n % 256 == 0) ? 256 : 128; }
+
+// K slices for a dense GEMM whose output has too few tiles to fill the GPU (the decode
+// regime): aim for ~128 CTAs, each slice at least 4 K blocks (kblk elements each).
+int split_for(int T, int N, int bn, int K, int kblk) {
+  const int tiles = ((T + GEMM_BM - 1) / GEMM_BM) * (N / bn);
+  if (tiles >= 64) return 1;
+  int ks = 1;
+  while (ks * 2 * tiles <= 128 && K % (ks * 2 * kblk) == 0 && K / (ks * 2) >= 4 * kblk) ks *= 2;
+  return ks;
+}
+
+struct SplitPlan {
+  int router, pool, unpool;
+  size_t part_floats;
+};
+
+SplitPlan split_plan(const moe_config_t& c) {
+  SplitPlan sp{};
+  const int Ep = (c.E + 15) / 16 * 16;
+  const bool f32 = c.act == MOE_F32;
+  sp.router = std::min(split_for(c.T, Ep, Ep, c.d, 32), 32);
+  sp.pool = split_for(c.T, c.p, bn_for(c.p), c.d, f32 ? 32 : 64);
+  sp.unpool = split_for(c.T, c.d, bn_for(c.d), c.p, f32 ? 32 : 64);
+  size_t m = 0;
+  if (sp.router > 1) m = std::max(m, size_t(sp.router) * c.T * Ep);
+  if (sp.pool > 1) m = std::max(m, size_t(sp.pool) * c.T * c.p);
+  if (sp.unpool > 1) m = std::max(m, size_t(sp.unpool) * c.T * c.d);
+  sp.part_floats = m;
+  return sp;
+}
+
 struct WsLayout {
-  size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, row_cnt, src, inv, a_perm,
-      s, y, c, sf_u, sf_s, alpha, total;
+  size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, mt2_off, row_cnt, src, inv,
+      a_perm, s, y, c, sf_u, sf_s, alpha, part, total;
   int nchunks;
   size_t rows;    // dispatched rows (NVFP4: 128-aligned per expert)
 };
@@ -171,6 +217,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.chunk = take(size_t(L.nchunks) * E * 4);
   L.row_off = take((E + 1) * 4);
   L.mt_off = take((E + 1) * 4);
+  L.mt2_off = take((E + 1) * 4);
   L.row_cnt = take((E + 1) * 4);
   L.src = take(R * 4);
   L.inv = take(T * k * 4);
@@ -181,6 +228,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.sf_u = take(q ? R * p / 16 : 0);
   L.sf_s = take(q ? R * I / 16 : 0);
   L.alpha = take(q ? R * 4 : 0);
+  L.part = take(split_plan(c).part_floats * 4);   // split-K partial sums (small T only)
   L.total = off;
   return L;
 }
@@ -209,8 +257,6 @@ inline moe_status_t last_launch() {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-inline int bn_for(int n) { return (n % 256 == 0) ? 256 : 128; }
-
 template <int KIND, int EPI>
 moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& P,
                          int grid, cudaStream_t st) {
@@ -221,6 +267,7 @@ moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
 
 GemmParams base_params(int* status, uint32_t flags) {
   GemmParams P{};
+  P.ksplit = 1;
   P.status = status;
   P.timeout_ns = (flags & MOE_FLAG_TEST_TIMEOUT) ? TEST_WAIT_LIMIT_NS : WAIT_LIMIT_NS;
   return P;
@@ -289,6 +336,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   // ---- stage: router GEMM (TF32) + top-k ------------------------------------------------
   int32_t* ids = route_only ? ids_out : reinterpret_cast<int32_t*>(base + L.ids);
   float* wts = route_only ? w_out : reinterpret_cast<float*>(base + L.wts);
+  const SplitPlan sp = split_plan(c);
+  float* part = reinterpret_cast<float*>(base + L.part);
   if (internal_route) {
     const int bn = (E_ + 15) / 16 * 16;
     CUtensorMap ta, tb;
@@ -297,8 +346,16 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = bn; P.K = d; P.bn = bn; P.groups = 0;
-    P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
-    MOE_TRY((launch_gemm<OP_TF32, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st)));
+    if (sp.router > 1) {     // small T: K slices -> partial logits -> sum + top-k
+      P.ksplit = sp.router; P.split_stride = size_t(T) * bn;
+      P.out = part; P.ld_out = bn; P.out_fmt = OUT_F32;
+      MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, std::min(sms, mtiles * sp.router), st)));
+      router_reduce_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(part, sp.router, T, bn, E_, k, ids, wts);
+      MOE_TRY(last_launch());
+    } else {
+      P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
+      MOE_TRY((launch_gemm<OP_TF32, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st)));
+    }
   } else {
     ids = const_cast<int32_t*>(ids_in);
     wts = const_cast<float*>(w_in);
@@ -317,9 +374,16 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = p; P.K = d; P.bn = bn; P.groups = 0;
     P.out = pooled; P.ld_out = p; P.out_fmt = OUT_F32;
-    const int grid = std::min(sms, mtiles * (p / bn));
+    if (sp.pool > 1) { P.ksplit = sp.pool; P.split_stride = size_t(T) * p; P.out = part; }
+    const int grid = std::min(sms, mtiles * (p / bn) * sp.pool);
     if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
+    if (sp.pool > 1) {
+      const size_t n = size_t(T) * p;
+      splitk_reduce_kernel<<<static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096)), 256, 0, st>>>(
+          part, sp.pool, n, pooled, OUT_F32);
+      MOE_TRY(last_launch());
+    }
   }
   E.mark(3);
 
@@ -328,6 +392,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   int* chunk = reinterpret_cast<int*>(base + L.chunk);
   int* row_off = reinterpret_cast<int*>(base + L.row_off);
   int* mt_off = reinterpret_cast<int*>(base + L.mt_off);
+  int* mt2_off = reinterpret_cast<int*>(base + L.mt2_off);
   int* row_cnt = reinterpret_cast<int*>(base + L.row_cnt);
   int* src = reinterpret_cast<int*>(base + L.src);
   int* inv = reinterpret_cast<int*>(base + L.inv);
@@ -337,8 +402,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   float* alpha = reinterpret_cast<float*>(base + L.alpha);
   dispatch_hist_kernel<<<L.nchunks, MEM_THREADS, 0, st>>>(ids, rows, E_, chunk, status);
   MOE_TRY(last_launch());
-  dispatch_scan_kernel<<<1, 256, 0, st>>>(chunk, L.nchunks, E_, row_off, mt_off, row_cnt,
-                                          nvf4 ? 1 : 0);
+  dispatch_scan_kernel<<<1, 256, 0, st>>>(chunk, L.nchunks, E_, row_off, mt_off, mt2_off,
+                                          row_cnt, nvf4 ? 1 : 0);
   MOE_TRY(last_launch());
   dispatch_scatter_kernel<<<L.nchunks, 32, 0, st>>>(ids, rows, E_, chunk, inv, src);
   MOE_TRY(last_launch());
@@ -371,6 +436,23 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
     gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
     MOE_TRY(last_launch());
+  } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
+    // weights on the MMA's M side (256-row W13 blocks: 128 gate + 128 up), tokens on N
+    CUtensorMap tw, tx;
+    if (!make_tmap(&tw, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, 256) ||
+        !make_tmap(&tx, a_perm, k_up, p, rows, 128))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.N = 2 * I; P.K = p; P.bn = 256; P.groups = E_;
+    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
+    P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
+    P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
+    const int grid = std::min(sms, max_mt * (2 * I / 256));
+    if (exp_f32)
+      gemm_swap_kernel<OP_TF32, SWAP_SWIGLU><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
+    else
+      gemm_swap_kernel<OP_F16, SWAP_SWIGLU><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
+    MOE_TRY(last_launch());
   } else {
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, a_perm, k_up, p, rows, GEMM_BM) ||
@@ -401,6 +483,23 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
     const int grid = std::min(sms, max_mt * (p / NV_BN));
     gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    MOE_TRY(last_launch());
+  } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
+    // weights on M (128 rows of p), up to 256 tokens on N
+    CUtensorMap tw, tx;
+    if (!make_tmap(&tw, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128) ||
+        !make_tmap(&tx, s_buf, k_down, I, rows, 256))
+      return MOE_ERR_CUDA;
+    GemmParams P = base_params(status, c.flags);
+    P.N = p; P.K = I; P.bn = 128; P.groups = E_;
+    P.row_off = row_off; P.mt_off = mt2_off; P.row_cnt = row_cnt;
+    P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32;
+    const int max_mt2 = (rows + 255) / 256 + E_;
+    const int grid = std::min(sms, max_mt2 * (p / 128));
+    if (exp_f32)
+      gemm_swap_kernel<OP_TF32, SWAP_STORE><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
+    else
+      gemm_swap_kernel<OP_BF16, SWAP_STORE><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
     MOE_TRY(last_launch());
   } else {
     CUtensorMap ta, tb;
@@ -437,9 +536,18 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = d; P.K = p; P.bn = bn; P.groups = 0;
     P.out = out; P.ld_out = d; P.out_fmt = c.out == MOE_F32 ? OUT_F32 : OUT_BF16;
-    const int grid = std::min(sms, mtiles * (d / bn));
+    if (sp.unpool > 1) {
+      P.ksplit = sp.unpool; P.split_stride = size_t(T) * d; P.out = part; P.out_fmt = OUT_F32;
+    }
+    const int grid = std::min(sms, mtiles * (d / bn) * sp.unpool);
     if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
+    if (sp.unpool > 1) {
+      const size_t n = size_t(T) * d;
+      splitk_reduce_kernel<<<static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096)), 256, 0, st>>>(
+          part, sp.unpool, n, out, c.out == MOE_F32 ? OUT_F32 : OUT_BF16);
+      MOE_TRY(last_launch());
+    }
   }
   E.mark(8);
   return MOE_OK;
@@ -668,8 +776,10 @@ const char* moe_stage_name(int stage) {
 
 int moe_forward_launches(const moe_config_t* cfg, int route_internally) {
   if (validate(cfg) != MOE_OK || cfg->T == 0) return 0;
-  // norm, [router], pooler, 4 dispatch kernels, gate/up, down, combine, unpooler
-  return 10 + (route_internally ? 1 : 0);
+  // norm, [router], pooler, 4 dispatch kernels, gate/up, down, combine, unpooler,
+  // plus one reduction per split-K GEMM
+  const SplitPlan sp = split_plan(*cfg);
+  return 10 + (route_internally ? 1 + (sp.router > 1) : 0) + (sp.pool > 1) + (sp.unpool > 1);
 }
 
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n) {

@@ -107,8 +107,14 @@ def test_host_side_errors_before_any_launch():
     assert L.moe_forward(c0, W, FAKE, None, None, FAKE, FAKE, L.moe_workspace_size(c0), None) \
         == L.MOE_OK
     assert L.moe_forward_launches(c0, True) == 0
-    assert L.moe_forward_launches(c, True) == 11
-    assert L.moe_forward_launches(c, False) == 10
+    big = cfg(T=16384)                       # enough output tiles: no split-K reductions
+    assert L.moe_forward_launches(big, True) == 11
+    assert L.moe_forward_launches(big, False) == 10
+    # few tokens at full widths: the router, pooler and unpooler split K and add one
+    # reduction each
+    dec = cfg(T=64, d=8192, p=4096, E=256, top_k=8, I=4096)
+    assert L.moe_forward_launches(dec, True) == 14
+    assert L.moe_forward_launches(dec, False) == 12
 
 
 def test_stage_names_and_status_strings():

@@ -353,3 +353,24 @@ def test_empty_and_crowded_experts():
     check_dispatch(layer, T, ids.numpy())
     check_stagewise(layer, oracle_view(inp), shape, T, ids.numpy(), w.numpy(), out)
     assert rel_err(to_np(out), ref) <= tol_for(shape)
+
+
+@pytest.mark.parametrize("name", ["mid_bf16", "tiny_f32"])
+def test_weight_tile_variant_matches(name):
+    """The expert GEMMs with weight rows on the MMA's M side (MOE_FLAG_WEIGHT_TILES) pass
+    the same stage-wise checks as the default 128-token tiles, and both variants agree
+    to FP32 accumulation noise."""
+    need_gpu()
+    from latent_moe_layer_rmsnorm_gb300 import _lib as L
+    shape = SHAPES[name]
+    inp = make_case(shape, seed=21)
+    layer, dev = gpu_layer(shape, inp, out="f32")
+    a = layer.forward(dev["x"]).clone()
+    b = layer.forward(dev["x"], flags=L.MOE_FLAG_WEIGHT_TILES).clone()
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    T = shape.T
+    ids = layer.intermediate("ids", T).cpu().numpy()
+    w = to_np(layer.intermediate("w", T))
+    check_stagewise(layer, oracle_view(inp), shape, T, ids, w, b)
+    assert rel_err(to_np(b), to_np(a)) <= tol_for(shape)
