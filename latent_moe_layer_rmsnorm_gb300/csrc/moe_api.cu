@@ -6,6 +6,7 @@
 #include "../../include/latent_moe.h"
 #include "common.cuh"
 #include "gemm_nvf4.cuh"
+#include "gemm_pair.cuh"
 #include "gemm_swap.cuh"
 #include "gemm_tcgen05.cuh"
 #include "kernels_mem.cuh"
@@ -120,6 +121,22 @@ moe_status_t device_ready(int* sms) {
       e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_F32>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_smem_bytes()));
+    const int pair_smem = static_cast<int>(pair_smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_F16, EPI_STORE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_F16, EPI_SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_BF16, EPI_STORE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_STORE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_SWIGLU>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     D.ready = true;
   }
@@ -265,6 +282,20 @@ moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
   return last_launch();
 }
 
+// CTA-pair GEMM: one cluster of 2 CTAs per 256 x 256 tile, up to one cluster per 2 SMs.
+// `ta64` / `tb64` map A / B with 64-row boxes (the grouped GEMMs' M = 128 tiles; `tb64`
+// only for the gate/up GEMM; both unused when dense).
+template <int KIND, int EPI>
+moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& ta64, const CUtensorMap& tb,
+                         const CUtensorMap& tb64, const GemmParams& P, int max_tiles, int sms,
+                         cudaStream_t st) {
+  const int clusters = std::min(sms / 2, max_tiles);
+  if (clusters <= 0) return MOE_OK;
+  gemm_pair_kernel<KIND, EPI><<<2 * clusters, GEMM_THREADS, pair_smem_bytes(), st>>>(
+      ta, ta64, tb, tb64, P);
+  return last_launch();
+}
+
 GemmParams base_params(int* status, uint32_t flags) {
   GemmParams P{};
   P.ksplit = 1;
@@ -376,7 +407,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = pooled; P.ld_out = p; P.out_fmt = OUT_F32;
     if (sp.pool > 1) { P.ksplit = sp.pool; P.split_stride = size_t(T) * p; P.out = part; }
     const int grid = std::min(sms, mtiles * (p / bn) * sp.pool);
-    if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
+    if (sp.pool == 1 && bn == 256) {          // CTA pairs: B half-tiles of 128 rows
+      CUtensorMap tb2;
+      if (!make_tmap(&tb2, W->w_pool, k_proj, d, p, 128)) return MOE_ERR_CUDA;
+      const int tiles = ((T + 255) / 256) * (p / 256);
+      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
+    } else if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     if (sp.pool > 1) {
       const size_t n = size_t(T) * p;
@@ -454,18 +491,22 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       gemm_swap_kernel<OP_F16, SWAP_SWIGLU><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
     MOE_TRY(last_launch());
   } else {
-    CUtensorMap ta, tb;
+    // CTA pairs over 256-row tiles of each expert (M = 128 pair tiles for remainders);
+    // each CTA of a pair loads half of a 256-row W13 block: 128 gate or 128 up rows
+    CUtensorMap ta, ta64, tb, tb64;
     if (!make_tmap(&ta, a_perm, k_up, p, rows, GEMM_BM) ||
-        !make_tmap(&tb, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, 2 * W13_GROUP))
+        !make_tmap(&ta64, a_perm, k_up, p, rows, GEMM_BM / 2) ||
+        !make_tmap(&tb, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, W13_GROUP) ||
+        !make_tmap(&tb64, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, W13_GROUP / 2))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = 2 * I; P.K = p; P.bn = 2 * W13_GROUP; P.groups = E_;
-    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
+    P.row_off = row_off; P.mt_off = mt2_off; P.row_cnt = row_cnt;
     P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
-    const int grid = std::min(sms, max_mt * (2 * I / P.bn));
-    if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_SWIGLU>(ta, tb, P, grid, st)));
-    else MOE_TRY((launch_gemm<OP_F16, EPI_SWIGLU>(ta, tb, P, grid, st)));
+    const int tiles = (rows / 256 + E_) * (2 * I / P.bn);
+    if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_SWIGLU>(ta, ta64, tb, tb64, P, tiles, sms, st)));
+    else MOE_TRY((launch_pair<OP_F16, EPI_SWIGLU>(ta, ta64, tb, tb64, P, tiles, sms, st)));
   }
   E.mark(5);
 
@@ -504,16 +545,29 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   } else {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
-    if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
-        !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, bn))
-      return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = bn; P.groups = E_;
-    P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
+    P.row_off = row_off; P.row_cnt = row_cnt;
     P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32;
-    const int grid = std::min(sms, max_mt * (p / bn));
-    if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
-    else MOE_TRY((launch_gemm<OP_BF16, EPI_STORE>(ta, tb, P, grid, st)));
+    if (bn == 256) {    // CTA pairs over 256-row tiles (M = 128 pair tiles for remainders)
+      CUtensorMap ta64;
+      if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
+          !make_tmap(&ta64, s_buf, k_down, I, rows, GEMM_BM / 2) ||
+          !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128))
+        return MOE_ERR_CUDA;
+      P.mt_off = mt2_off;
+      const int tiles = (rows / 256 + E_) * (p / 256);
+      if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta64, tb, tb, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_BF16, EPI_STORE>(ta, ta64, tb, tb, P, tiles, sms, st)));
+    } else {
+      if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
+          !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, bn))
+        return MOE_ERR_CUDA;
+      P.mt_off = mt_off;
+      const int grid = std::min(sms, max_mt * (p / bn));
+      if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
+      else MOE_TRY((launch_gemm<OP_BF16, EPI_STORE>(ta, tb, P, grid, st)));
+    }
   }
   E.mark(6);
 
@@ -540,7 +594,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       P.ksplit = sp.unpool; P.split_stride = size_t(T) * d; P.out = part; P.out_fmt = OUT_F32;
     }
     const int grid = std::min(sms, mtiles * (d / bn) * sp.unpool);
-    if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
+    if (sp.unpool == 1 && bn == 256) {        // CTA pairs
+      CUtensorMap tb2;
+      if (!make_tmap(&tb2, W->w_unpool, k_proj, p, d, 128)) return MOE_ERR_CUDA;
+      const int tiles = ((T + 255) / 256) * (d / 256);
+      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
+    } else if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     if (sp.unpool > 1) {
       const size_t n = size_t(T) * d;
