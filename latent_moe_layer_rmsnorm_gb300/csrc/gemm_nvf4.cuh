@@ -81,6 +81,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
   } else {
     const float sc = P.grp_scale[tc.e] * P.out_scale[tc.e];
     const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * NV_BN;
+    float ss = 0.f;     // the tile is one 128-column block of the row (row_ssq)
 #pragma unroll 1
     for (int c0 = 0; c0 < NV_BN; c0 += 32) {
       uint32_t a[16], b[16];
@@ -97,7 +98,12 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
         store16(P.out, base + c0, OUT_F32, va);
         store16(P.out, base + c0 + 16, OUT_F32, vb);
       }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
     }
+    if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + tc.n_blk] = ss;
   }
 }
 

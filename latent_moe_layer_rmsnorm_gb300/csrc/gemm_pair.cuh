@@ -181,6 +181,7 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
     }
   } else {
     const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * P.bn + h * 128;
+    float ss = 0.f;
     for (int c0 = 0; c0 < 128; c0 += 32) {
       uint32_t a[16], b[16];
       tmem_ld16(taddr + c0, a);
@@ -193,7 +194,14 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
         store16(P.out, base + c0, P.out_fmt, va);
         store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
     }
+    // same column order as the full-tile epilogue, so the block sums agree bit for bit
+    if (P.row_ssq && row_ok)
+      P.row_ssq[row * (P.N >> 7) + ((tc.n_blk * P.bn) >> 7) + h] = ss;
   }
 }
 

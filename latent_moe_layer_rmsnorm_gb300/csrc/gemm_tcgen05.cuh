@@ -73,6 +73,10 @@ struct GemmParams {
   const float* grp_scale;
   const float* out_scale;   // requantisation global scale (gate/up) / extra factor (down)
   uint8_t* out_sf;          // requantised output: chunked scales (codes go to `out`)
+  // expert outputs: per-row sums of squares of each 128-column block of the stored FP32
+  // values, at row_ssq[row * (N / 128) + column / 128], each summed in column order
+  // (the per-expert RMSNorm reads these instead of a second pass over the row)
+  float* row_ssq;
 };
 
 struct GemmSmem {
@@ -189,6 +193,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
   if constexpr (EPI == EPI_STORE) {
     const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * P.bn +
                         static_cast<size_t>(tc.split) * P.split_stride;
+    float ss = 0.f;     // sum of squares of the current 128-column block (row_ssq)
     for (int c0 = 0; c0 < P.bn; c0 += 32) {    // bn is a multiple of 16
       const bool two = c0 + 16 < P.bn;          // uniform across the warp
       uint32_t a[16], b[16];
@@ -201,6 +206,17 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
       if (row_ok) {
         store16(P.out, base + c0, P.out_fmt, va);
         if (two) store16(P.out, base + c0 + 16, P.out_fmt, vb);
+      }
+      if (P.row_ssq) {          // expert outputs: bn is 128 or 256, stored as FP32
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
+        if (((c0 + 32) & 127) == 0) {
+          if (row_ok)
+            P.row_ssq[row * (P.N >> 7) + ((tc.n_blk * P.bn + c0) >> 7)] = ss;
+          ss = 0.f;
+        }
       }
     }
   } else if constexpr (EPI == EPI_SWIGLU) {

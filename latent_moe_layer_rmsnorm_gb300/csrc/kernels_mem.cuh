@@ -287,88 +287,65 @@ __global__ void __launch_bounds__(MEM_THREADS)
 }
 
 // ---- combine -----------------------------------------------------------------------
-// One block per token.  Pass 1: sum of squares of each selected expert output row (the
-// values as stored).  Pass 2: c = sum_j w_j * y_j * rsqrt(mean(y_j^2) + eps) * g_exp[e_j]
-// accumulated in FP32 in slot order j = 0..k-1, stored as the unpooler's operand: FP16
+// One block per token.  The down GEMM's epilogue left, for every stored expert output row,
+// the sum of squares of each 128-column block (row_ssq, [rows, p / 128]); the k row norms
+// r_j = rsqrt(sum / p + eps) come from those blocks added in column order, so the rows
+// are read once: c = sum_j w_j * r_j * g_exp[e_j] * y_j, accumulated in FP32 in slot
+// order j = 0..k-1 and stored as the unpooler's operand: FP16
 // (|c_i| <= sum_j |w_j| * sqrt(p) * max|g_exp|), or TF32-rounded FP32.
-template <bool Y_F32, bool C_F32>
+template <bool C_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
-    combine_kernel(const void* __restrict__ y, const int* __restrict__ inv,
-                   const int32_t* __restrict__ ids, const float* __restrict__ wts,
-                   const float* __restrict__ g_exp, void* __restrict__ c_out, int p, int k,
-                   int E, float eps) {
-  __shared__ float red[32 * MAX_TOPK];
+    combine_kernel(const float* __restrict__ y, const float* __restrict__ row_ssq,
+                   const int* __restrict__ inv, const int32_t* __restrict__ ids,
+                   const float* __restrict__ wts, const float* __restrict__ g_exp,
+                   void* __restrict__ c_out, int p, int k, int E, float eps) {
   __shared__ int rows[MAX_TOPK];
   __shared__ int eids[MAX_TOPK];
-  __shared__ float wj[MAX_TOPK];
-  __shared__ float rsj[MAX_TOPK];
+  __shared__ float sj[MAX_TOPK];     // w_j * r_j
   const size_t t = blockIdx.x;
   if (threadIdx.x < k) {
     int r = inv[t * k + threadIdx.x];
     int e = ids[t * k + threadIdx.x];
     if (e < 0 || e >= E) { r = -1; e = 0; }
+    float ss = 0.f;
+    if (r >= 0) {
+      const float* q = row_ssq + size_t(r) * (p >> 7);
+      for (int i = 0; i < (p >> 7); ++i) ss += q[i];
+    }
     rows[threadIdx.x] = r;
     eids[threadIdx.x] = e;
-    wj[threadIdx.x] = wts[t * k + threadIdx.x];
+    sj[threadIdx.x] = wts[t * k + threadIdx.x] * rsqrtf(ss / static_cast<float>(p) + eps);
   }
   __syncthreads();
   const int nchunk = p >> 3;
-  auto load8 = [&](int r, int c, float (&v)[8]) {
-    if constexpr (Y_F32) {
-      const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(y) + size_t(r) * p) + 2 * c;
-      const float4 a = s[0], b = s[1];
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-      const uint4 a = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + size_t(r) * p)[c];
-      float2 f;
-      f = unpack_bf16x2(a.x); v[0] = f.x; v[1] = f.y;
-      f = unpack_bf16x2(a.y); v[2] = f.x; v[3] = f.y;
-      f = unpack_bf16x2(a.z); v[4] = f.x; v[5] = f.y;
-      f = unpack_bf16x2(a.w); v[6] = f.x; v[7] = f.y;
-    }
-  };
-  float ss[MAX_TOPK];
-#pragma unroll
-  for (int j = 0; j < MAX_TOPK; ++j) ss[j] = 0.f;
   for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    float4 ya[MAX_TOPK], yb[MAX_TOPK];      // issue every row's loads before the sums
 #pragma unroll
     for (int j = 0; j < MAX_TOPK; ++j) {
       if (j < k && rows[j] >= 0) {
-        float v[8];
-        load8(rows[j], c, v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ss[j] = fmaf(v[i], v[i], ss[j]);
+        const float4* src = reinterpret_cast<const float4*>(y + size_t(rows[j]) * p) + 2 * c;
+        ya[j] = src[0];
+        yb[j] = src[1];
       }
     }
-  }
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-#pragma unroll
-  for (int j = 0; j < MAX_TOPK; ++j) {
-    const float s = warp_sum(ss[j]);
-    if (l == 0) red[j * 32 + w] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x < k) {
-    float s = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[threadIdx.x * 32 + i];
-    rsj[threadIdx.x] = rsqrtf(s / static_cast<float>(p) + eps);
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int r = rows[j];
-      if (r < 0) continue;
-      float v[8];
-      load8(r, c, v);
-      const float s = wj[j] * rsj[j];
-      const float4 g0 = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p)[2 * c];
-      const float4 g1 = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p)[2 * c + 1];
-      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s, v[i] * gg[i], acc[i]);
+    for (int j = 0; j < MAX_TOPK; ++j) {
+      if (j < k && rows[j] >= 0) {
+        const float4* g = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p) + 2 * c;
+        const float4 g0 = g[0], g1 = g[1];
+        const float s = sj[j];
+        acc[0] = fmaf(s, ya[j].x * g0.x, acc[0]);
+        acc[1] = fmaf(s, ya[j].y * g0.y, acc[1]);
+        acc[2] = fmaf(s, ya[j].z * g0.z, acc[2]);
+        acc[3] = fmaf(s, ya[j].w * g0.w, acc[3]);
+        acc[4] = fmaf(s, yb[j].x * g1.x, acc[4]);
+        acc[5] = fmaf(s, yb[j].y * g1.y, acc[5]);
+        acc[6] = fmaf(s, yb[j].z * g1.z, acc[6]);
+        acc[7] = fmaf(s, yb[j].w * g1.w, acc[7]);
+      }
     }
     if constexpr (C_F32) {
       float4* dst = reinterpret_cast<float4*>(static_cast<float*>(c_out) + t * p) + 2 * c;
@@ -380,6 +357,28 @@ __global__ void __launch_bounds__(MEM_THREADS)
       o.z = pack_f16x2(acc[4], acc[5]); o.w = pack_f16x2(acc[6], acc[7]);
       reinterpret_cast<uint4*>(static_cast<__half*>(c_out) + t * p)[c] = o;
     }
+  }
+}
+
+// Block sums of squares of stored expert output rows, for the down GEMM variants whose
+// epilogue does not produce them (weight-row tiles): one thread per (row, 128 columns),
+// summed in column order like the GEMM epilogues.
+__global__ void __launch_bounds__(MEM_THREADS)
+    row_ssq_kernel(const float* __restrict__ y, int rows, int p, float* __restrict__ row_ssq) {
+  const int parts = p >> 7;
+  const size_t n = size_t(rows) * parts;
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n;
+       i += size_t(gridDim.x) * blockDim.x) {
+    const float4* src = reinterpret_cast<const float4*>(y + (i / parts) * p + (i % parts) * 128);
+    float ss = 0.f;
+    for (int q = 0; q < 32; ++q) {
+      const float4 v = src[q];
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+    row_ssq[i] = ss;
   }
 }
 

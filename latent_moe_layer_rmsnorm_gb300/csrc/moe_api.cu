@@ -205,7 +205,7 @@ SplitPlan split_plan(const moe_config_t& c) {
 
 struct WsLayout {
   size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, mt2_off, row_cnt, src, inv,
-      a_perm, s, y, c, sf_u, sf_s, alpha, part, total;
+      a_perm, s, y, ssq, c, sf_u, sf_s, alpha, part, total;
   int nchunks;
   size_t rows;    // dispatched rows (NVFP4: 128-aligned per expert)
 };
@@ -241,6 +241,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.a_perm = take(q ? R * p / 2 : R * p * ee);
   L.s = take(q ? R * I / 2 : R * I * ee);
   L.y = take(R * p * 4);     // expert outputs stay FP32 until the per-expert norm
+  L.ssq = take(R * (p / 128) * 4);   // their sums of squares per 128-column block
   L.c = take(T * p * ea);
   L.sf_u = take(q ? R * p / 16 : 0);
   L.sf_s = take(q ? R * I / 16 : 0);
@@ -512,6 +513,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
 
   // ---- stage: grouped down GEMM -> y ------------------------------------------------------
   void* y_buf = base + L.y;
+  float* ssq = reinterpret_cast<float*>(base + L.ssq);
   if (nvf4) {
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, s_buf, OP_NVF4, I / 2, R, GEMM_BM) ||
@@ -520,7 +522,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = NV_BN; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
-    P.out = y_buf; P.ld_out = p;
+    P.out = y_buf; P.ld_out = p; P.row_ssq = ssq;
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
     const int grid = std::min(sms, max_mt * (p / NV_BN));
     gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
@@ -542,13 +544,17 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     else
       gemm_swap_kernel<OP_BF16, SWAP_STORE><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
     MOE_TRY(last_launch());
+    const size_t n = rows * static_cast<size_t>(p / 128);
+    row_ssq_kernel<<<static_cast<int>(std::min<size_t>((n + MEM_THREADS - 1) / MEM_THREADS, 4096)),
+                     MEM_THREADS, 0, st>>>(static_cast<const float*>(y_buf), rows, p, ssq);
+    MOE_TRY(last_launch());
   } else {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = bn; P.groups = E_;
     P.row_off = row_off; P.row_cnt = row_cnt;
-    P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32;
+    P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32; P.row_ssq = ssq;
     if (bn == 256) {    // CTA pairs over 256-row tiles (M = 128 pair tiles for remainders)
       CUtensorMap ta64;
       if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
@@ -574,9 +580,11 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   // ---- stage: per-expert RMSNorm + FP32 weighted sum -------------------------------------
   void* c_buf = base + L.c;
   if (act_f32)
-    combine_kernel<true, true><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+    combine_kernel<true><<<T, MEM_THREADS, 0, st>>>(static_cast<const float*>(y_buf), ssq, inv, ids,
+                                                    wts, W->g_exp, c_buf, p, k, E_, c.eps);
   else
-    combine_kernel<true, false><<<T, MEM_THREADS, 0, st>>>(y_buf, inv, ids, wts, W->g_exp, c_buf, p, k, E_, c.eps);
+    combine_kernel<false><<<T, MEM_THREADS, 0, st>>>(static_cast<const float*>(y_buf), ssq, inv, ids,
+                                                     wts, W->g_exp, c_buf, p, k, E_, c.eps);
   MOE_TRY(last_launch());
   E.mark(7);
 
@@ -839,7 +847,10 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally) {
   // norm, [router], pooler, 4 dispatch kernels, gate/up, down, combine, unpooler,
   // plus one reduction per split-K GEMM
   const SplitPlan sp = split_plan(*cfg);
-  return 10 + (route_internally ? 1 + (sp.router > 1) : 0) + (sp.pool > 1) + (sp.unpool > 1);
+  // the weight-row down GEMM leaves the row sums of squares to one more kernel
+  const int ssq_pass = (cfg->flags & MOE_FLAG_WEIGHT_TILES) && cfg->expert != MOE_NVFP4 ? 1 : 0;
+  return 10 + (route_internally ? 1 + (sp.router > 1) : 0) + (sp.pool > 1) + (sp.unpool > 1) +
+         ssq_pass;
 }
 
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n) {
