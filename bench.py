@@ -2,7 +2,7 @@
 E=256, top-k 8, I=4096, BF16) through the C ABI on GB300s.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload prefill_bf16|decode_bf16|skewed_bf16|tiny_f32]
+                  [--workload prefill_bf16|decode_bf16|skewed_bf16|prefill_nvfp4|decode_nvfp4|...]
 
 A step is one moe_forward over one batch of T synthetic tokens (all eight stages:
 norm, router + top-k, pooler, dispatch, gate/up + SwiGLU, down, combine, unpooler).

@@ -65,8 +65,13 @@ SKEWED_BF16 = Shape("skewed_bf16", T=8192, d=8192, p=4096, E=256, top_k=8, I=409
 PREFILL_SLICE_BF16 = Shape("prefill_slice_bf16", T=1024, d=8192, p=4096, E=16, top_k=8,
                            I=4096)
 
+PREFILL_SLICE_NVFP4 = PREFILL_SLICE_BF16.replace(name="prefill_slice_nvfp4", expert="nvfp4")
+# Decode with NVFP4 experts: the weight stream is 4.5 bits per weight instead of 16.
+DECODE_NVFP4 = DECODE_BF16.replace(name="decode_nvfp4", expert="nvfp4")
+
 WORKLOADS = {s.name: s for s in (TINY_F32, PREFILL_BF16, DECODE_BF16, PREFILL_NVFP4,
-                                 SKEWED_BF16, PREFILL_SLICE_BF16)}
+                                 SKEWED_BF16, PREFILL_SLICE_BF16, PREFILL_SLICE_NVFP4,
+                                 DECODE_NVFP4)}
 
 
 def storage_dtype(kind: str) -> torch.dtype:
