@@ -162,6 +162,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// Each lane writes 16 consecutive 32-bit columns of its own TMEM lane (the warp's
+// 32-lane quadrant).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -212,7 +228,7 @@ __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t adesc, uint6
 // Block-scaled FP4 MMA (NVFP4: E2M1 operands, one UE4M3 scale per 16 elements of K):
 // scale_a / scale_b are the TMEM addresses of this K=64 step's scales (A row r: lane r,
 // column scale_a + r/32; B column n: lane n%32, column scale_b + n/32; 4 bytes = the 4
-// blocks of 16), as laid down by tcgen05.cp .32x128b.warpx4 from 4x32 chunks.
+// blocks of 16): the layout a tcgen05.cp .32x128b.warpx4 of a 4x32 chunk leaves.
 __device__ __forceinline__ void mma_issue_nvf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                uint32_t idesc, uint32_t scale_a, uint32_t scale_b,
                                                uint32_t accumulate) {
@@ -239,14 +255,6 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>(sbo >> 4) << 32;
   d |= static_cast<uint64_t>(1u) << 46;
   return d;
-}
-
-// Copy one 4x32 scale chunk (512 B: 32 rows of 16 bytes, byte 4j + b of row i = scale b
-// of operand row 32j + i) into 4 TMEM columns of all four lane quadrants.
-__device__ __forceinline__ void tmem_cp_scales(uint32_t taddr, const void* chunk) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
-               "l"(sdesc_plain(smem_u32(chunk), 16, 128))
-               : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05.mma this thread issued so far has completed.

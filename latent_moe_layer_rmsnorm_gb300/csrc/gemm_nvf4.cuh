@@ -13,8 +13,12 @@
 // Same pipeline as gemm_tcgen05.cuh (TMA producer warp, one MMA-issuing thread, four
 // epilogue warps, double-buffered TMEM accumulators, bounded waits), with per-stage
 // scale tiles: the producer bulk-copies the 4 scale chunks (512 B each) of the A and B
-// tiles next to the operand tiles; the MMA thread moves them to TMEM with tcgen05.cp
-// (.32x128b.warpx4) and issues 4 block-scaled MMAs (K = 64 each) per 128-byte K slice.
+// tiles next to the operand tiles, and four scale warps (one per TMEM lane quadrant)
+// write them into TMEM with tcgen05.st, each quadrant getting the same 32 lanes x 16
+// columns per operand that a tcgen05.cp .32x128b.warpx4 of the chunks would leave.
+// Copying them with tcgen05.cp instead costs about 50 tensor-pipe cycles per chunk,
+// more than the 4 MMAs of the slice take (measured on GB300).  The MMA thread issues
+// 4 block-scaled MMAs (K = 64 each) per 128-byte K slice once its scales are in place.
 // TMEM: accumulators in columns [0, 256), a ring of per-stage scale columns after them.
 // A rows are 128-aligned per expert (padded dispatch), so a tile's scales are whole chunks.
 #pragma once
@@ -30,6 +34,7 @@ constexpr int NV_B_STAGE = NV_BN * 128;
 constexpr int NV_SF_STAGE = 4 * 512;         // 4 scale chunks per operand per stage
 constexpr int NV_SF_COL0 = 256;
 constexpr int NV_SF_COLS = 32;               // per stage: 16 (A) + 16 (B)
+constexpr int NV_THREADS = 384;              // warps 0-7 as in gemm_tcgen05.cuh, 8-11 scales
 
 enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_F32 = 1 };
 
@@ -37,6 +42,7 @@ struct NvSmem {
   GemmSmem g;                // barriers and schedule (its `full`/`empty` sized for GEMM_STAGES)
   uint64_t full[NV_STAGES];
   uint64_t empty[NV_STAGES];
+  uint64_t sf_ready[NV_STAGES];   // the 4 scale warps have written the stage's scales
   float recip[256];
 };
 
@@ -108,7 +114,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(NV_THREADS, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -128,6 +134,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     for (int s = 0; s < NV_STAGES; ++s) {
       mbar_init(&N->full[s], 1);
       mbar_init(&N->empty[s], 1);
+      mbar_init(&N->sf_ready[s], 4);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&S->tfull[a], 1);
@@ -213,13 +220,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           ok = false;
           break;
         }
+        if (!mbar_wait_bounded(&N->sf_ready[stage], phase, abort_flag, P.status,
+                               WAIT_MMA_FULL, limit)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sf_col = tmem_base + NV_SF_COL0 + stage * NV_SF_COLS;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          tmem_cp_scales(sf_col + 4 * j, sSA + stage * NV_SF_STAGE + 512 * j);
-          tmem_cp_scales(sf_col + 16 + 4 * j, sSB + stage * NV_SF_STAGE + 512 * j);
-        }
         const uint32_t a0 = smem_u32(sA + stage * NV_A_STAGE);
         const uint32_t b0 = smem_u32(sB + stage * NV_B_STAGE);
 #pragma unroll
@@ -237,6 +244,39 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     {
       volatile int never = 0;
       mbar_wait_bounded(&S->drain, 0, &never, P.status, WAIT_DRAIN, limit);
+    }
+  } else if (warp >= 8) {
+    // ---------------- scale warps: stage scales -> TMEM (quadrant warp % 4) ----------
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      bool ok = true;
+      for (int kb = 0; kb < kblocks; ++kb) {
+        if (!mbar_wait_bounded(&N->full[stage], phase, abort_flag, P.status, WAIT_MMA_FULL,
+                               limit)) {
+          ok = false;
+          break;
+        }
+        // lane l: row l of each 512-byte chunk (16 bytes = 4 columns), chunk j -> 4j..
+        uint32_t va[16], vb[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 a = *reinterpret_cast<const uint4*>(sSA + stage * NV_SF_STAGE + 512 * j + 16 * lane);
+          const uint4 b = *reinterpret_cast<const uint4*>(sSB + stage * NV_SF_STAGE + 512 * j + 16 * lane);
+          va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
+          vb[4 * j] = b.x; vb[4 * j + 1] = b.y; vb[4 * j + 2] = b.z; vb[4 * j + 3] = b.w;
+        }
+        const uint32_t sf_col = tmem_base + NV_SF_COL0 + stage * NV_SF_COLS + lane_base;
+        tmem_st16(sf_col, va);
+        tmem_st16(sf_col + 16, vb);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&N->sf_ready[stage]);
+        if (++stage == NV_STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
     }
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------

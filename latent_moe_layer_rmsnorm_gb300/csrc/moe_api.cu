@@ -472,7 +472,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.sf_a = sf_u; P.sf_b = W->sf13; P.row_scale = alpha; P.grp_scale = W->gs13;
     P.out_scale = W->gs_act2; P.out_sf = sf_s;
     const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
     MOE_TRY(last_launch());
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on the MMA's M side (256-row W13 blocks: 128 gate + 128 up), tokens on N
@@ -525,7 +525,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = y_buf; P.ld_out = p; P.row_ssq = ssq;
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
     const int grid = std::min(sms, max_mt * (p / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, GEMM_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
     MOE_TRY(last_launch());
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on M (128 rows of p), up to 256 tokens on N
