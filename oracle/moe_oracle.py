@@ -172,6 +172,33 @@ def combine(y: np.ndarray, ids: np.ndarray, wts: np.ndarray, g_exp, eps: float) 
     return c
 
 
+# ---- between two blocks ----------------------------------------------------------------
+
+def boundary(x: np.ndarray, y: np.ndarray, g_post, g_next, eps: float, gate=None,
+             act: str = "bf16"):
+    """What follows the block in the decoder: the sandwich post-norm, the residual add and
+    the next block's pre-norm ("vLLM 对 Muse Spark Open 的 Day 0 支持", section "三明治归一化":
+    x + post_norm(F(norm(x))); "SGLang and Miles Add Day-0 Support for Muse Spark Open",
+    section "Kernel Optimizations": post-FFN norm, gated residual add and pre-attention
+    norm form one elementwise chain).
+
+        a_t  = RMSNorm_{g_post}(y_t)            y = the block's output F(norm(x))
+        x'_t = x_t + gate * a_t                 gate per channel; None = plain residual
+        h'_t = RMSNorm_{g_next}(x'_t)           on x' as stored in the residual stream
+
+    The pages name the residual "gated" without giving the gate's form; a per-channel
+    gate vector is the reading taken (None gives the plain residual of the sandwich
+    form).  x' and h' are stored in the residual-stream format `act` ("bf16", "f32" or
+    "f64" for no rounding); returns (x', h') as float64 arrays.
+    """
+    a = rmsnorm(y, g_post, eps)
+    if gate is not None:
+        a = a * as_f64(gate)
+    xn = _store(as_f64(x) + a, act)
+    hn = _store(rmsnorm(xn, g_next, eps), act)
+    return xn, hn
+
+
 # ---- the layer ---------------------------------------------------------------------
 
 def storage_kinds(act: str, expert: str, out: str, chain: bool) -> dict:

@@ -183,3 +183,28 @@ def test_nvfp4_prefill_chunk_sampled():
     err = rel_err(to_np(out[torch.as_tensor(tok, device=out.device)]), ref["out"])
     print(f"nvfp4 prefill sampled {tok}: {err:.2e}")
     assert err <= TOL_NVFP4
+
+
+@pytest.mark.slow
+def test_nvfp4_decode_batch():
+    """The decode batch (T=64, full widths) with NVFP4 experts: about 226 experts with one
+    to three rows each, so nearly every tile is a 128-row tile holding a handful of rows.
+    All 64 tokens against the NVFP4 oracle."""
+    need_gpu()
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+    shape = synth.DECODE_NVFP4
+    inp = synth.make_inputs(shape, seed=5, device="cuda")
+    fix_margins(inp, shape, seed=5)
+    layer = LatentMoE(shape, inp, out="f32")
+    out = layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    tok = list(range(shape.T))
+    view = oracle_view(inp, lazy=True)
+    ref = oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act="bf16",
+                             expert="nvfp4", out="f32", tokens=tok, return_parts=True)
+    ids = layer.intermediate("ids", shape.T).cpu().numpy()
+    np.testing.assert_array_equal(ids, ref["ids"])
+    err = rel_err(to_np(out), ref["out"])
+    print(f"nvfp4 decode: {len(np.unique(ids))} experts touched, {err:.2e}")
+    assert err <= TOL_NVFP4
