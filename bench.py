@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-boundary", action="store_true",
+                    help="skip the separate timing of moe_boundary on the step's output")
     return ap.parse_args()
 
 
@@ -279,6 +281,30 @@ def run_ours(args):
                "d2h_bytes_per_step": out.numel() * out.element_size(),
                "ms_per_step": e2e_ms / n_e2e}
 
+    # ---- the block boundary (post-norm, residual add, next pre-norm), timed on its own ----
+    boundary = None
+    if not args.no_boundary:
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed + 17)
+        g_post = torch.rand(shape.d, generator=gen, device="cuda") + 0.5
+        g_next = torch.rand(shape.d, generator=gen, device="cuda") + 0.5
+        xo, hn = torch.empty_like(x), torch.empty_like(x)
+        for _ in range(3):
+            layer.boundary(x, out, g_post, g_next, x_out=xo, h_next=hn)
+        torch.cuda.synchronize()
+        b0 = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(args.steps):
+            layer.boundary(x, out, g_post, g_next, x_out=xo, h_next=hn)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        b_ms = max_over_ranks(b0.elapsed_time(b1), "cuda") / args.steps
+        b_bytes = 3 * x.numel() * x.element_size() + out.numel() * out.element_size()
+        boundary = {"ms": round(b_ms, 4), "gbs": round(b_bytes / (b_ms / 1e3) / 1e9, 1),
+                    "bytes": b_bytes}
+        del xo, hn
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -336,6 +362,11 @@ def run_ours(args):
         "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
+    if boundary is not None:
+        # not part of the step: the pass that follows the block (moe_boundary), timed alone
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        boundary["frac_of_hbm"] = round(boundary["gbs"] / hbm, 3)
+        line["boundary"] = boundary
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

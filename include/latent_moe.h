@@ -235,7 +235,32 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* W, const 
                          const int32_t* ids, const float* w, void* out, void* ws,
                          size_t ws_bytes, moe_stream_t stream);
 
-/* moe_forward with CUDA events recorded on `stream` at each stage boundary:
+/* What follows the block in the decoder, in one pass per row ("vLLM 对 Muse Spark Open 的
+ * Day 0 支持", section "三明治归一化": each block sits between two norms,
+ * x + post_norm(F(norm(x))); "SGLang and Miles Add Day-0 Support for Muse Spark Open",
+ * section "Kernel Optimizations": post-FFN norm, gated residual add and pre-attention
+ * norm fused, each row kept in registers across both RMS reductions):
+ *   x_out  = x + gate * RMSNorm_{g_post}(y)       stored in the act dtype
+ *   h_next = RMSNorm_{g_next}(x_out as stored)    stored in the act dtype
+ * Uses cfg->T, d, eps, act (x, x_out, h_next) and out (y); the other fields must still
+ * form a valid config.
+ *   x       [T,d] act dtype (device): the residual stream entering the block
+ *   y       [T,d] out dtype (device): the block's output, e.g. moe_forward's `out`
+ *   g_post  [d] FP32 (device): gain of the post-norm;  g_next [d] FP32: of the next
+ *           block's pre-norm
+ *   gate    [d] FP32 (device) or NULL: per-channel gate of the residual add (NULL: 1).
+ *           The pages do not give the gate's form; a per-channel vector is this
+ *           library's reading.
+ *   x_out   [T,d] act dtype (device, written); may be x itself (updated in place)
+ *   h_next  [T,d] act dtype (device, written); may not overlap x, y or x_out
+ * Every pointer 16-byte aligned.  Sums of squares are FP32, added in a fixed order; when
+ * T is small several CTAs (a cluster) share each row through distributed shared memory.
+ * Returns MOE_ERR_INVALID_ARG for null, misaligned or overlapping buffers. */
+moe_status_t moe_boundary(const moe_config_t* cfg, const void* x, const void* y,
+                          const float* g_post, const float* gate, const float* g_next,
+                          void* x_out, void* h_next, moe_stream_t stream);
+
+/* moe_forward with CUDA events recorded on `stream` at each stage boundary:/* moe_forward with CUDA events recorded on `stream` at each stage boundary:
  * events[0] before the first kernel and events[i] after stage i-1 (i = 1..n_events-1,
  * at most moe_num_stages()+1 events).  For measurement only; same results. */
 moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* W,

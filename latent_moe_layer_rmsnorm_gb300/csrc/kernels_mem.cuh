@@ -382,6 +382,160 @@ __global__ void __launch_bounds__(MEM_THREADS)
   }
 }
 
+// ---- block boundary: post-norm + residual + next pre-norm ------------------------------
+// "vLLM 对 Muse Spark Open 的 Day 0 支持", section "三明治归一化": the block sits between
+// two norms, x + post_norm(F(norm(x))); "SGLang and Miles Add Day-0 Support for Muse Spark
+// Open", section "Kernel Optimizations": the post-FFN norm, the gated residual add and
+// the pre-attention norm run as one kernel that keeps each row in registers across both
+// RMS reductions, and a cluster of CTAs shares one row through distributed shared memory
+// when rows alone do not fill the GPU.
+//
+//   a = RMSNorm_{g_post}(y);  x' = x + gate * a (gate per channel, or 1);  stored as the
+//   residual stream's type;  h' = RMSNorm_{g_next}(x' as stored)
+//
+// C CTAs (one cluster) share a row: CTA r holds columns [r d/C, (r+1) d/C), at most
+// BND_MAXV values per thread.  Both sums of squares go thread -> warp -> CTA (fixed
+// order) -> cluster (partials of ranks 0..C-1 added in rank order by every CTA), so all
+// CTAs of a row use the same bits.
+constexpr int BND_MAXV = 32;   // values per thread: d / C <= 8192
+
+__device__ __forceinline__ float cluster_row_sum(float v, float* red, float* part, int C) {
+  const float s = block_sum(v, red);
+  if (C == 1) return s;
+  if (threadIdx.x == 0) *part = s;
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+  float total = 0.f;
+  for (int r = 0; r < C; ++r) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(part)), "r"(r));
+    float q;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(q) : "r"(a) : "memory");
+    total += q;
+  }
+  return total;
+}
+
+template <int C>
+__global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(MEM_THREADS)
+    boundary_kernel(const void* __restrict__ x, const void* __restrict__ y,
+                    const float* __restrict__ g_post, const float* __restrict__ gate,
+                    const float* __restrict__ g_next, void* x_out, void* __restrict__ h_next,
+                    int d, float eps, int x_f32, int y_f32) {
+  __shared__ float red[32];
+  __shared__ float part[2];
+  const int rank = C == 1 ? 0 : static_cast<int>(blockIdx.x % C);
+  const size_t t = blockIdx.x / C;
+  const int cols = d / C;
+  const int c0 = rank * cols;
+  const int nchunk = cols >> 3;       // 8 values per chunk
+  constexpr int MAXCH = BND_MAXV / 8;
+  float v[MAXCH][8];
+  // 1. block output y and its sum of squares
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int c = threadIdx.x + i * MEM_THREADS;
+    if (c < nchunk) {
+      const size_t off = t * d + c0 + 8 * c;
+      if (y_f32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(y) + off);
+        const float4 a = src[0], b = src[1];
+        v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
+        v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
+      } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + off);
+        float2 f;
+        f = unpack_bf16x2(a.x); v[i][0] = f.x; v[i][1] = f.y;
+        f = unpack_bf16x2(a.y); v[i][2] = f.x; v[i][3] = f.y;
+        f = unpack_bf16x2(a.z); v[i][4] = f.x; v[i][5] = f.y;
+        f = unpack_bf16x2(a.w); v[i][6] = f.x; v[i][7] = f.y;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(v[i][j], v[i][j], ss);
+    }
+  }
+  const float rs_y = rsqrtf(cluster_row_sum(ss, red, &part[0], C) / static_cast<float>(d) + eps);
+  // 2. residual add, rounded to the stream's type, kept in registers
+  float ss2 = 0.f;
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int c = threadIdx.x + i * MEM_THREADS;
+    if (c < nchunk) {
+      const int col = c0 + 8 * c;
+      const size_t off = t * d + col;
+      float xv[8];
+      if (x_f32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + off);
+        const float4 a = src[0], b = src[1];
+        xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w; xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+      } else {
+        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + off);
+        float2 f;
+        f = unpack_bf16x2(a.x); xv[0] = f.x; xv[1] = f.y;
+        f = unpack_bf16x2(a.y); xv[2] = f.x; xv[3] = f.y;
+        f = unpack_bf16x2(a.z); xv[4] = f.x; xv[5] = f.y;
+        f = unpack_bf16x2(a.w); xv[6] = f.x; xv[7] = f.y;
+      }
+      const float4 p0 = reinterpret_cast<const float4*>(g_post + col)[0];
+      const float4 p1 = reinterpret_cast<const float4*>(g_post + col)[1];
+      const float gp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      float gt[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+      if (gate) {
+        const float4 q0 = reinterpret_cast<const float4*>(gate + col)[0];
+        const float4 q1 = reinterpret_cast<const float4*>(gate + col)[1];
+        gt[0] = q0.x; gt[1] = q0.y; gt[2] = q0.z; gt[3] = q0.w;
+        gt[4] = q1.x; gt[5] = q1.y; gt[6] = q1.z; gt[7] = q1.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float a = v[i][j] * rs_y * gp[j];
+        float r = xv[j] + gt[j] * a;
+        if (!x_f32) r = __bfloat162float(__float2bfloat16_rn(r));
+        v[i][j] = r;
+        ss2 = fmaf(r, r, ss2);
+      }
+      if (x_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(x_out) + off);
+        dst[0] = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
+        dst[1] = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
+      } else {
+        uint4 o;
+        o.x = pack_bf16x2(v[i][0], v[i][1]); o.y = pack_bf16x2(v[i][2], v[i][3]);
+        o.z = pack_bf16x2(v[i][4], v[i][5]); o.w = pack_bf16x2(v[i][6], v[i][7]);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(x_out) + off) = o;
+      }
+    }
+  }
+  // 3. the next block's pre-norm on the stored residual
+  const float rs_x = rsqrtf(cluster_row_sum(ss2, red, &part[1], C) / static_cast<float>(d) + eps);
+#pragma unroll
+  for (int i = 0; i < MAXCH; ++i) {
+    const int c = threadIdx.x + i * MEM_THREADS;
+    if (c < nchunk) {
+      const int col = c0 + 8 * c;
+      const size_t off = t * d + col;
+      const float4 n0 = reinterpret_cast<const float4*>(g_next + col)[0];
+      const float4 n1 = reinterpret_cast<const float4*>(g_next + col)[1];
+      const float gn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+      float o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = v[i][j] * rs_x * gn[j];
+      if (x_f32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(h_next) + off);
+        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+      } else {
+        uint4 q;
+        q.x = pack_bf16x2(o[0], o[1]); q.y = pack_bf16x2(o[2], o[3]);
+        q.z = pack_bf16x2(o[4], o[5]); q.w = pack_bf16x2(o[6], o[7]);
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(h_next) + off) = q;
+      }
+    }
+  }
+  // no CTA of the cluster leaves while another may still read its partials
+  if (C > 1) asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ---- weight preparation ----------------------------------------------------------------
 // Element conversion applied while packing a weight: FP32 -> TF32 (ties away) for FP32
 // configurations, BF16 -> FP16 for BF16 ones (exact for |w| >= 2^-17; smaller values

@@ -826,6 +826,49 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* W, const 
                    reinterpret_cast<cudaStream_t>(stream), nullptr, 0);
 }
 
+moe_status_t moe_boundary(const moe_config_t* cfg, const void* x, const void* y,
+                          const float* g_post, const float* gate, const float* g_next,
+                          void* x_out, void* h_next, moe_stream_t stream) {
+  const moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config_t& c = *cfg;
+  if (c.T == 0) return MOE_OK;
+  if (!x || !y || !g_post || !g_next || !x_out || !h_next) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(g_post) || !aligned16(g_next) ||
+      !aligned16(x_out) || !aligned16(h_next) || (gate && !aligned16(gate)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t ex = c.act == MOE_F32 ? 4 : 2, ey = c.out == MOE_F32 ? 4 : 2;
+  const size_t bx = size_t(c.T) * c.d * ex, by = size_t(c.T) * c.d * ey;
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+  };
+  // x_out may be x itself (in-place residual update); nothing else may overlap
+  if ((x_out != x && overlap(x_out, bx, x, bx)) || overlap(x_out, bx, y, by) ||
+      overlap(h_next, bx, x, bx) || overlap(h_next, bx, y, by) ||
+      overlap(h_next, bx, x_out, bx))
+    return MOE_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // CTAs per row: enough that every thread holds at most BND_MAXV values, and more (up
+  // to a cluster of 8) while the rows alone would leave SMs idle
+  int C = 1;
+  while (C < 8 && (c.d / C > BND_MAXV * MEM_THREADS || static_cast<long long>(c.T) * C < 2 * sms))
+    C *= 2;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int xf = c.act == MOE_F32, yf = c.out == MOE_F32;
+  const unsigned grid = static_cast<unsigned>(c.T) * C;
+  switch (C) {
+    case 1: boundary_kernel<1><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 2: boundary_kernel<2><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 4: boundary_kernel<4><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    default: boundary_kernel<8><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+  }
+  return last_launch();
+}
+
 moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* W,
                                   const void* x, const int32_t* ids, const float* w,
                                   void* out, void* ws, size_t ws_bytes, moe_stream_t stream,

@@ -150,6 +150,20 @@ class LatentMoE:
                             ws, nbytes, _stream()), "moe_route")
         return ids, w
 
+    def boundary(self, x: torch.Tensor, y: torch.Tensor, g_post: torch.Tensor,
+                 g_next: torch.Tensor, gate=None, x_out=None, h_next=None):
+        """Post-norm of the block output y, residual add into x and the next block's
+        pre-norm (moe_boundary).  Returns (x_out, h_next); x_out may be x (in place)."""
+        T = x.shape[0]
+        if x_out is None:
+            x_out = torch.empty_like(x)
+        if h_next is None:
+            h_next = torch.empty_like(x)
+        L.check(L.moe_boundary(self.config(T), x.data_ptr(), y.data_ptr(), g_post.data_ptr(),
+                               None if gate is None else gate.data_ptr(), g_next.data_ptr(),
+                               x_out.data_ptr(), h_next.data_ptr(), _stream()), "moe_boundary")
+        return x_out, h_next
+
     def read_status(self):
         ws, nbytes = self.workspace(1) if self.ws is None else (self.ws.data_ptr() + self.ws_off,
                                                                  self.ws_bytes)

@@ -117,6 +117,27 @@ def test_host_side_errors_before_any_launch():
     assert L.moe_forward_launches(dec, False) == 12
 
 
+def test_boundary_host_side_errors():
+    """moe_boundary rejects null, misaligned and overlapping buffers before any launch;
+    T = 0 is a no-op.  (x_out == x, the in-place update, is allowed.)"""
+    c = cfg(T=4, d=256)
+    n = 4 * 256 * 2                     # bytes of one [T, d] BF16 buffer
+    X, Y, XO, H, G = FAKE, 2 * FAKE, 3 * FAKE, 4 * FAKE, 5 * FAKE
+    assert L.moe_boundary(c, None, Y, G, None, G, XO, H, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, None, None, G, XO, H, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, G, None, G, XO, None, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X + 2, Y, G, None, G, XO, H, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, G, G + 4, G, XO, H, None) == L.MOE_ERR_INVALID_ARG
+    # h_next overlapping x, y or x_out; x_out overlapping y or part of x
+    assert L.moe_boundary(c, X, Y, G, None, G, XO, X + n - 16, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, G, None, G, XO, Y, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, G, None, G, XO, XO + 16, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, G, None, G, Y, H, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(c, X, Y, G, None, G, X + 16, H, None) == L.MOE_ERR_INVALID_ARG
+    assert L.lib().moe_boundary(None, X, Y, G, None, G, XO, H, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_boundary(cfg(T=0, d=256), X, Y, G, None, G, XO, H, None) == L.MOE_OK
+
+
 def test_stage_names_and_status_strings():
     n = L.moe_num_stages()
     assert n == 8
