@@ -57,7 +57,8 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
     // columns [0, 64) gate, [64, 128) up of output features n_blk*64 ..
-    const float sc = P.row_scale[row] * P.grp_scale[tc.e];
+    // rows past the tile's valid ones may lie past the scale array: never read them
+    const float sc = row_ok ? P.row_scale[row] * P.grp_scale[tc.e] : 0.f;
     const float gam = P.out_scale[tc.e];
     const float six_g = 6.0f * gam;
     const float inv_g = gam > 0.f ? 1.0f / gam : 0.f;
