@@ -57,8 +57,9 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
     // columns [0, 64) gate, [64, 128) up of output features n_blk*64 ..
-    // rows past the tile's valid ones may lie past the scale array: never read them
-    const float sc = row_ok ? P.row_scale[row] * P.grp_scale[tc.e] : 0.f;
+    // every row of a tile lies inside the expert's 128-row padded block, so the scale
+    // array (one entry per padded row) covers it even when the row holds no token
+    const float sc = P.row_scale[row] * P.grp_scale[tc.e];
     const float gam = P.out_scale[tc.e];
     const float six_g = 6.0f * gam;
     const float inv_g = gam > 0.f ? 1.0f / gam : 0.f;
@@ -75,7 +76,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       for (int i = 0; i < 16; ++i) {
         const float a = __uint_as_float(g[i]) * sc;
         const float b = __uint_as_float(u[i]) * sc;
-        s[i] = a / (1.0f + __expf(-a)) * b;     // silu(a) * b
+        s[i] = __fdividef(a, 1.0f + __expf(-a)) * b;     // silu(a) * b
       }
       uint2 q;
       const uint32_t code = quantize16(s, six_g, inv_g, q, recip);

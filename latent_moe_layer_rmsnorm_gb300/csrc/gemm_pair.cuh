@@ -175,7 +175,7 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float a = __uint_as_float(g[i]);
-        v[i] = a / (1.0f + __expf(-a)) * __uint_as_float(u[i]);   // silu(a) * b
+        v[i] = __fdividef(a, 1.0f + __expf(-a)) * __uint_as_float(u[i]);   // silu(a) * b
       }
       if (row_ok) store16(P.out, base + c0, P.out_fmt, v);
     }

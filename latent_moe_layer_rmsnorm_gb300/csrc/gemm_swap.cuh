@@ -82,7 +82,7 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& P, const SwapTil
         if (c0 + jj < tc.valid) {
           const float a = __uint_as_float(g[jj]);
           const float b = __uint_as_float(u[jj]);
-          const float s = a / (1.0f + __expf(-a)) * b;      // silu(a) * b
+          const float s = __fdividef(a, 1.0f + __expf(-a)) * b;      // silu(a) * b
           const size_t idx = static_cast<size_t>(tc.tok_row + c0 + jj) * P.ld_out + f;
           if (P.out_fmt == OUT_BF16)
             reinterpret_cast<__nv_bfloat16*>(P.out)[idx] = __float2bfloat16_rn(s);

@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(MEM_THREADS)
 // ---- combine -----------------------------------------------------------------------
 // One block per token.  The down GEMM's epilogue left, for every stored expert output row,
 // the sum of squares of each 128-column block (row_ssq, [rows, p / 128]); the k row norms
-// r_j = rsqrt(sum / p + eps) come from those blocks added in column order, so the rows
-// are read once: c = sum_j w_j * r_j * g_exp[e_j] * y_j, accumulated in FP32 in slot
+// r_j = rsqrt(sum / p + eps) come from those blocks (added by a fixed warp tree) while
+// the first loads of the rows are in flight, so the rows are read once: c = sum_j w_j * r_j * g_exp[e_j] * y_j, accumulated in FP32 in slot
 // order j = 0..k-1 and stored as the unpooler's operand: FP16
 // (|c_i| <= sum_j |w_j| * sqrt(p) * max|g_exp|), or TF32-rounded FP32.
 template <bool C_F32>
@@ -299,33 +299,53 @@ __global__ void __launch_bounds__(MEM_THREADS)
                    const int* __restrict__ inv, const int32_t* __restrict__ ids,
                    const float* __restrict__ wts, const float* __restrict__ g_exp,
                    void* __restrict__ c_out, int p, int k, int E, float eps) {
-  __shared__ int rows[MAX_TOPK];
-  __shared__ int eids[MAX_TOPK];
   __shared__ float sj[MAX_TOPK];     // w_j * r_j
   const size_t t = blockIdx.x;
-  if (threadIdx.x < k) {
-    int r = inv[t * k + threadIdx.x];
-    int e = ids[t * k + threadIdx.x];
-    if (e < 0 || e >= E) { r = -1; e = 0; }
-    float ss = 0.f;
-    if (r >= 0) {
-      const float* q = row_ssq + size_t(r) * (p >> 7);
-      for (int i = 0; i < (p >> 7); ++i) ss += q[i];
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  // every thread reads the token's k slots (broadcast loads) so that its row loads can
+  // be in flight while the norms are formed
+  int rows[MAX_TOPK], eids[MAX_TOPK];
+#pragma unroll
+  for (int j = 0; j < MAX_TOPK; ++j) {
+    rows[j] = -1;
+    eids[j] = 0;
+    if (j < k) {
+      const int e = ids[t * k + j];
+      if (e >= 0 && e < E) { rows[j] = inv[t * k + j]; eids[j] = e; }
     }
-    rows[threadIdx.x] = r;
-    eids[threadIdx.x] = e;
-    sj[threadIdx.x] = wts[t * k + threadIdx.x] * rsqrtf(ss / static_cast<float>(p) + eps);
   }
-  __syncthreads();
   const int nchunk = p >> 3;
-  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-    float4 ya[MAX_TOPK], yb[MAX_TOPK];      // issue every row's loads before the sums
+  const int c = threadIdx.x;               // first chunk of this thread
+  float4 ya[MAX_TOPK], yb[MAX_TOPK];
+  if (c < nchunk) {
 #pragma unroll
     for (int j = 0; j < MAX_TOPK; ++j) {
-      if (j < k && rows[j] >= 0) {
+      if (rows[j] >= 0) {
         const float4* src = reinterpret_cast<const float4*>(y + size_t(rows[j]) * p) + 2 * c;
         ya[j] = src[0];
         yb[j] = src[1];
+      }
+    }
+  }
+  // warp j: the 128-column sums of squares of slot j's row, added by a fixed tree
+  if (w < k) {
+    const int parts = p >> 7;
+    float ss = 0.f;
+    if (rows[w] >= 0)
+      for (int i = l; i < parts; i += 32) ss += row_ssq[size_t(rows[w]) * parts + i];
+    ss = warp_sum(ss);
+    if (l == 0) sj[w] = wts[t * k + w] * rsqrtf(ss / static_cast<float>(p) + eps);
+  }
+  __syncthreads();
+  for (int cc = c; cc < nchunk; cc += blockDim.x) {
+    if (cc != c) {
+#pragma unroll
+      for (int j = 0; j < MAX_TOPK; ++j) {
+        if (rows[j] >= 0) {
+          const float4* src = reinterpret_cast<const float4*>(y + size_t(rows[j]) * p) + 2 * cc;
+          ya[j] = src[0];
+          yb[j] = src[1];
+        }
       }
     }
     float acc[8];
@@ -333,29 +353,29 @@ __global__ void __launch_bounds__(MEM_THREADS)
     for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
     for (int j = 0; j < MAX_TOPK; ++j) {
-      if (j < k && rows[j] >= 0) {
-        const float4* g = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p) + 2 * c;
+      if (rows[j] >= 0) {
+        const float4* g = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p) + 2 * cc;
         const float4 g0 = g[0], g1 = g[1];
-        const float s = sj[j];
-        acc[0] = fmaf(s, ya[j].x * g0.x, acc[0]);
-        acc[1] = fmaf(s, ya[j].y * g0.y, acc[1]);
-        acc[2] = fmaf(s, ya[j].z * g0.z, acc[2]);
-        acc[3] = fmaf(s, ya[j].w * g0.w, acc[3]);
-        acc[4] = fmaf(s, yb[j].x * g1.x, acc[4]);
-        acc[5] = fmaf(s, yb[j].y * g1.y, acc[5]);
-        acc[6] = fmaf(s, yb[j].z * g1.z, acc[6]);
-        acc[7] = fmaf(s, yb[j].w * g1.w, acc[7]);
+        const float sc = sj[j];
+        acc[0] = fmaf(sc, ya[j].x * g0.x, acc[0]);
+        acc[1] = fmaf(sc, ya[j].y * g0.y, acc[1]);
+        acc[2] = fmaf(sc, ya[j].z * g0.z, acc[2]);
+        acc[3] = fmaf(sc, ya[j].w * g0.w, acc[3]);
+        acc[4] = fmaf(sc, yb[j].x * g1.x, acc[4]);
+        acc[5] = fmaf(sc, yb[j].y * g1.y, acc[5]);
+        acc[6] = fmaf(sc, yb[j].z * g1.z, acc[6]);
+        acc[7] = fmaf(sc, yb[j].w * g1.w, acc[7]);
       }
     }
     if constexpr (C_F32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(c_out) + t * p) + 2 * c;
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(c_out) + t * p) + 2 * cc;
       dst[0] = make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]), tf32_rna(acc[2]), tf32_rna(acc[3]));
       dst[1] = make_float4(tf32_rna(acc[4]), tf32_rna(acc[5]), tf32_rna(acc[6]), tf32_rna(acc[7]));
     } else {
       uint4 o;
       o.x = pack_f16x2(acc[0], acc[1]); o.y = pack_f16x2(acc[2], acc[3]);
       o.z = pack_f16x2(acc[4], acc[5]); o.w = pack_f16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(static_cast<__half*>(c_out) + t * p)[c] = o;
+      reinterpret_cast<uint4*>(static_cast<__half*>(c_out) + t * p)[cc] = o;
     }
   }
 }
