@@ -46,13 +46,41 @@ struct NvSmem {
   float recip[256];
 };
 
+// The down GEMM's epilogue writes y through shared memory: each epilogue warp stages a
+// 32-row x 32-column FP32 box (4 KB, 128-byte swizzle) and stores it with TMA, instead of
+// 32 rows of 16-byte pieces per store instruction (those stores cost about a third of
+// the kernel's time, measured).  Expert rows are padded to 128 per expert, so a box never
+// reaches another expert's rows; rows past an expert's last token are padding.
+constexpr int NV_Y_BOX = 32 * 32 * 4;
+
 constexpr size_t nvf4_smem_bytes() {
-  return 1024 + size_t(NV_STAGES) * (NV_A_STAGE + NV_B_STAGE + 2 * NV_SF_STAGE) + sizeof(NvSmem);
+  return 1024 + size_t(NV_STAGES) * (NV_A_STAGE + NV_B_STAGE + 2 * NV_SF_STAGE) +
+         4 * NV_Y_BOX + sizeof(NvSmem);
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0,
+                                             int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// the previous stores have read their shared-memory source
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 template <int EPI>
 __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoord& tc,
-                                              uint32_t taddr, int r, const float* recip) {
+                                              uint32_t taddr, int r, const float* recip,
+                                              const CUtensorMap* tmY, uint8_t* ybox) {
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
@@ -88,7 +116,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
     }
   } else {
     const float sc = P.grp_scale[tc.e] * P.out_scale[tc.e];
-    const size_t base = row * P.ld_out + static_cast<size_t>(tc.n_blk) * NV_BN;
+    const int lane = r & 31;
     float ss = 0.f;     // the tile is one 128-column block of the row (row_ssq)
 #pragma unroll 1
     for (int c0 = 0; c0 < NV_BN; c0 += 32) {
@@ -102,10 +130,19 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
         va[i] = __uint_as_float(a[i]) * sc;
         vb[i] = __uint_as_float(b[i]) * sc;
       }
-      if (row_ok) {
-        store16(P.out, base + c0, OUT_F32, va);
-        store16(P.out, base + c0 + 16, OUT_F32, vb);
+      // this warp's 32 rows x 32 columns through the staging box: row `lane`, 16-byte
+      // chunk j at chunk (j ^ lane % 8) (the 128-byte swizzle of the tensor map)
+      if (lane == 0) tma_store_wait_read();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float* v = j < 4 ? va + 4 * j : vb + 4 * (j - 4);
+        *reinterpret_cast<float4*>(ybox + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            make_float4(v[0], v[1], v[2], v[3]);
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + c0, tc.a_row + (r - lane));
 #pragma unroll
       for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
 #pragma unroll
@@ -118,7 +155,8 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
 template <int EPI>
 __global__ void __launch_bounds__(NV_THREADS, 1)
     gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmParams P) {
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmY, const GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -126,7 +164,8 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
   uint8_t* sB = sA + NV_STAGES * NV_A_STAGE;
   uint8_t* sSA = sB + NV_STAGES * NV_B_STAGE;
   uint8_t* sSB = sSA + NV_STAGES * NV_SF_STAGE;
-  NvSmem* N = reinterpret_cast<NvSmem*>(sSB + NV_STAGES * NV_SF_STAGE);
+  uint8_t* sY = sSB + NV_STAGES * NV_SF_STAGE;     // 4 staging boxes (down GEMM), 1 KB aligned
+  NvSmem* N = reinterpret_cast<NvSmem*>(sY + 4 * NV_Y_BOX);
   GemmSmem* S = &N->g;
 
   const int warp = threadIdx.x >> 5;
@@ -294,11 +333,12 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       tc_fence_after();
       const TileCoord tc = gemm_tile(P, S, t);
       const uint32_t taddr = tmem_base + acc * NV_BN + (static_cast<uint32_t>(q * 32) << 16);
-      nvf4_epilogue<EPI>(P, tc, taddr, r, N->recip);
+      nvf4_epilogue<EPI>(P, tc, taddr, r, N->recip, &tmY, sY + q * NV_Y_BOX);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S->tempty[acc]);
     }
+    if (EPI == NV_EPI_STORE_F32 && lane == 0) tma_store_wait_all();   // y fully written
   }
 
   tc_fence_before();

@@ -472,7 +472,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.sf_a = sf_u; P.sf_b = W->sf13; P.row_scale = alpha; P.grp_scale = W->gs13;
     P.out_scale = W->gs_act2; P.out_sf = sf_s;
     const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, ta, P);
     MOE_TRY(last_launch());
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on the MMA's M side (256-row W13 blocks: 128 gate + 128 up), tokens on N
@@ -515,9 +515,10 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   void* y_buf = base + L.y;
   float* ssq = reinterpret_cast<float*>(base + L.ssq);
   if (nvf4) {
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;   // ty: y in 32 x 32 FP32 boxes for the epilogue's stores
     if (!make_tmap(&ta, s_buf, OP_NVF4, I / 2, R, GEMM_BM) ||
-        !make_tmap(&tb, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, NV_BN))
+        !make_tmap(&tb, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, NV_BN) ||
+        !make_tmap(&ty, y_buf, OP_TF32, p, R, 32))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = NV_BN; P.groups = E_;
@@ -525,7 +526,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = y_buf; P.ld_out = p; P.row_ssq = ssq;
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
     const int grid = std::min(sms, max_mt * (p / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, P);
+    gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, ty, P);
     MOE_TRY(last_launch());
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on M (128 rows of p), up to 256 tokens on N
