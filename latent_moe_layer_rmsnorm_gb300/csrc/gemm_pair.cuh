@@ -31,7 +31,10 @@
 
 namespace lmoe {
 
-constexpr int PAIR_STAGES = 6;
+// Seven 32 KB stages: the kernel is bound by how far the loads run ahead of the MMAs
+// (6 stages kept the tensor pipe ~76 % busy), so the per-expert tables stay in global
+// memory (L1-cached reads) to leave the shared memory to the stages.
+constexpr int PAIR_STAGES = 7;
 constexpr int PAIR_STAGE = 2 * 128 * 128;     // A 128 rows + B 128 rows of 128 bytes
 
 struct PairSmem {
@@ -42,9 +45,6 @@ struct PairSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int mt_off[GEMM_MAX_GROUPS + 1];
-  int row_off[GEMM_MAX_GROUPS + 1];
-  int row_cnt[GEMM_MAX_GROUPS + 1];
 };
 
 constexpr size_t pair_smem_bytes() {
@@ -139,17 +139,18 @@ __device__ __forceinline__ TileCoord pair_tile(const GemmParams& P, const PairSm
   int lo = 0, hi = P.groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (S->mt_off[mid] * nb <= t) lo = mid; else hi = mid - 1;
+    if (__ldg(P.mt_off + mid) * nb <= t) lo = mid; else hi = mid - 1;
   }
   const int e = lo;
-  const int np_e = S->mt_off[e + 1] - S->mt_off[e];
-  const int local = t - S->mt_off[e] * nb;
+  const int mt_e = __ldg(P.mt_off + e);
+  const int np_e = __ldg(P.mt_off + e + 1) - mt_e;
+  const int local = t - mt_e * nb;
   c.n_blk = local / np_e;
   const int pr = local - c.n_blk * np_e;
-  const int left = S->row_cnt[e] - pr * 256;     // rows of this expert from the tile on
+  const int left = __ldg(P.row_cnt + e) - pr * 256;   // rows of this expert from the tile on
   small = left <= 128;
   const int half = small ? 64 : 128;
-  c.a_row = S->row_off[e] + pr * 256 + half * static_cast<int>(rank);
+  c.a_row = __ldg(P.row_off + e) + pr * 256 + half * static_cast<int>(rank);
   c.b_row = e * P.N + c.n_blk * P.bn + 128 * static_cast<int>(rank);
   c.valid = min(half, left - half * static_cast<int>(rank));
   c.e = e;
@@ -241,13 +242,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmB64);
     }
   }
-  if (P.groups > 0) {
-    for (int i = threadIdx.x; i <= P.groups; i += blockDim.x) {
-      S->mt_off[i] = P.mt_off[i];
-      S->row_off[i] = P.row_off[i];
-      S->row_cnt[i] = P.row_cnt[i];
-    }
-  }
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&S->tmem_base)),
@@ -262,7 +256,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
   constexpr bool TF32 = KIND == OP_TF32;
   const uint32_t tmem_base = S->tmem_base;
   const int nb = P.N / P.bn;
-  const int num_tiles = P.groups == 0 ? ((P.M + 255) / 256) * nb : S->mt_off[P.groups] * nb;
+  const int num_tiles = P.groups == 0 ? ((P.M + 255) / 256) * nb : __ldg(P.mt_off + P.groups) * nb;
   const int cluster_id = blockIdx.x >> 1;
   const int num_clusters = gridDim.x >> 1;
   const int kblocks = P.K / (TF32 ? 32 : 64);
