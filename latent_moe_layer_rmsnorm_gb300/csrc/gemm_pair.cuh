@@ -31,10 +31,10 @@
 
 namespace lmoe {
 
-// Seven 32 KB stages: the kernel is bound by how far the loads run ahead of the MMAs
-// (6 stages kept the tensor pipe ~76 % busy), so the per-expert tables stay in global
-// memory (L1-cached reads) to leave the shared memory to the stages.
-constexpr int PAIR_STAGES = 7;
+// Six 32 KB stages (a seventh measured neutral) and four 4 KB output boxes; the
+// per-expert tables stay in global memory (L1-cached reads).
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_BOX = 32 * 128;            // one epilogue warp's 32 rows x 128 bytes
 constexpr int PAIR_STAGE = 2 * 128 * 128;     // A 128 rows + B 128 rows of 128 bytes
 
 struct PairSmem {
@@ -48,7 +48,7 @@ struct PairSmem {
 };
 
 constexpr size_t pair_smem_bytes() {
-  return 1024 + size_t(PAIR_STAGES) * PAIR_STAGE + sizeof(PairSmem);
+  return 1024 + size_t(PAIR_STAGES) * PAIR_STAGE + 4 * PAIR_BOX + sizeof(PairSmem);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -206,16 +206,113 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
   }
 }
 
+// Put 16 consecutive output values of row `lane` into the warp's staging box at byte
+// offset `off` of the row (128-byte swizzle: 16-byte chunk j lands at chunk j ^ lane % 8).
+__device__ __forceinline__ void box_put16(uint8_t* box, int lane, int off, int fmt,
+                                          const float (&v)[16]) {
+  uint8_t* row = box + lane * 128;
+  if (fmt == OUT_BF16) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = (off >> 4) + h;
+      uint4 o;
+      o.x = pack_bf16x2(v[8 * h], v[8 * h + 1]);     o.y = pack_bf16x2(v[8 * h + 2], v[8 * h + 3]);
+      o.z = pack_bf16x2(v[8 * h + 4], v[8 * h + 5]); o.w = pack_bf16x2(v[8 * h + 6], v[8 * h + 7]);
+      *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
+    }
+  } else {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int j = (off >> 4) + h;
+      float w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = fmt == OUT_TF32 ? tf32_rna(v[4 * h + i]) : v[4 * h + i];
+      *reinterpret_cast<float4*>(row + ((j ^ (lane & 7)) << 4)) = make_float4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// Epilogue of one warp whose 32 rows of a full-height tile are all valid: values go
+// through the warp's shared-memory box and leave as 32-row x 128-byte TMA stores (a row
+// segment per store instead of 16 bytes of each of 32 rows per store instruction).
+// Same values, and for the down GEMM the same 128-column sums of squares in the same
+// column order, as gemm_epilogue.
+template <int EPI>
+__device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const TileCoord& tc,
+                                                    uint32_t taddr, int q, int lane,
+                                                    const CUtensorMap* tmOut, uint8_t* box) {
+  const int es = P.out_fmt == OUT_BF16 ? 2 : 4;
+  const int per_box = 128 / es;                       // values per box row
+  const int row0 = tc.a_row + 32 * q;
+  const size_t row = static_cast<size_t>(row0 + lane);
+  auto put = [&](int col, const float (&v)[16], int col_base) {
+    const int off = ((col - col_base) % per_box) * es;
+    if (off == 0) {
+      if (lane == 0) tma_store_wait_read();
+      __syncwarp();
+    }
+    box_put16(box, lane, off, P.out_fmt, v);
+    if (off + 16 * es == 128) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_store_2d(tmOut, box, col - (col - col_base) % per_box, row0);
+    }
+  };
+  if constexpr (EPI == EPI_STORE) {
+    const int col_base = tc.n_blk * P.bn;
+    float ss = 0.f;
+    for (int c0 = 0; c0 < P.bn; c0 += 32) {
+      uint32_t a[16], b[16];
+      tmem_ld16(taddr + c0, a);
+      tmem_ld16(taddr + c0 + 16, b);
+      tmem_ld_wait();
+      float va[16], vb[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { va[i] = __uint_as_float(a[i]); vb[i] = __uint_as_float(b[i]); }
+      put(col_base + c0, va, col_base);
+      put(col_base + c0 + 16, vb, col_base);
+      if (P.row_ssq) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
+        if (((c0 + 32) & 127) == 0) {
+          P.row_ssq[row * (P.N >> 7) + ((col_base + c0) >> 7)] = ss;
+          ss = 0.f;
+        }
+      }
+    }
+  } else {   // EPI_SWIGLU: gate columns [0, bn/2), up columns [bn/2, bn)
+    const int half = P.bn >> 1;
+    const int col_base = tc.n_blk * half;
+    for (int c0 = 0; c0 < half; c0 += 16) {
+      uint32_t g[16], u[16];
+      tmem_ld16(taddr + c0, g);
+      tmem_ld16(taddr + half + c0, u);
+      tmem_ld_wait();
+      float s[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a = __uint_as_float(g[i]);
+        s[i] = __fdividef(a, 1.0f + __expf(-a)) * __uint_as_float(u[i]);   // silu(a) * b
+      }
+      put(col_base + c0, s, col_base);
+    }
+  }
+}
+
 template <int KIND, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmA64,
                      const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmB64, const GemmParams P) {
+                     const __grid_constant__ CUtensorMap tmB64,
+                     const __grid_constant__ CUtensorMap tmOut, const GemmParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  PairSmem* S = reinterpret_cast<PairSmem*>(smem + PAIR_STAGES * PAIR_STAGE);
+  uint8_t* boxes = smem + PAIR_STAGES * PAIR_STAGE;     // 1 KB aligned
+  PairSmem* S = reinterpret_cast<PairSmem*>(boxes + 4 * PAIR_BOX);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -367,11 +464,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t taddr =
           tmem_base + acc * GEMM_BN_MAX + (static_cast<uint32_t>(q * 32) << 16);
       if (small) pair_small_epilogue<EPI>(P, tc, taddr, (q & 1) * 32 + lane, q >> 1);
+      else if (P.out_box && tc.valid >= 32 * (q + 1))
+        pair_epilogue_boxes<EPI>(P, tc, taddr, q, lane, &tmOut, boxes + q * PAIR_BOX);
       else gemm_epilogue<EPI>(P, tc, taddr, r);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&S->tempty[acc]), 0));
     }
+    if (lane == 0) tma_store_wait_all();   // the box stores have landed
   }
 
   tc_fence_before();

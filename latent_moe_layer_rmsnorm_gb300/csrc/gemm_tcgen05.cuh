@@ -77,6 +77,8 @@ struct GemmParams {
   // values, at row_ssq[row * (N / 128) + column / 128], each summed in column order
   // (the per-expert RMSNorm reads these instead of a second pass over the row)
   float* row_ssq;
+  int out_box;   // CTA-pair kernels: 1 = write full 32-row blocks through the output's
+                 // tensor map (the kernel's tmOut) instead of per-thread stores
 };
 
 struct GemmSmem {

@@ -287,13 +287,16 @@ moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
 // `ta64` / `tb64` map A / B with 64-row boxes (the grouped GEMMs' M = 128 tiles; `tb64`
 // only for the gate/up GEMM; both unused when dense).
 template <int KIND, int EPI>
+// `tout` maps the output in 32-row boxes of 128 bytes: warps whose 32 rows of a tile are
+// all valid write through it (P.out_box is set here).
 moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& ta64, const CUtensorMap& tb,
-                         const CUtensorMap& tb64, const GemmParams& P, int max_tiles, int sms,
-                         cudaStream_t st) {
+                         const CUtensorMap& tb64, const CUtensorMap& tout, GemmParams P,
+                         int max_tiles, int sms, cudaStream_t st) {
   const int clusters = std::min(sms / 2, max_tiles);
   if (clusters <= 0) return MOE_OK;
+  P.out_box = 1;
   gemm_pair_kernel<KIND, EPI><<<2 * clusters, GEMM_THREADS, pair_smem_bytes(), st>>>(
-      ta, ta64, tb, tb64, P);
+      ta, ta64, tb, tb64, tout, P);
   return last_launch();
 }
 
@@ -409,11 +412,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     if (sp.pool > 1) { P.ksplit = sp.pool; P.split_stride = size_t(T) * p; P.out = part; }
     const int grid = std::min(sms, mtiles * (p / bn) * sp.pool);
     if (sp.pool == 1 && bn == 256) {          // CTA pairs: B half-tiles of 128 rows
-      CUtensorMap tb2;
-      if (!make_tmap(&tb2, W->w_pool, k_proj, d, p, 128)) return MOE_ERR_CUDA;
+      CUtensorMap tb2, to;
+      if (!make_tmap(&tb2, W->w_pool, k_proj, d, p, 128) ||
+          !make_tmap(&to, pooled, OP_TF32, p, T, 32))
+        return MOE_ERR_CUDA;
       const int tiles = ((T + 255) / 256) * (p / 256);
-      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
-      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
+      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
     } else if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     if (sp.pool > 1) {
@@ -505,9 +510,11 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.row_off = row_off; P.mt_off = mt2_off; P.row_cnt = row_cnt;
     P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
+    CUtensorMap to;
+    if (!make_tmap(&to, s_buf, exp_f32 ? OP_TF32 : OP_BF16, I, rows, 32)) return MOE_ERR_CUDA;
     const int tiles = (rows / 256 + E_) * (2 * I / P.bn);
-    if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_SWIGLU>(ta, ta64, tb, tb64, P, tiles, sms, st)));
-    else MOE_TRY((launch_pair<OP_F16, EPI_SWIGLU>(ta, ta64, tb, tb64, P, tiles, sms, st)));
+    if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_SWIGLU>(ta, ta64, tb, tb64, to, P, tiles, sms, st)));
+    else MOE_TRY((launch_pair<OP_F16, EPI_SWIGLU>(ta, ta64, tb, tb64, to, P, tiles, sms, st)));
   }
   E.mark(5);
 
@@ -557,15 +564,16 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.row_off = row_off; P.row_cnt = row_cnt;
     P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32; P.row_ssq = ssq;
     if (bn == 256) {    // CTA pairs over 256-row tiles (M = 128 pair tiles for remainders)
-      CUtensorMap ta64;
+      CUtensorMap ta64, to;
       if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
           !make_tmap(&ta64, s_buf, k_down, I, rows, GEMM_BM / 2) ||
-          !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128))
+          !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128) ||
+          !make_tmap(&to, y_buf, OP_TF32, p, rows, 32))
         return MOE_ERR_CUDA;
       P.mt_off = mt2_off;
       const int tiles = (rows / 256 + E_) * (p / 256);
-      if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta64, tb, tb, P, tiles, sms, st)));
-      else MOE_TRY((launch_pair<OP_BF16, EPI_STORE>(ta, ta64, tb, tb, P, tiles, sms, st)));
+      if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_BF16, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
     } else {
       if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
           !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, bn))
@@ -604,11 +612,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     }
     const int grid = std::min(sms, mtiles * (d / bn) * sp.unpool);
     if (sp.unpool == 1 && bn == 256) {        // CTA pairs
-      CUtensorMap tb2;
-      if (!make_tmap(&tb2, W->w_unpool, k_proj, p, d, 128)) return MOE_ERR_CUDA;
+      CUtensorMap tb2, to;
+      if (!make_tmap(&tb2, W->w_unpool, k_proj, p, d, 128) ||
+          !make_tmap(&to, out, P.out_fmt == OUT_BF16 ? OP_BF16 : OP_TF32, d, T, 32))
+        return MOE_ERR_CUDA;
       const int tiles = ((T + 255) / 256) * (d / 256);
-      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
-      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, P, tiles, sms, st)));
+      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
     } else if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     if (sp.unpool > 1) {
