@@ -282,7 +282,7 @@ __device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const T
         }
       }
     }
-  } else {   // EPI_SWIGLU: gate columns [0, bn/2), up columns [bn/2, bn)
+  } else if constexpr (EPI == EPI_SWIGLU) {   // gate columns [0, bn/2), up [bn/2, bn)
     const int half = P.bn >> 1;
     const int col_base = tc.n_blk * half;
     for (int c0 = 0; c0 < half; c0 += 16) {

@@ -137,6 +137,9 @@ moe_status_t device_ready(int* sms) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_SWIGLU>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_ROUTER>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     D.ready = true;
   }
@@ -291,10 +294,10 @@ template <int KIND, int EPI>
 // all valid write through it (P.out_box is set here).
 moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& ta64, const CUtensorMap& tb,
                          const CUtensorMap& tb64, const CUtensorMap& tout, GemmParams P,
-                         int max_tiles, int sms, cudaStream_t st) {
+                         int max_tiles, int sms, cudaStream_t st, bool boxes = true) {
   const int clusters = std::min(sms / 2, max_tiles);
   if (clusters <= 0) return MOE_OK;
-  P.out_box = 1;
+  P.out_box = boxes ? 1 : 0;
   gemm_pair_kernel<KIND, EPI><<<2 * clusters, GEMM_THREADS, pair_smem_bytes(), st>>>(
       ta, ta64, tb, tb64, tout, P);
   return last_launch();
@@ -387,6 +390,12 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, std::min(sms, mtiles * sp.router), st)));
       router_reduce_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(part, sp.router, T, bn, E_, k, ids, wts);
       MOE_TRY(last_launch());
+    } else if (bn == 256) {   // CTA pairs: each CTA loads 128 of the 256 router rows
+      P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
+      CUtensorMap tb2;
+      if (!make_tmap(&tb2, W->w_router, OP_TF32, d, E_, 128)) return MOE_ERR_CUDA;
+      MOE_TRY((launch_pair<OP_TF32, EPI_ROUTER>(ta, ta, tb2, tb2, ta, P, (T + 255) / 256, sms, st,
+                                                false)));
     } else {
       P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
       MOE_TRY((launch_gemm<OP_TF32, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st)));
