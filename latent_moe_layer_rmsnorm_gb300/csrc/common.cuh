@@ -21,6 +21,7 @@ enum : int {
   WAIT_MMA_TMEM_EMPTY = 3,
   WAIT_EPI_TMEM_FULL = 4,
   WAIT_DRAIN = 5,
+  WAIT_COMBINE = 6,
   CHECK_EXPERT_ID = 16,
   CHECK_ROW = 17,
 };

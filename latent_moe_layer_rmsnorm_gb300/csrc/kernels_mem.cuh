@@ -287,96 +287,98 @@ __global__ void __launch_bounds__(MEM_THREADS)
 }
 
 // ---- combine -----------------------------------------------------------------------
-// One block per token.  The down GEMM's epilogue left, for every stored expert output row,
-// the sum of squares of each 128-column block (row_ssq, [rows, p / 128]); the k row norms
-// r_j = rsqrt(sum / p + eps) come from those blocks (added by a fixed warp tree) while
-// the first loads of the rows are in flight, so the rows are read once: c = sum_j w_j * r_j * g_exp[e_j] * y_j, accumulated in FP32 in slot
-// order j = 0..k-1 and stored as the unpooler's operand: FP16
+// One block per (token, slice of `cols` columns, at most 1024) with cols / 4 threads.
+// The down GEMM's epilogue left, for every stored expert output row, the sum of squares
+// of each 128-column block (row_ssq, [rows, p / 128]).  Thread 0 bulk-copies the token's
+// k row slices into shared memory while the warps form r_j = rsqrt(sum / p + eps) from
+// row j's blocks (a fixed warp tree), so the rows are read once and each block keeps up
+// to 32 KB in flight with few registers; then c = sum_j w_j * r_j * g_exp[e_j] * y_j is accumulated in FP32
+// in slot order j = 0..k-1 and stored as the unpooler's operand: FP16
 // (|c_i| <= sum_j |w_j| * sqrt(p) * max|g_exp|), or TF32-rounded FP32.
+constexpr int COMBINE_MAX_COLS = 1024;
+
+// Columns per block: the largest multiple of 128 that divides p, at most 1024.
+inline int combine_cols(int p) {
+  for (int c = COMBINE_MAX_COLS; c > 128; c -= 128)
+    if (p % c == 0) return c;
+  return 128;
+}
+
 template <bool C_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     combine_kernel(const float* __restrict__ y, const float* __restrict__ row_ssq,
                    const int* __restrict__ inv, const int32_t* __restrict__ ids,
                    const float* __restrict__ wts, const float* __restrict__ g_exp,
-                   void* __restrict__ c_out, int p, int k, int E, float eps) {
+                   void* __restrict__ c_out, int p, int cols, int k, int E, float eps,
+                   int* status, unsigned long long timeout_ns) {
+  extern __shared__ __align__(16) uint8_t cmb_smem[];
+  __shared__ uint64_t landed;
   __shared__ float sj[MAX_TOPK];     // w_j * r_j
-  const size_t t = blockIdx.x;
+  __shared__ int srow[MAX_TOPK], seid[MAX_TOPK];
+  const int nq = p / cols;
+  const size_t t = blockIdx.x / nq;
+  const int col0 = static_cast<int>(blockIdx.x % nq) * cols;
+  const uint32_t slice = static_cast<uint32_t>(cols) * 4;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  // every thread reads the token's k slots (broadcast loads) so that its row loads can
-  // be in flight while the norms are formed
-  int rows[MAX_TOPK], eids[MAX_TOPK];
-#pragma unroll
-  for (int j = 0; j < MAX_TOPK; ++j) {
-    rows[j] = -1;
-    eids[j] = 0;
-    if (j < k) {
-      const int e = ids[t * k + j];
-      if (e >= 0 && e < E) { rows[j] = inv[t * k + j]; eids[j] = e; }
+  if (threadIdx.x < MAX_TOPK) {
+    int r = -1, e = 0;
+    if (static_cast<int>(threadIdx.x) < k) {
+      const int id = ids[t * k + threadIdx.x];
+      if (id >= 0 && id < E) { r = inv[t * k + threadIdx.x]; e = id; }
     }
+    srow[threadIdx.x] = r;
+    seid[threadIdx.x] = e;
   }
-  const int nchunk = p >> 3;
-  const int c = threadIdx.x;               // first chunk of this thread
-  float4 ya[MAX_TOPK], yb[MAX_TOPK];
-  if (c < nchunk) {
-#pragma unroll
-    for (int j = 0; j < MAX_TOPK; ++j) {
-      if (rows[j] >= 0) {
-        const float4* src = reinterpret_cast<const float4*>(y + size_t(rows[j]) * p) + 2 * c;
-        ya[j] = src[0];
-        yb[j] = src[1];
-      }
-    }
-  }
-  // warp j: the 128-column sums of squares of slot j's row, added by a fixed tree
-  if (w < k) {
-    const int parts = p >> 7;
-    float ss = 0.f;
-    if (rows[w] >= 0)
-      for (int i = l; i < parts; i += 32) ss += row_ssq[size_t(rows[w]) * parts + i];
-    ss = warp_sum(ss);
-    if (l == 0) sj[w] = wts[t * k + w] * rsqrtf(ss / static_cast<float>(p) + eps);
+  if (threadIdx.x == 0) {
+    mbar_init(&landed, 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  for (int cc = c; cc < nchunk; cc += blockDim.x) {
-    if (cc != c) {
-#pragma unroll
-      for (int j = 0; j < MAX_TOPK; ++j) {
-        if (rows[j] >= 0) {
-          const float4* src = reinterpret_cast<const float4*>(y + size_t(rows[j]) * p) + 2 * cc;
-          ya[j] = src[0];
-          yb[j] = src[1];
-        }
-      }
-    }
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-    for (int j = 0; j < MAX_TOPK; ++j) {
-      if (rows[j] >= 0) {
-        const float4* g = reinterpret_cast<const float4*>(g_exp + size_t(eids[j]) * p) + 2 * cc;
-        const float4 g0 = g[0], g1 = g[1];
-        const float sc = sj[j];
-        acc[0] = fmaf(sc, ya[j].x * g0.x, acc[0]);
-        acc[1] = fmaf(sc, ya[j].y * g0.y, acc[1]);
-        acc[2] = fmaf(sc, ya[j].z * g0.z, acc[2]);
-        acc[3] = fmaf(sc, ya[j].w * g0.w, acc[3]);
-        acc[4] = fmaf(sc, yb[j].x * g1.x, acc[4]);
-        acc[5] = fmaf(sc, yb[j].y * g1.y, acc[5]);
-        acc[6] = fmaf(sc, yb[j].z * g1.z, acc[6]);
-        acc[7] = fmaf(sc, yb[j].w * g1.w, acc[7]);
-      }
-    }
-    if constexpr (C_F32) {
-      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(c_out) + t * p) + 2 * cc;
-      dst[0] = make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]), tf32_rna(acc[2]), tf32_rna(acc[3]));
-      dst[1] = make_float4(tf32_rna(acc[4]), tf32_rna(acc[5]), tf32_rna(acc[6]), tf32_rna(acc[7]));
-    } else {
-      uint4 o;
-      o.x = pack_f16x2(acc[0], acc[1]); o.y = pack_f16x2(acc[2], acc[3]);
-      o.z = pack_f16x2(acc[4], acc[5]); o.w = pack_f16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(static_cast<__half*>(c_out) + t * p)[cc] = o;
-    }
+  if (threadIdx.x == 0) {
+    uint32_t bytes = 0;
+    for (int j = 0; j < k; ++j) bytes += srow[j] >= 0 ? slice : 0;
+    mbar_arrive_expect_tx(&landed, bytes);
+    for (int j = 0; j < k; ++j)
+      if (srow[j] >= 0)
+        bulk_load(cmb_smem + j * slice, y + size_t(srow[j]) * p + col0, slice, &landed);
+  }
+  // slot j's 128-column sums of squares, added by a fixed warp tree (warp j mod warps)
+  for (int j = w; j < k; j += static_cast<int>(blockDim.x >> 5)) {
+    const int parts = p >> 7;
+    const int r = srow[j];
+    float ss = 0.f;
+    if (r >= 0)
+      for (int i = l; i < parts; i += 32) ss += row_ssq[size_t(r) * parts + i];
+    ss = warp_sum(ss);
+    if (l == 0) sj[j] = wts[t * k + j] * rsqrtf(ss / static_cast<float>(p) + eps);
+  }
+  {
+    volatile int never = 0;
+    mbar_wait_bounded(&landed, 0, &never, status, WAIT_COMBINE, timeout_ns);
+  }
+  __syncthreads();
+  // each thread: 4 consecutive columns of the quarter
+  const int cl = 4 * threadIdx.x;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    if (srow[j] < 0) continue;
+    const float4 v = *reinterpret_cast<const float4*>(cmb_smem + j * slice + 4 * cl);
+    const float4 g = *reinterpret_cast<const float4*>(g_exp + size_t(seid[j]) * p + col0 + cl);
+    const float sc = sj[j];
+    acc[0] = fmaf(sc, v.x * g.x, acc[0]);
+    acc[1] = fmaf(sc, v.y * g.y, acc[1]);
+    acc[2] = fmaf(sc, v.z * g.z, acc[2]);
+    acc[3] = fmaf(sc, v.w * g.w, acc[3]);
+  }
+  const size_t off = t * p + col0 + cl;
+  if constexpr (C_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(c_out) + off) =
+        make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]), tf32_rna(acc[2]), tf32_rna(acc[3]));
+  } else {
+    uint2 o;
+    o.x = pack_f16x2(acc[0], acc[1]);
+    o.y = pack_f16x2(acc[2], acc[3]);
+    *reinterpret_cast<uint2*>(static_cast<__half*>(c_out) + off) = o;
   }
 }
 

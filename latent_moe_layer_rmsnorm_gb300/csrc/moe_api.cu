@@ -597,12 +597,15 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
 
   // ---- stage: per-expert RMSNorm + FP32 weighted sum -------------------------------------
   void* c_buf = base + L.c;
+  const int ccols = combine_cols(p);
   if (act_f32)
-    combine_kernel<true><<<T, MEM_THREADS, 0, st>>>(static_cast<const float*>(y_buf), ssq, inv, ids,
-                                                    wts, W->g_exp, c_buf, p, k, E_, c.eps);
+    combine_kernel<true><<<T * (p / ccols), ccols / 4, size_t(MAX_TOPK) * ccols * 4, st>>>(
+        static_cast<const float*>(y_buf), ssq, inv, ids, wts, W->g_exp, c_buf, p, ccols, k, E_,
+        c.eps, status, base_params(status, c.flags).timeout_ns);
   else
-    combine_kernel<false><<<T, MEM_THREADS, 0, st>>>(static_cast<const float*>(y_buf), ssq, inv, ids,
-                                                     wts, W->g_exp, c_buf, p, k, E_, c.eps);
+    combine_kernel<false><<<T * (p / ccols), ccols / 4, size_t(MAX_TOPK) * ccols * 4, st>>>(
+        static_cast<const float*>(y_buf), ssq, inv, ids, wts, W->g_exp, c_buf, p, ccols, k, E_,
+        c.eps, status, base_params(status, c.flags).timeout_ns);
   MOE_TRY(last_launch());
   E.mark(7);
 
