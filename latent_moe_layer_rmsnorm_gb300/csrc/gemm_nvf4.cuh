@@ -19,7 +19,13 @@
 // Copying them with tcgen05.cp instead costs about 50 tensor-pipe cycles per chunk,
 // more than the 4 MMAs of the slice take (measured on GB300).  The MMA thread issues
 // 4 block-scaled MMAs (K = 64 each) per 128-byte K slice once its scales are in place.
-// TMEM: accumulators in columns [0, 256), a ring of per-stage scale columns after them.
+// Tiles are 128 rows x 256 columns: per K slice 16 KB of A, 32 KB of B and 6 KB of
+// scales for 128 x 256 x 256 MACs, a quarter fewer bytes per MAC than 128 x 128 tiles
+// (the kernel is bound by the rate TMA fills shared memory, about 52 B/clk per SM
+// measured).  TMEM then holds one 256-column accumulator (columns [0, 256)) and a ring
+// of per-stage scale columns after it, so the epilogue of a tile runs before the next
+// tile's MMAs start; eight epilogue warps (two per lane quadrant, one per 128-column
+// half) keep that gap short.
 // A rows are 128-aligned per expert (padded dispatch), so a tile's scales are whole chunks.
 #pragma once
 
@@ -27,14 +33,21 @@
 
 namespace lmoe {
 
-constexpr int NV_BN = 128;
-constexpr int NV_STAGES = 5;
+constexpr int NV_BN = 256;
+constexpr int NV_STAGES = 3;
 constexpr int NV_A_STAGE = GEMM_BM * 128;    // 128 rows x 256 FP4
 constexpr int NV_B_STAGE = NV_BN * 128;
-constexpr int NV_SF_STAGE = 4 * 512;         // 4 scale chunks per operand per stage
+constexpr int NV_SFA_STAGE = 4 * 512;        // 4 scale chunks (K = 64 steps) of 128 A rows
+constexpr int NV_SFB_STAGE = 8 * 512;        // the same for both 128-row halves of B
 constexpr int NV_SF_COL0 = 256;
-constexpr int NV_SF_COLS = 32;               // per stage: 16 (A) + 16 (B)
-constexpr int NV_THREADS = 384;              // warps 0-7 as in gemm_tcgen05.cuh, 8-11 scales
+constexpr int NV_SF_COLS = 48;               // per stage: 16 (A) + 32 (B)
+// warps 0 TMA, 1 MMA, 2 TMEM owner, 4-7 epilogue (columns 0-127), 8-11 scales,
+// 12-15 epilogue (columns 128-255)
+constexpr int NV_THREADS = 512;
+// NVFP4 W13 rows interleave gate and up in blocks of 64: each 128-column half of a tile
+// holds 64 gate columns and the matching 64 up columns (the layout moe_quantize_nvfp4
+// writes and include/latent_moe.h documents)
+constexpr int NV_W13_GROUP = 64;
 
 enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_F32 = 1 };
 
@@ -54,20 +67,23 @@ struct NvSmem {
 constexpr int NV_Y_BOX = 32 * 32 * 4;
 
 constexpr size_t nvf4_smem_bytes() {
-  return 1024 + size_t(NV_STAGES) * (NV_A_STAGE + NV_B_STAGE + 2 * NV_SF_STAGE) +
-         4 * NV_Y_BOX + sizeof(NvSmem);
+  return 1024 + size_t(NV_STAGES) * (NV_A_STAGE + NV_B_STAGE + NV_SFA_STAGE + NV_SFB_STAGE) +
+         8 * NV_Y_BOX + sizeof(NvSmem);
 }
 
 
 
+// One warp's 32 rows of one 128-column half `hh` of the tile (taddr points at the
+// half's first column).
 template <int EPI>
 __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoord& tc,
-                                              uint32_t taddr, int r, const float* recip,
+                                              uint32_t taddr, int r, int hh, const float* recip,
                                               const CUtensorMap* tmY, uint8_t* ybox) {
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
-    // columns [0, 64) gate, [64, 128) up of output features n_blk*64 ..
+    // columns [0, 64) of the half gate, [64, 128) up, of output features
+    // n_blk * 128 + hh * 64 ..
     // every row of a tile lies inside the expert's 128-row padded block, so the scale
     // array (one entry per padded row) covers it even when the row holds no token
     const float sc = P.row_scale[row] * P.grp_scale[tc.e];
@@ -92,7 +108,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       uint2 q;
       const uint32_t code = quantize16(s, six_g, inv_g, q, recip);
       if (row_ok) {
-        const int col = tc.n_blk * 64 + c0;
+        const int col = tc.n_blk * (NV_BN / 2) + hh * 64 + c0;
         *reinterpret_cast<uint2*>(codes + col / 2) = q;
         P.out_sf[sf_offset(row, col / 16, I)] = static_cast<uint8_t>(code);
       }
@@ -100,9 +116,9 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
   } else {
     const float sc = P.grp_scale[tc.e] * P.out_scale[tc.e];
     const int lane = r & 31;
-    float ss = 0.f;     // the tile is one 128-column block of the row (row_ssq)
+    float ss = 0.f;     // the half is one 128-column block of the row (row_ssq)
 #pragma unroll 1
-    for (int c0 = 0; c0 < NV_BN; c0 += 32) {
+    for (int c0 = 0; c0 < 128; c0 += 32) {
       uint32_t a[16], b[16];
       tmem_ld16(taddr + c0, a);
       tmem_ld16(taddr + c0 + 16, b);
@@ -125,13 +141,14 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + c0, tc.a_row + (r - lane));
+      if (lane == 0)
+        tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0, tc.a_row + (r - lane));
 #pragma unroll
       for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
 #pragma unroll
       for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
     }
-    if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + tc.n_blk] = ss;
+    if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + 2 * tc.n_blk + hh] = ss;
   }
 }
 
@@ -146,9 +163,9 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = sA + NV_STAGES * NV_A_STAGE;
   uint8_t* sSA = sB + NV_STAGES * NV_B_STAGE;
-  uint8_t* sSB = sSA + NV_STAGES * NV_SF_STAGE;
-  uint8_t* sY = sSB + NV_STAGES * NV_SF_STAGE;     // 4 staging boxes (down GEMM), 1 KB aligned
-  NvSmem* N = reinterpret_cast<NvSmem*>(sY + 4 * NV_Y_BOX);
+  uint8_t* sSB = sSA + NV_STAGES * NV_SFA_STAGE;
+  uint8_t* sY = sSB + NV_STAGES * NV_SFB_STAGE;    // 8 staging boxes (down GEMM), 1 KB aligned
+  NvSmem* N = reinterpret_cast<NvSmem*>(sY + 8 * NV_Y_BOX);
   GemmSmem* S = &N->g;
 
   const int warp = threadIdx.x >> 5;
@@ -160,10 +177,8 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       mbar_init(&N->empty[s], 1);
       mbar_init(&N->sf_ready[s], 4);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&S->tfull[a], 1);
-      mbar_init(&S->tempty[a], 4);
-    }
+    mbar_init(&S->tfull[0], 1);       // one accumulator: the [0] barriers only
+    mbar_init(&S->tempty[0], 8);
     mbar_init(&S->drain, 1);
     S->abort_flag = 0;
     fence_mbar_init();
@@ -192,7 +207,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    const uint32_t bytes = NV_A_STAGE + NV_B_STAGE + 2 * NV_SF_STAGE;
+    const uint32_t bytes = NV_A_STAGE + NV_B_STAGE + NV_SFA_STAGE + NV_SFB_STAGE;
     int stage = 0;
     uint32_t phase = 0;
     int last_phase[NV_STAGES];
@@ -202,6 +217,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       const TileCoord tc = gemm_tile(P, S, t);
       const uint8_t* sfa = P.sf_a + (static_cast<size_t>(tc.a_row >> 7) * kchunks) * 512;
       const uint8_t* sfb = P.sf_b + (static_cast<size_t>(tc.b_row >> 7) * kchunks) * 512;
+      const uint8_t* sfb1 = sfb + static_cast<size_t>(kchunks) * 512;   // rows 128-255
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!mbar_wait_bounded(&N->empty[stage], phase ^ 1, abort_flag, P.status,
                                WAIT_PRODUCER_EMPTY, limit))
@@ -209,8 +225,10 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         mbar_arrive_expect_tx(&N->full[stage], bytes);
         tma_load_2d(sA + stage * NV_A_STAGE, &tmA, &N->full[stage], kb * 128, tc.a_row);
         tma_load_2d(sB + stage * NV_B_STAGE, &tmB, &N->full[stage], kb * 128, tc.b_row);
-        bulk_load(sSA + stage * NV_SF_STAGE, sfa + kb * NV_SF_STAGE, NV_SF_STAGE, &N->full[stage]);
-        bulk_load(sSB + stage * NV_SF_STAGE, sfb + kb * NV_SF_STAGE, NV_SF_STAGE, &N->full[stage]);
+        bulk_load(sSA + stage * NV_SFA_STAGE, sfa + kb * NV_SFA_STAGE, NV_SFA_STAGE,
+                  &N->full[stage]);
+        bulk_load(sSB + stage * NV_SFB_STAGE, sfb + kb * 2048, 2048, &N->full[stage]);
+        bulk_load(sSB + stage * NV_SFB_STAGE + 2048, sfb1 + kb * 2048, 2048, &N->full[stage]);
         last_phase[stage] = static_cast<int>(phase);
         if (++stage == NV_STAGES) { stage = 0; phase ^= 1; }
       }
@@ -230,13 +248,11 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     uint32_t phase = 0;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait_bounded(&S->tempty[acc], acc_phase ^ 1, abort_flag, P.status,
+      if (!mbar_wait_bounded(&S->tempty[0], (it & 1) ^ 1, abort_flag, P.status,
                              WAIT_MMA_TMEM_EMPTY, limit))
         break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * NV_BN;
+      const uint32_t d_tmem = tmem_base;
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb) {
         if (!mbar_wait_bounded(&N->full[stage], phase, abort_flag, P.status, WAIT_MMA_FULL,
@@ -256,20 +272,20 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           mma_issue_nvf4(d_tmem, sdesc_sw128(a0 + 32 * j), sdesc_sw128(b0 + 32 * j), idesc,
-                         sf_col + 4 * j, sf_col + 16 + 4 * j, (kb | j) != 0);
+                         sf_col + 4 * j, sf_col + 16 + 8 * j, (kb | j) != 0);
         }
         mma_commit(&N->empty[stage]);
         if (++stage == NV_STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      mma_commit(&S->tfull[acc]);
+      mma_commit(&S->tfull[0]);
     }
     mma_commit(&S->drain);
     {
       volatile int never = 0;
       mbar_wait_bounded(&S->drain, 0, &never, P.status, WAIT_DRAIN, limit);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ---------------- scale warps: stage scales -> TMEM (quadrant warp % 4) ----------
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     int stage = 0;
@@ -282,18 +298,29 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
           ok = false;
           break;
         }
-        // lane l: row l of each 512-byte chunk (16 bytes = 4 columns), chunk j -> 4j..
-        uint32_t va[16], vb[16];
+        // lane l: row l of each 512-byte chunk (16 bytes = 4 columns).  A: chunk j ->
+        // columns 4j..; B (N = 256): K step j takes 8 columns, rows 0-127 (chunk j of the
+        // first half) then rows 128-255 (chunk j of the second half)
+        uint32_t va[16], vb0[16], vb1[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          const uint4 a = *reinterpret_cast<const uint4*>(sSA + stage * NV_SF_STAGE + 512 * j + 16 * lane);
-          const uint4 b = *reinterpret_cast<const uint4*>(sSB + stage * NV_SF_STAGE + 512 * j + 16 * lane);
+          const uint4 a = *reinterpret_cast<const uint4*>(sSA + stage * NV_SFA_STAGE + 512 * j + 16 * lane);
           va[4 * j] = a.x; va[4 * j + 1] = a.y; va[4 * j + 2] = a.z; va[4 * j + 3] = a.w;
-          vb[4 * j] = b.x; vb[4 * j + 1] = b.y; vb[4 * j + 2] = b.z; vb[4 * j + 3] = b.w;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint8_t* sb = sSB + stage * NV_SFB_STAGE;
+          const uint4 b0 = *reinterpret_cast<const uint4*>(sb + 512 * j + 16 * lane);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(sb + 2048 + 512 * j + 16 * lane);
+          uint32_t* v = j < 2 ? vb0 : vb1;
+          const int o = 8 * (j & 1);
+          v[o] = b0.x; v[o + 1] = b0.y; v[o + 2] = b0.z; v[o + 3] = b0.w;
+          v[o + 4] = b1.x; v[o + 5] = b1.y; v[o + 6] = b1.z; v[o + 7] = b1.w;
         }
         const uint32_t sf_col = tmem_base + NV_SF_COL0 + stage * NV_SF_COLS + lane_base;
         tmem_st16(sf_col, va);
-        tmem_st16(sf_col + 16, vb);
+        tmem_st16(sf_col + 16, vb0);
+        tmem_st16(sf_col + 32, vb1);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -303,23 +330,22 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       if (!ok) break;
     }
   } else if (warp >= 4) {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue: warps 4-7 columns 0-127, 12-15 columns 128-255 -------
     const int q = warp & 3;
+    const int hh = warp >= 12 ? 1 : 0;
     const int r = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait_bounded(&S->tfull[acc], acc_phase, abort_flag, P.status,
-                             WAIT_EPI_TMEM_FULL, limit))
+      if (!mbar_wait_bounded(&S->tfull[0], it & 1, abort_flag, P.status, WAIT_EPI_TMEM_FULL,
+                             limit))
         break;
       tc_fence_after();
       const TileCoord tc = gemm_tile(P, S, t);
-      const uint32_t taddr = tmem_base + acc * NV_BN + (static_cast<uint32_t>(q * 32) << 16);
-      nvf4_epilogue<EPI>(P, tc, taddr, r, N->recip, &tmY, sY + q * NV_Y_BOX);
+      const uint32_t taddr = tmem_base + hh * 128 + (static_cast<uint32_t>(q * 32) << 16);
+      nvf4_epilogue<EPI>(P, tc, taddr, r, hh, N->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S->tempty[acc]);
+      if (lane == 0) mbar_arrive(&S->tempty[0]);
     }
     if (EPI == NV_EPI_STORE_F32 && lane == 0) tma_store_wait_all();   // y fully written
   }

@@ -791,7 +791,7 @@ moe_status_t moe_quantize_nvfp4(const moe_config_t* cfg, const void* w_gate, con
   MOE_TRY(last_launch());
   quantize_weight_kernel<<<static_cast<unsigned>(E * 2 * I), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(w_gate), static_cast<const __nv_bfloat16*>(w_up),
-      w13_out, sf13_out, gs13_out, static_cast<int>(2 * I), c.p, NV_BN / 2);
+      w13_out, sf13_out, gs13_out, static_cast<int>(2 * I), c.p, NV_W13_GROUP);
   MOE_TRY(last_launch());
   quantize_weight_kernel<<<static_cast<unsigned>(E * p), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(w_down), nullptr, w2_out, sf2_out, gs2_out, c.p, c.I, 0);
