@@ -408,15 +408,15 @@ __global__ void __launch_bounds__(MEM_THREADS)
 // "vLLM 对 Muse Spark Open 的 Day 0 支持", section "三明治归一化": the block sits between
 // two norms, x + post_norm(F(norm(x))); "SGLang and Miles Add Day-0 Support for Muse Spark
 // Open", section "Kernel Optimizations": the post-FFN norm, the gated residual add and
-// the pre-attention norm run as one kernel that keeps each row in registers across both
-// RMS reductions, and a cluster of CTAs shares one row through distributed shared memory
+// the pre-attention norm run as one kernel that keeps each row on chip across both
+// RMS reductions (here in shared memory), and a cluster of CTAs shares one row through distributed shared memory
 // when rows alone do not fill the GPU.
 //
 //   a = RMSNorm_{g_post}(y);  x' = x + gate * a (gate per channel, or 1);  stored as the
 //   residual stream's type;  h' = RMSNorm_{g_next}(x' as stored)
 //
-// C CTAs (one cluster) share a row: CTA r holds columns [r d/C, (r+1) d/C), at most
-// BND_MAXV values per thread.  Both sums of squares go thread -> warp -> CTA (fixed
+// C CTAs (one cluster) share a row: CTA r holds columns [r d/C, (r+1) d/C) (at most
+// BND_MAXV * MEM_THREADS) in shared memory.  Both sums of squares go thread -> warp -> CTA (fixed
 // order) -> cluster (partials of ranks 0..C-1 added in rank order by every CTA), so all
 // CTAs of a row use the same bits.
 constexpr int BND_MAXV = 32;   // values per thread: d / C <= 8192
@@ -437,12 +437,40 @@ __device__ __forceinline__ float cluster_row_sum(float v, float* red, float* par
   return total;
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// 8 consecutive values of a BF16 or FP32 array in shared memory
+__device__ __forceinline__ void smem_load8(const uint8_t* base, int idx, int is_f32,
+                                           float (&v)[8]) {
+  if (is_f32) {
+    const float4 a = reinterpret_cast<const float4*>(base)[2 * idx];
+    const float4 b = reinterpret_cast<const float4*>(base)[2 * idx + 1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 a = reinterpret_cast<const uint4*>(base)[idx];
+    float2 f;
+    f = unpack_bf16x2(a.x); v[0] = f.x; v[1] = f.y;
+    f = unpack_bf16x2(a.y); v[2] = f.x; v[3] = f.y;
+    f = unpack_bf16x2(a.z); v[4] = f.x; v[5] = f.y;
+    f = unpack_bf16x2(a.w); v[6] = f.x; v[7] = f.y;
+  }
+}
+
+// Shared memory of one CTA of the boundary kernel: its x and y slices.
+inline size_t boundary_smem_bytes(int cols, int x_f32, int y_f32) {
+  return size_t(cols) * ((x_f32 ? 4 : 2) + (y_f32 ? 4 : 2));
+}
+
 template <int C>
 __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(MEM_THREADS)
     boundary_kernel(const void* __restrict__ x, const void* __restrict__ y,
                     const float* __restrict__ g_post, const float* __restrict__ gate,
                     const float* __restrict__ g_next, void* x_out, void* __restrict__ h_next,
                     int d, float eps, int x_f32, int y_f32) {
+  extern __shared__ __align__(16) uint8_t bnd_smem[];
   __shared__ float red[32];
   __shared__ float part[2];
   const int rank = C == 1 ? 0 : static_cast<int>(blockIdx.x % C);
@@ -450,108 +478,92 @@ __global__ void __cluster_dims__(C, 1, 1) __launch_bounds__(MEM_THREADS)
   const int cols = d / C;
   const int c0 = rank * cols;
   const int nchunk = cols >> 3;       // 8 values per chunk
-  constexpr int MAXCH = BND_MAXV / 8;
-  float v[MAXCH][8];
-  // 1. block output y and its sum of squares
+  const int xe = x_f32 ? 4 : 2, ye = y_f32 ? 4 : 2;
+  uint8_t* sy = bnd_smem;
+  uint8_t* sx = bnd_smem + size_t(cols) * ye;
+  // the CTA's slices of y and x, fetched with asynchronous 16-byte copies (many in flight,
+  // few registers), then the row stays on chip across both reductions
+  {
+    const uint8_t* gy = static_cast<const uint8_t*>(y) + (t * d + c0) * ye;
+    const uint8_t* gx = static_cast<const uint8_t*>(x) + (t * d + c0) * xe;
+    const int ny = cols * ye / 16, nx = cols * xe / 16;
+    for (int i = threadIdx.x; i < ny; i += blockDim.x) cp_async16(sy + 16 * i, gy + 16 * i);
+    for (int i = threadIdx.x; i < nx; i += blockDim.x) cp_async16(sx + 16 * i, gx + 16 * i);
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+  }
+  // 1. sum of squares of the block output
   float ss = 0.f;
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    float v[8];
+    smem_load8(sy, c, y_f32, v);
 #pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const int c = threadIdx.x + i * MEM_THREADS;
-    if (c < nchunk) {
-      const size_t off = t * d + c0 + 8 * c;
-      if (y_f32) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(y) + off);
-        const float4 a = src[0], b = src[1];
-        v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
-        v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
-      } else {
-        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + off);
-        float2 f;
-        f = unpack_bf16x2(a.x); v[i][0] = f.x; v[i][1] = f.y;
-        f = unpack_bf16x2(a.y); v[i][2] = f.x; v[i][3] = f.y;
-        f = unpack_bf16x2(a.z); v[i][4] = f.x; v[i][5] = f.y;
-        f = unpack_bf16x2(a.w); v[i][6] = f.x; v[i][7] = f.y;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ss = fmaf(v[i][j], v[i][j], ss);
-    }
+    for (int j = 0; j < 8; ++j) ss = fmaf(v[j], v[j], ss);
   }
   const float rs_y = rsqrtf(cluster_row_sum(ss, red, &part[0], C) / static_cast<float>(d) + eps);
-  // 2. residual add, rounded to the stream's type, kept in registers
+  // 2. residual add, rounded to the stream's type: written out and kept on chip
   float ss2 = 0.f;
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    const int col = c0 + 8 * c;
+    float v[8], xv[8];
+    smem_load8(sy, c, y_f32, v);
+    smem_load8(sx, c, x_f32, xv);
+    const float4 p0 = reinterpret_cast<const float4*>(g_post + col)[0];
+    const float4 p1 = reinterpret_cast<const float4*>(g_post + col)[1];
+    const float gp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+    float gt[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+    if (gate) {
+      const float4 q0 = reinterpret_cast<const float4*>(gate + col)[0];
+      const float4 q1 = reinterpret_cast<const float4*>(gate + col)[1];
+      gt[0] = q0.x; gt[1] = q0.y; gt[2] = q0.z; gt[3] = q0.w;
+      gt[4] = q1.x; gt[5] = q1.y; gt[6] = q1.z; gt[7] = q1.w;
+    }
+    float r[8];
 #pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const int c = threadIdx.x + i * MEM_THREADS;
-    if (c < nchunk) {
-      const int col = c0 + 8 * c;
-      const size_t off = t * d + col;
-      float xv[8];
-      if (x_f32) {
-        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(x) + off);
-        const float4 a = src[0], b = src[1];
-        xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w; xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
-      } else {
-        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + off);
-        float2 f;
-        f = unpack_bf16x2(a.x); xv[0] = f.x; xv[1] = f.y;
-        f = unpack_bf16x2(a.y); xv[2] = f.x; xv[3] = f.y;
-        f = unpack_bf16x2(a.z); xv[4] = f.x; xv[5] = f.y;
-        f = unpack_bf16x2(a.w); xv[6] = f.x; xv[7] = f.y;
-      }
-      const float4 p0 = reinterpret_cast<const float4*>(g_post + col)[0];
-      const float4 p1 = reinterpret_cast<const float4*>(g_post + col)[1];
-      const float gp[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-      float gt[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-      if (gate) {
-        const float4 q0 = reinterpret_cast<const float4*>(gate + col)[0];
-        const float4 q1 = reinterpret_cast<const float4*>(gate + col)[1];
-        gt[0] = q0.x; gt[1] = q0.y; gt[2] = q0.z; gt[3] = q0.w;
-        gt[4] = q1.x; gt[5] = q1.y; gt[6] = q1.z; gt[7] = q1.w;
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float a = v[i][j] * rs_y * gp[j];
-        float r = xv[j] + gt[j] * a;
-        if (!x_f32) r = __bfloat162float(__float2bfloat16_rn(r));
-        v[i][j] = r;
-        ss2 = fmaf(r, r, ss2);
-      }
-      if (x_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(x_out) + off);
-        dst[0] = make_float4(v[i][0], v[i][1], v[i][2], v[i][3]);
-        dst[1] = make_float4(v[i][4], v[i][5], v[i][6], v[i][7]);
-      } else {
-        uint4 o;
-        o.x = pack_bf16x2(v[i][0], v[i][1]); o.y = pack_bf16x2(v[i][2], v[i][3]);
-        o.z = pack_bf16x2(v[i][4], v[i][5]); o.w = pack_bf16x2(v[i][6], v[i][7]);
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(x_out) + off) = o;
-      }
+    for (int j = 0; j < 8; ++j) {
+      r[j] = xv[j] + gt[j] * (v[j] * rs_y * gp[j]);
+      if (!x_f32) r[j] = __bfloat162float(__float2bfloat16_rn(r[j]));
+      ss2 = fmaf(r[j], r[j], ss2);
+    }
+    const size_t off = t * d + col;
+    if (x_f32) {
+      const float4 o0 = make_float4(r[0], r[1], r[2], r[3]), o1 = make_float4(r[4], r[5], r[6], r[7]);
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(x_out) + off);
+      dst[0] = o0;
+      dst[1] = o1;
+      reinterpret_cast<float4*>(sx)[2 * c] = o0;
+      reinterpret_cast<float4*>(sx)[2 * c + 1] = o1;
+    } else {
+      uint4 o;
+      o.x = pack_bf16x2(r[0], r[1]); o.y = pack_bf16x2(r[2], r[3]);
+      o.z = pack_bf16x2(r[4], r[5]); o.w = pack_bf16x2(r[6], r[7]);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(x_out) + off) = o;
+      reinterpret_cast<uint4*>(sx)[c] = o;
     }
   }
-  // 3. the next block's pre-norm on the stored residual
+  // 3. the next block's pre-norm on the stored residual (each thread rereads its own
+  // chunks, so no barrier is needed between the write above and the read below)
   const float rs_x = rsqrtf(cluster_row_sum(ss2, red, &part[1], C) / static_cast<float>(d) + eps);
+  for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
+    const int col = c0 + 8 * c;
+    float v[8];
+    smem_load8(sx, c, x_f32, v);
+    const float4 n0 = reinterpret_cast<const float4*>(g_next + col)[0];
+    const float4 n1 = reinterpret_cast<const float4*>(g_next + col)[1];
+    const float gn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+    float o[8];
 #pragma unroll
-  for (int i = 0; i < MAXCH; ++i) {
-    const int c = threadIdx.x + i * MEM_THREADS;
-    if (c < nchunk) {
-      const int col = c0 + 8 * c;
-      const size_t off = t * d + col;
-      const float4 n0 = reinterpret_cast<const float4*>(g_next + col)[0];
-      const float4 n1 = reinterpret_cast<const float4*>(g_next + col)[1];
-      const float gn[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-      float o[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] = v[i][j] * rs_x * gn[j];
-      if (x_f32) {
-        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(h_next) + off);
-        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
-      } else {
-        uint4 q;
-        q.x = pack_bf16x2(o[0], o[1]); q.y = pack_bf16x2(o[2], o[3]);
-        q.z = pack_bf16x2(o[4], o[5]); q.w = pack_bf16x2(o[6], o[7]);
-        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(h_next) + off) = q;
-      }
+    for (int j = 0; j < 8; ++j) o[j] = v[j] * rs_x * gn[j];
+    const size_t off = t * d + col;
+    if (x_f32) {
+      float4* dst = reinterpret_cast<float4*>(static_cast<float*>(h_next) + off);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+    } else {
+      uint4 q;
+      q.x = pack_bf16x2(o[0], o[1]); q.y = pack_bf16x2(o[2], o[3]);
+      q.z = pack_bf16x2(o[4], o[5]); q.w = pack_bf16x2(o[6], o[7]);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(h_next) + off) = q;
     }
   }
   // no CTA of the cluster leaves while another may still read its partials

@@ -140,6 +140,16 @@ moe_status_t device_ready(int* sms) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_ROUTER>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    // boundary kernel: x and y slices of up to BND_MAXV * MEM_THREADS FP32 columns each
+    const int bnd_smem = static_cast<int>(boundary_smem_bytes(BND_MAXV * MEM_THREADS, 1, 1));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(boundary_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, bnd_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(boundary_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, bnd_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(boundary_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, bnd_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(boundary_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, bnd_smem);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     D.ready = true;
   }
@@ -871,23 +881,22 @@ moe_status_t moe_boundary(const moe_config_t* cfg, const void* x, const void* y,
       overlap(h_next, bx, x, bx) || overlap(h_next, bx, y, by) ||
       overlap(h_next, bx, x_out, bx))
     return MOE_ERR_INVALID_ARG;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  // CTAs per row: enough that every thread holds at most BND_MAXV values, and more (up
-  // to a cluster of 8) while the rows alone would leave SMs idle
+  int sms = 0;
+  MOE_TRY(device_ready(&sms));
+  // CTAs per row: enough that a CTA holds at most BND_MAXV * MEM_THREADS columns, and
+  // more (up to a cluster of 8) while the rows alone would leave SMs idle
   int C = 1;
   while (C < 8 && (c.d / C > BND_MAXV * MEM_THREADS || static_cast<long long>(c.T) * C < 2 * sms))
     C *= 2;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int xf = c.act == MOE_F32, yf = c.out == MOE_F32;
   const unsigned grid = static_cast<unsigned>(c.T) * C;
+  const size_t smem = boundary_smem_bytes(c.d / C, xf, yf);
   switch (C) {
-    case 1: boundary_kernel<1><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-    case 2: boundary_kernel<2><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-    case 4: boundary_kernel<4><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-    default: boundary_kernel<8><<<grid, MEM_THREADS, 0, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 1: boundary_kernel<1><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 2: boundary_kernel<2><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 4: boundary_kernel<4><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    default: boundary_kernel<8><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
   }
   return last_launch();
 }
