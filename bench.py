@@ -74,17 +74,42 @@ def bytes_per_token(s, act_bytes=2) -> dict:
     """Compulsory HBM bytes per token of the memory-bound stages (each operand read
     once, each result written once)."""
     k = s.top_k
+    yb = 4 if s.expert == "f32" else 2          # expert outputs y: BF16 unless FP32 experts
     return {
         "norm": s.d * act_bytes + s.d * 4 + s.d * act_bytes,            # x in; h32, h16 out
         "dispatch": s.p * 4 + k * s.p * act_bytes + 16 * k,             # pooled in; k rows out
-        "combine": k * s.p * 4 + s.p * act_bytes + 8 * k,               # k FP32 rows in; c out
+        "combine": k * s.p * yb + k * (s.p // 128) * 4 + s.p * act_bytes + 8 * k,  # y, sums in; c out
+    }
+
+
+def expert_gemm_bytes(s, n_experts_touched: int, T: int) -> dict:
+    """Compulsory HBM bytes of one launch of each expert GEMM: the weights of the experts
+    the batch routes to (read once), the R = T * top_k dispatched rows in and the rows
+    out.  BF16 experts: FP16 W13 and u, BF16 W2 and s; FP32 experts: FP32 throughout.
+    NVFP4 experts: 4-bit codes plus
+    one FP8 scale per 16 elements for the weights, u and s.  The down GEMM writes y (BF16;
+    FP32 for FP32 experts) and one FP32 sum of squares per 128 columns."""
+    R = T * s.top_k
+    if s.expert == "nvfp4":
+        q = 0.5 + 1.0 / 16
+        w13, w2, u, s_in, s_out = q, q, q, q, q
+    elif s.expert == "f32":     # TF32-rounded FP32 weights and operands
+        w13, w2, u, s_in, s_out = 4, 4, 4, 4, 4
+    else:
+        w13, w2, u, s_in, s_out = 2, 2, 2, 2, 2
+    yb = 4 if s.expert == "f32" else 2
+    return {
+        "gemm1_gate_up_swiglu": n_experts_touched * s.p * 2 * s.I * w13 + R * s.p * u
+                                + R * s.I * s_out,
+        "gemm2_down": n_experts_touched * s.I * s.p * w2 + R * s.I * s_in + R * s.p * yb
+                      + R * (s.p // 128) * 4,
     }
 
 
 # ---- clocks --------------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi sampling (200 ms) of SM clock and throttle reasons while running."""
+    """nvidia-smi sampling (100 ms) of SM clock and throttle reasons while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -96,7 +121,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -110,7 +135,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], None, set()
+        sm, pw, smax, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -121,13 +146,22 @@ class ClockSampler:
                 smax = float(f[2])
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pw.append(float("nan"))
             for name, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(name)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "samples": len(sm),
-                "reasons": sorted(reasons)}
+        # under load = the samples drawing at least half the highest power seen (the
+        # idle lead-in before the timed region is left out of the median)
+        top = max((w for w in pw if w == w), default=None)
+        load = [c for c, w in zip(sm, pw) if top is None or (w == w and w >= 0.5 * top)]
+        return {"sm_mhz": statistics.median(load or sm), "sm_max_mhz": smax,
+                "samples": len(sm), "load_samples": len(load),
+                "power_w_max": top, "reasons": sorted(reasons)}
 
 
 # ---- ncu traffic record ----------------------------------------------------------------
@@ -216,6 +250,9 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         layer.forward(x, out=out)
+    ids_probe, _ = layer.route(x)       # experts this batch touches (for the byte count)
+    n_touched = int(torch.unique(ids_probe).numel())
+    del ids_probe
     torch.cuda.synchronize()
     st = layer.read_status()
     if st != (0, 0):
@@ -238,7 +275,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), "cuda")
     st = layer.read_status()
     if st != (0, 0):
@@ -254,32 +290,73 @@ def run_ours(args):
     value = tokens / (elapsed_ms / 1e3)
 
     # ---- end to end from pinned host buffers ------------------------------------------
+    # Every step copies its tokens host -> device, runs the layer and copies its output
+    # back.  Two device slots let the copies of neighbouring steps run on their own
+    # streams (one per direction) under the current step's kernels; events order each
+    # slot's copy-in -> forward -> copy-out, and the timed region spans the first
+    # copy-in to the last copy-out.
     e2e = None
     if not args.no_e2e:
         hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
         hx.copy_(x)
-        ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        dx = torch.empty_like(x)
-        for _ in range(2):
-            dx.copy_(hx, non_blocking=True)
-            layer.forward(dx, out=out)
-            ho.copy_(out, non_blocking=True)
+        ho = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
+        dx = [torch.empty_like(x) for _ in range(2)]
+        dout = [torch.empty_like(out) for _ in range(2)]
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def pipelined(n, start_event=None):
+            fwd_done = [None, None]
+            out_done = [None, None]
+            if start_event is not None:
+                h2d.wait_event(start_event)
+            for i in range(n):
+                j = i & 1
+                if fwd_done[j] is not None:
+                    h2d.wait_event(fwd_done[j])     # slot j's previous forward has read dx[j]
+                with torch.cuda.stream(h2d):
+                    dx[j].copy_(hx, non_blocking=True)
+                    in_done = torch.cuda.Event()
+                    in_done.record(h2d)
+                stream.wait_event(in_done)
+                if out_done[j] is not None:
+                    stream.wait_event(out_done[j])  # slot j's previous output has left
+                layer.forward(dx[j], out=dout[j])
+                fwd_done[j] = torch.cuda.Event()
+                fwd_done[j].record(stream)
+                d2h.wait_event(fwd_done[j])
+                with torch.cuda.stream(d2h):
+                    ho[j].copy_(dout[j], non_blocking=True)
+                    out_done[j] = torch.cuda.Event()
+                    out_done[j].record(d2h)
+            for ev in out_done:
+                if ev is not None:
+                    stream.wait_event(ev)
+
+        pipelined(3)
         torch.cuda.synchronize()
+        if layer.read_status() != (0, 0):
+            raise SystemExit(f"device status after the end-to-end warm-up: {layer.read_status()}")
+        if not torch.equal(ho[0].to(out.device), out) or not torch.equal(ho[1].to(out.device), out):
+            raise SystemExit("end-to-end output differs from the device-resident run")
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        n_e2e = max(3, args.steps // 2)
+        n_e2e = max(4, args.steps // 2)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(n_e2e):
-            dx.copy_(hx, non_blocking=True)
-            layer.forward(dx, out=out)
-            ho.copy_(out, non_blocking=True)
+        pipelined(n_e2e, start_event=e0)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), "cuda")
         e2e = {"value": T * n_e2e * world / (e2e_ms / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": x.numel() * x.element_size(),
                "d2h_bytes_per_step": out.numel() * out.element_size(),
-               "ms_per_step": e2e_ms / n_e2e}
+               "ms_per_step": e2e_ms / n_e2e,
+               "copies": "pinned host buffers; copy-in and copy-out on their own streams, "
+                         "overlapping the neighbouring steps' kernels (two device slots)"}
+
+    clocks = sampler.stop()           # samples cover both timed regions
 
     # ---- the block boundary (post-norm, residual add, next pre-norm), timed on its own ----
     boundary = None
@@ -317,10 +394,14 @@ def run_ours(args):
     by = bytes_per_token(shape)
     stage_tflops = {n: fl[n] * T / (stage_ms[n] / 1e3) / 1e12 for n in fl if stage_ms.get(n)}
     stage_gbs = {n: by[n] * T / (stage_ms[n] / 1e3) / 1e9 for n in by if stage_ms.get(n)}
+    gb = expert_gemm_bytes(shape, n_touched, T)
+    for n, b in gb.items():
+        if stage_ms.get(n):
+            stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9
     dominant = max(fl, key=lambda n: stage_ms.get(n, 0.0))
-    achieved = stage_tflops[dominant]
     bf16_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     bf16_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     traffic = recorded_traffic(args.workload, dominant)
     if shape.expert == "nvfp4" and dominant.startswith("gemm"):
         # a contraction takes the peak of its own dtype: dense FP4 = 6 x dense BF16
@@ -332,10 +413,29 @@ def run_ours(args):
         peak = bf16_peak
         kind = (f"bf16_tflops_sustained ({peak_src}); the kernel runs inside a "
                 f"{ms_per_step:.1f} ms step, back to back")
-    roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
-                "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "peak_kind": kind, "flops_per_launch": fl[dominant] * T,
-                "peak_burst_bf16": bf16_burst}
+    flops_launch = fl[dominant] * T
+    bytes_launch = gb.get(dominant)
+    ridge = peak * 1e12 / (hbm_peak * 1e9)          # FLOP per byte where the two bounds meet
+    intensity = flops_launch / bytes_launch if bytes_launch else None
+    if intensity is not None and intensity < ridge:
+        # too few rows per expert to reuse a weight tile: the launch streams the weights
+        achieved = stage_gbs[dominant]
+        roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
+                    "peak": round(hbm_peak, 1), "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                    "peak_kind": f"hbm_gbs ({peak_src}, copy bandwidth)",
+                    "bytes_per_launch": bytes_launch, "flops_per_launch": flops_launch,
+                    "experts_touched": n_touched,
+                    "intensity_flop_per_byte": round(intensity, 2), "ridge": round(ridge, 1),
+                    "tensor_tflops": round(stage_tflops[dominant], 1)}
+    else:
+        achieved = stage_tflops[dominant]
+        roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
+                    "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": traffic, "peak_kind": kind, "flops_per_launch": flops_launch,
+                    "bytes_per_launch": bytes_launch, "experts_touched": n_touched,
+                    "intensity_flop_per_byte": round(intensity, 1) if intensity else None,
+                    "ridge": round(ridge, 1), "peak_burst_bf16": bf16_burst}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -359,7 +459,7 @@ def run_ours(args):
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "stages_tflops": {k: round(v, 1) for k, v in stage_tflops.items()},
         "stages_gbs": {k: round(v, 1) for k, v in stage_gbs.items()},
-        "hbm_peak_gbs": float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])),
+        "hbm_peak_gbs": hbm_peak,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
     if boundary is not None:

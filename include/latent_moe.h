@@ -280,11 +280,12 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally);
  *   0 h32 [T,d] FP32 (TF32-rounded)   1 h16 [T,d] FP16     2 ids [T,k] int32
  *   3 w [T,k] FP32                    4 pooled [T,p] FP32   5 row_off [E+1] int32
  *   6 src [T*k] int32 (dispatched row -> t*k+j)              7 inv [T*k] int32
- *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (BF16 / FP32)   10 y [T*k,p] FP32
+ *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (BF16 / FP32)
+ *  10 y [T*k,p] (BF16 / FP32: FP32 for FP32 experts only)
  *  11 c [T,p] (FP16 / FP32)
  * NVFP4 configs: dispatched rows start at a 128-row boundary per expert (R rows in all,
  * R = 128 * (ceil(T*k/128) + E)); 8 A_perm [R, p/2] E2M1 codes, 9 s [R, I/2] codes,
- * 10 y [R, p] FP32, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
+ * 10 y [R, p] BF16, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
  * FP32 per-row scales.  All configs: 15 row_cnt [E+1] int32 rows per expert.
  * Writes min(n, 16) offsets and returns how many it wrote (0 for an invalid config). */
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n);

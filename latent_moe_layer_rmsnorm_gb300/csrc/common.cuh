@@ -307,6 +307,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// The value an output row holds once stored: BF16 rounds to nearest even, FP32 keeps it.
+// Epilogues square this value, so a row's sums of squares describe the stored row.
+__device__ __forceinline__ float stored_value(float v, bool bf16) {
+  return bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

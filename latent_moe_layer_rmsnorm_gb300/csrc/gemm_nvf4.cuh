@@ -8,7 +8,7 @@
 //   gate/up  u [rows, p] x W13_e [2I, p] (gate/up rows interleaved in blocks of 64)
 //            epilogue: a, b = acc * alpha[row] * beta13[e]; s = silu(a) * b; s -> NVFP4
 //            with the static global scale gamma[e] (codes + chunked scales)
-//   down     s [rows, I] x W2_e [p, I]; epilogue y = acc * gamma[e] * beta2[e] (FP32)
+//   down     s [rows, I] x W2_e [p, I]; epilogue y = acc * gamma[e] * beta2[e] (BF16)
 //
 // Same pipeline as gemm_tcgen05.cuh (TMA producer warp, one MMA-issuing thread, four
 // epilogue warps, double-buffered TMEM accumulators, bounded waits), with per-stage
@@ -49,7 +49,7 @@ constexpr int NV_THREADS = 512;
 // writes and include/latent_moe.h documents)
 constexpr int NV_W13_GROUP = 64;
 
-enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_F32 = 1 };
+enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_BF16 = 1 };
 
 struct NvSmem {
   GemmSmem g;                // barriers and schedule (its `full`/`empty` sized for GEMM_STAGES)
@@ -60,11 +60,11 @@ struct NvSmem {
 };
 
 // The down GEMM's epilogue writes y through shared memory: each epilogue warp stages a
-// 32-row x 32-column FP32 box (4 KB, 128-byte swizzle) and stores it with TMA, instead of
+// 32-row x 64-column BF16 box (4 KB, 128-byte swizzle) and stores it with TMA, instead of
 // 32 rows of 16-byte pieces per store instruction (those stores cost about a third of
 // the kernel's time, measured).  Expert rows are padded to 128 per expert, so a box never
 // reaches another expert's rows; rows past an expert's last token are padding.
-constexpr int NV_Y_BOX = 32 * 32 * 4;
+constexpr int NV_Y_BOX = 32 * 128;
 
 constexpr size_t nvf4_smem_bytes() {
   return 1024 + size_t(NV_STAGES) * (NV_A_STAGE + NV_B_STAGE + NV_SFA_STAGE + NV_SFB_STAGE) +
@@ -129,24 +129,31 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
         va[i] = __uint_as_float(a[i]) * sc;
         vb[i] = __uint_as_float(b[i]) * sc;
       }
-      // this warp's 32 rows x 32 columns through the staging box: row `lane`, 16-byte
-      // chunk j at chunk (j ^ lane % 8) (the 128-byte swizzle of the tensor map)
-      if (lane == 0) tma_store_wait_read();
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float* v = j < 4 ? va + 4 * j : vb + 4 * (j - 4);
-        *reinterpret_cast<float4*>(ybox + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-            make_float4(v[0], v[1], v[2], v[3]);
+      // this warp's 32 rows x 64 BF16 columns fill one staging box over two passes (the
+      // first pass chunks 0-3 of each 128-byte row, the second chunks 4-7): row `lane`,
+      // 16-byte chunk j at chunk (j ^ lane % 8) (the 128-byte swizzle of the tensor map)
+      const int half = (c0 >> 5) & 1;
+      if (half == 0) {
+        if (lane == 0) tma_store_wait_read();
+        __syncwarp();
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0)
-        tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0, tc.a_row + (r - lane));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+      for (int j = 0; j < 4; ++j) {
+        const float* v = j < 2 ? va + 8 * j : vb + 8 * (j - 2);
+        const uint4 o = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+        *reinterpret_cast<uint4*>(ybox + lane * 128 + (((4 * half + j) ^ (lane & 7)) << 4)) = o;
+      }
+      if (half == 1) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0 - 32, tc.a_row + (r - lane));
+      }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
+      for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], true); ss = fmaf(q, q, ss); }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], true); ss = fmaf(q, q, ss); }
     }
     if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + 2 * tc.n_blk + hh] = ss;
   }
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S->tempty[0]);
     }
-    if (EPI == NV_EPI_STORE_F32 && lane == 0) tma_store_wait_all();   // y fully written
+    if (EPI == NV_EPI_STORE_BF16 && lane == 0) tma_store_wait_all();   // y fully written
   }
 
   tc_fence_before();

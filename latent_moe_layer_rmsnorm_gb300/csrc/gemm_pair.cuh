@@ -195,10 +195,11 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
         store16(P.out, base + c0, P.out_fmt, va);
         store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
+      const bool rb = P.out_fmt == OUT_BF16;       // squared as stored
 #pragma unroll
-      for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+      for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
+      for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], rb); ss = fmaf(q, q, ss); }
     }
     // same column order as the full-tile epilogue, so the block sums agree bit for bit
     if (P.row_ssq && row_ok)
@@ -271,11 +272,12 @@ __device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const T
       for (int i = 0; i < 16; ++i) { va[i] = __uint_as_float(a[i]); vb[i] = __uint_as_float(b[i]); }
       put(col_base + c0, va, col_base);
       put(col_base + c0 + 16, vb, col_base);
-      if (P.row_ssq) {
+      if (P.row_ssq) {                                // squared as stored
+        const bool rb = P.out_fmt == OUT_BF16;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+        for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
+        for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], rb); ss = fmaf(q, q, ss); }
         if (((c0 + 32) & 127) == 0) {
           P.row_ssq[row * (P.N >> 7) + ((col_base + c0) >> 7)] = ss;
           ss = 0.f;

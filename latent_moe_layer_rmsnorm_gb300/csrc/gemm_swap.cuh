@@ -100,7 +100,10 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& P, const SwapTil
       for (int jj = 0; jj < 16; ++jj) {
         if (c0 + jj < tc.valid) {
           const size_t idx = static_cast<size_t>(tc.tok_row + c0 + jj) * P.ld_out + f;
-          reinterpret_cast<float*>(P.out)[idx] = __uint_as_float(v[jj]);
+          if (P.out_fmt == OUT_BF16)
+            reinterpret_cast<__nv_bfloat16*>(P.out)[idx] = __float2bfloat16_rn(__uint_as_float(v[jj]));
+          else
+            reinterpret_cast<float*>(P.out)[idx] = __uint_as_float(v[jj]);
         }
       }
     }

@@ -209,11 +209,12 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
         store16(P.out, base + c0, P.out_fmt, va);
         if (two) store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
-      if (P.row_ssq) {          // expert outputs: bn is 128 or 256, stored as FP32
+      if (P.row_ssq) {          // expert outputs (bn is 128 or 256), squared as stored
+        const bool rb = P.out_fmt == OUT_BF16;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ss = fmaf(va[i], va[i], ss);
+        for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ss = fmaf(vb[i], vb[i], ss);
+        for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], rb); ss = fmaf(q, q, ss); }
         if (((c0 + 32) & 127) == 0) {
           if (row_ok)
             P.row_ssq[row * (P.N >> 7) + ((tc.n_blk * P.bn + c0) >> 7)] = ss;

@@ -288,6 +288,7 @@ __global__ void __launch_bounds__(MEM_THREADS)
 
 // ---- combine -----------------------------------------------------------------------
 // One block per (token, slice of `cols` columns, at most 1024) with cols / 4 threads.
+// Expert output rows y are FP32, or BF16 when Y_BF16 (BF16 experts and NVFP4 experts).
 // The down GEMM's epilogue left, for every stored expert output row, the sum of squares
 // of each 128-column block (row_ssq, [rows, p / 128]).  Thread 0 bulk-copies the token's
 // k row slices into shared memory while the warps form r_j = rsqrt(sum / p + eps) from
@@ -304,9 +305,9 @@ inline int combine_cols(int p) {
   return 128;
 }
 
-template <bool C_F32>
+template <bool C_F32, bool Y_BF16>
 __global__ void __launch_bounds__(MEM_THREADS)
-    combine_kernel(const float* __restrict__ y, const float* __restrict__ row_ssq,
+    combine_kernel(const void* __restrict__ y, const float* __restrict__ row_ssq,
                    const int* __restrict__ inv, const int32_t* __restrict__ ids,
                    const float* __restrict__ wts, const float* __restrict__ g_exp,
                    void* __restrict__ c_out, int p, int cols, int k, int E, float eps,
@@ -318,7 +319,8 @@ __global__ void __launch_bounds__(MEM_THREADS)
   const int nq = p / cols;
   const size_t t = blockIdx.x / nq;
   const int col0 = static_cast<int>(blockIdx.x % nq) * cols;
-  const uint32_t slice = static_cast<uint32_t>(cols) * 4;
+  constexpr int YB = Y_BF16 ? 2 : 4;          // bytes per stored y value
+  const uint32_t slice = static_cast<uint32_t>(cols) * YB;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (threadIdx.x < MAX_TOPK) {
     int r = -1, e = 0;
@@ -340,7 +342,9 @@ __global__ void __launch_bounds__(MEM_THREADS)
     mbar_arrive_expect_tx(&landed, bytes);
     for (int j = 0; j < k; ++j)
       if (srow[j] >= 0)
-        bulk_load(cmb_smem + j * slice, y + size_t(srow[j]) * p + col0, slice, &landed);
+        bulk_load(cmb_smem + j * slice,
+                  static_cast<const uint8_t*>(y) + (size_t(srow[j]) * p + col0) * YB, slice,
+                  &landed);
   }
   // slot j's 128-column sums of squares, added by a fixed warp tree (warp j mod warps)
   for (int j = w; j < k; j += static_cast<int>(blockDim.x >> 5)) {
@@ -362,7 +366,14 @@ __global__ void __launch_bounds__(MEM_THREADS)
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < k; ++j) {
     if (srow[j] < 0) continue;
-    const float4 v = *reinterpret_cast<const float4*>(cmb_smem + j * slice + 4 * cl);
+    float4 v;
+    if constexpr (Y_BF16) {
+      const uint2 b = *reinterpret_cast<const uint2*>(cmb_smem + j * slice + 2 * cl);
+      const float2 lo = unpack_bf16x2(b.x), hi = unpack_bf16x2(b.y);
+      v = make_float4(lo.x, lo.y, hi.x, hi.y);
+    } else {
+      v = *reinterpret_cast<const float4*>(cmb_smem + j * slice + 4 * cl);
+    }
     const float4 g = *reinterpret_cast<const float4*>(g_exp + size_t(seid[j]) * p + col0 + cl);
     const float sc = sj[j];
     acc[0] = fmaf(sc, v.x * g.x, acc[0]);
@@ -382,23 +393,39 @@ __global__ void __launch_bounds__(MEM_THREADS)
   }
 }
 
-// Block sums of squares of stored expert output rows, for the down GEMM variants whose
-// epilogue does not produce them (weight-row tiles): one thread per (row, 128 columns),
-// summed in column order like the GEMM epilogues.
+// Block sums of squares of stored expert output rows (FP32, or BF16 when Y_BF16), for the
+// down GEMM variants whose epilogue does not produce them (weight-row tiles): one thread
+// per (row, 128 columns), summed in column order like the GEMM epilogues.
+template <bool Y_BF16>
 __global__ void __launch_bounds__(MEM_THREADS)
-    row_ssq_kernel(const float* __restrict__ y, int rows, int p, float* __restrict__ row_ssq) {
+    row_ssq_kernel(const void* __restrict__ y, int rows, int p, float* __restrict__ row_ssq) {
   const int parts = p >> 7;
   const size_t n = size_t(rows) * parts;
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n;
        i += size_t(gridDim.x) * blockDim.x) {
-    const float4* src = reinterpret_cast<const float4*>(y + (i / parts) * p + (i % parts) * 128);
+    const size_t e0 = (i / parts) * p + (i % parts) * 128;
     float ss = 0.f;
-    for (int q = 0; q < 32; ++q) {
-      const float4 v = src[q];
-      ss = fmaf(v.x, v.x, ss);
-      ss = fmaf(v.y, v.y, ss);
-      ss = fmaf(v.z, v.z, ss);
-      ss = fmaf(v.w, v.w, ss);
+    if constexpr (Y_BF16) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + e0);
+      for (int q = 0; q < 16; ++q) {
+        const uint4 v = src[q];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const float2 f = unpack_bf16x2(w[h]);
+          ss = fmaf(f.x, f.x, ss);
+          ss = fmaf(f.y, f.y, ss);
+        }
+      }
+    } else {
+      const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(y) + e0);
+      for (int q = 0; q < 32; ++q) {
+        const float4 v = src[q];
+        ss = fmaf(v.x, v.x, ss);
+        ss = fmaf(v.y, v.y, ss);
+        ss = fmaf(v.z, v.z, ss);
+        ss = fmaf(v.w, v.w, ss);
+      }
     }
     row_ssq[i] = ss;
   }

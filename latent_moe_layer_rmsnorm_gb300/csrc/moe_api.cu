@@ -118,7 +118,7 @@ moe_status_t device_ready(int* sms) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_smem_bytes()));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_F32>,
+      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_BF16>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_smem_bytes()));
     const int pair_smem = static_cast<int>(pair_smem_bytes());
@@ -253,7 +253,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.inv = take(T * k * 4);
   L.a_perm = take(q ? R * p / 2 : R * p * ee);
   L.s = take(q ? R * I / 2 : R * I * ee);
-  L.y = take(R * p * 4);     // expert outputs stay FP32 until the per-expert norm
+  L.y = take(R * p * (c.expert == MOE_F32 ? 4 : 2));   // expert outputs: BF16 (FP32 experts: FP32)
   L.ssq = take(R * (p / 128) * 4);   // their sums of squares per 128-column block
   L.c = take(T * p * ea);
   L.sf_u = take(q ? R * p / 16 : 0);
@@ -538,13 +538,18 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   E.mark(5);
 
   // ---- stage: grouped down GEMM -> y ------------------------------------------------------
+  // y: BF16 (FP32 only for FP32 experts), with FP32 sums of squares of the stored values
+  // per 128 columns beside it; the per-expert norm and the weighted sum run in FP32
   void* y_buf = base + L.y;
   float* ssq = reinterpret_cast<float*>(base + L.ssq);
+  const bool y_bf16 = !exp_f32;
+  const int y_fmt = y_bf16 ? OUT_BF16 : OUT_F32;
+  const int y_op = y_bf16 ? OP_BF16 : OP_TF32;
   if (nvf4) {
-    CUtensorMap ta, tb, ty;   // ty: y in 32 x 32 FP32 boxes for the epilogue's stores
+    CUtensorMap ta, tb, ty;   // ty: y in 32-row x 64-column BF16 boxes for the epilogue
     if (!make_tmap(&ta, s_buf, OP_NVF4, I / 2, R, GEMM_BM) ||
         !make_tmap(&tb, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, NV_BN) ||
-        !make_tmap(&ty, y_buf, OP_TF32, p, R, 32))
+        !make_tmap(&ty, y_buf, OP_BF16, p, R, 32))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = NV_BN; P.groups = E_;
@@ -552,7 +557,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = y_buf; P.ld_out = p; P.row_ssq = ssq;
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
     const int grid = std::min(sms, max_mt * (p / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_STORE_F32><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, ty, P);
+    gemm_nvf4_kernel<NV_EPI_STORE_BF16><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, ty, P);
     MOE_TRY(last_launch());
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on M (128 rows of p), up to 256 tokens on N
@@ -563,7 +568,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = 128; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt2_off; P.row_cnt = row_cnt;
-    P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32;
+    P.out = y_buf; P.ld_out = p; P.out_fmt = y_fmt;
     const int max_mt2 = (rows + 255) / 256 + E_;
     const int grid = std::min(sms, max_mt2 * (p / 128));
     if (exp_f32)
@@ -572,8 +577,9 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       gemm_swap_kernel<OP_BF16, SWAP_STORE><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
     MOE_TRY(last_launch());
     const size_t n = rows * static_cast<size_t>(p / 128);
-    row_ssq_kernel<<<static_cast<int>(std::min<size_t>((n + MEM_THREADS - 1) / MEM_THREADS, 4096)),
-                     MEM_THREADS, 0, st>>>(static_cast<const float*>(y_buf), rows, p, ssq);
+    const int ssq_grid = static_cast<int>(std::min<size_t>((n + MEM_THREADS - 1) / MEM_THREADS, 4096));
+    if (y_bf16) row_ssq_kernel<true><<<ssq_grid, MEM_THREADS, 0, st>>>(y_buf, rows, p, ssq);
+    else row_ssq_kernel<false><<<ssq_grid, MEM_THREADS, 0, st>>>(y_buf, rows, p, ssq);
     MOE_TRY(last_launch());
   } else {
     CUtensorMap ta, tb;
@@ -581,13 +587,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = bn; P.groups = E_;
     P.row_off = row_off; P.row_cnt = row_cnt;
-    P.out = y_buf; P.ld_out = p; P.out_fmt = OUT_F32; P.row_ssq = ssq;
+    P.out = y_buf; P.ld_out = p; P.out_fmt = y_fmt; P.row_ssq = ssq;
     if (bn == 256) {    // CTA pairs over 256-row tiles (M = 128 pair tiles for remainders)
       CUtensorMap ta64, to;
       if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
           !make_tmap(&ta64, s_buf, k_down, I, rows, GEMM_BM / 2) ||
           !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128) ||
-          !make_tmap(&to, y_buf, OP_TF32, p, rows, 32))
+          !make_tmap(&to, y_buf, y_op, p, rows, 32))
         return MOE_ERR_CUDA;
       P.mt_off = mt2_off;
       const int tiles = (rows / 256 + E_) * (p / 256);
@@ -608,14 +614,17 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   // ---- stage: per-expert RMSNorm + FP32 weighted sum -------------------------------------
   void* c_buf = base + L.c;
   const int ccols = combine_cols(p);
-  if (act_f32)
-    combine_kernel<true><<<T * (p / ccols), ccols / 4, size_t(MAX_TOPK) * ccols * 4, st>>>(
-        static_cast<const float*>(y_buf), ssq, inv, ids, wts, W->g_exp, c_buf, p, ccols, k, E_,
-        c.eps, status, base_params(status, c.flags).timeout_ns);
-  else
-    combine_kernel<false><<<T * (p / ccols), ccols / 4, size_t(MAX_TOPK) * ccols * 4, st>>>(
-        static_cast<const float*>(y_buf), ssq, inv, ids, wts, W->g_exp, c_buf, p, ccols, k, E_,
-        c.eps, status, base_params(status, c.flags).timeout_ns);
+  {
+    const int cgrid = T * (p / ccols), cthreads = ccols / 4;
+    const size_t csmem = size_t(MAX_TOPK) * ccols * (y_bf16 ? 2 : 4);
+    const unsigned long long tmo = base_params(status, c.flags).timeout_ns;
+#define LMOE_COMBINE(CF, YB)                                                              \
+  combine_kernel<CF, YB><<<cgrid, cthreads, csmem, st>>>(y_buf, ssq, inv, ids, wts, W->g_exp, \
+                                                         c_buf, p, ccols, k, E_, c.eps, status, tmo)
+    if (act_f32) { if (y_bf16) LMOE_COMBINE(true, true); else LMOE_COMBINE(true, false); }
+    else { if (y_bf16) LMOE_COMBINE(false, true); else LMOE_COMBINE(false, false); }
+#undef LMOE_COMBINE
+  }
   MOE_TRY(last_launch());
   E.mark(7);
 

@@ -209,13 +209,16 @@ def storage_kinds(act: str, expert: str, out: str, chain: bool) -> dict:
     tc = act == "f32"            # FP32 activations run their GEMMs on TF32 operands
     te = expert == "f32"
     # BF16 configurations: the norm-bounded GEMM operands h, u, c (and the weights they
-    # meet: pooler, gate/up, unpooler) are FP16; s and the down weights stay BF16.
+    # meet: pooler, gate/up, unpooler) are FP16; s and the down weights stay BF16.  The
+    # pages fix the per-expert norm and the weighted sum in FP32 but not the format the
+    # expert outputs y wait in before them: BF16 (FP32 for FP32 experts), normalised
+    # from the stored values.
     return dict(
         h_pool="tf32" if tc else "f16",
         pooled="f32",
         u="tf32" if te else "f16",
         s="tf32" if te else "bf16",
-        y="f32",                              # expert outputs are kept in FP32
+        y="f32" if te else "bf16",            # expert outputs, the per-expert norm's input
         c="tf32" if tc else "f16",
         out=out,
         w_proj="tf32" if tc else "f16",
@@ -327,7 +330,7 @@ def route(inp: dict, *, top_k: int, eps: float, tokens=None):
 
 def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts):
     """The block with NVFP4 experts; storage points as in the BF16 chain except the
-    expert operands: u and s are NVFP4 (u quantised from its FP32 value), y FP32."""
+    expert operands: u and s are NVFP4 (u quantised from its FP32 value); y BF16."""
     st = storage_kinds("bf16", "bf16", out, True)
     x = as_f64(inp["x"])
     if tokens is not None:
@@ -359,7 +362,7 @@ def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts):
             if s_all is None:
                 s_all = np.zeros((n, top_k, s.shape[1]))
             s_all[rows, slots] = s
-        y_all[rows, slots] = F.fp32(expert_down(s_deq, wq["down"]))
+        y_all[rows, slots] = F.bf16(expert_down(s_deq, wq["down"]))
     c = _store(combine(y_all, ids, wts, inp["g_exp"], eps), st["c"])
     res = _store(unpool(c, _store(as_f64(inp["w_unpool"]), st["w_proj"])), st["out"])
     if not return_parts:

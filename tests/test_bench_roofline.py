@@ -1,0 +1,47 @@
+"""The benchmark's byte and FLOP counts for the expert GEMMs, on CPU: the algorithmic
+bytes of one launch and which roofline (tensor or HBM) each workload falls under."""
+import bench
+from latent_moe_layer_rmsnorm_gb300 import synth
+
+
+def test_gate_up_bytes_of_the_profiled_slice():
+    # 16 experts x (4096 x 8192) FP16 W13, 8192 dispatched FP16 rows of 4096 in, 8192 BF16
+    # rows of 4096 out: the 1.208 GB counted by hand for the ncu capture of this slice
+    s = synth.PREFILL_SLICE_BF16
+    b = bench.expert_gemm_bytes(s, 16, s.T)["gemm1_gate_up_swiglu"]
+    assert b == 16 * 4096 * 8192 * 2 + 8192 * 4096 * 2 + 8192 * 4096 * 2
+    assert abs(b / 1e9 - 1.208) < 1e-3
+
+
+def test_down_bytes_include_output_rows_and_partials():
+    s = synth.PREFILL_SLICE_BF16
+    b = bench.expert_gemm_bytes(s, 16, s.T)["gemm2_down"]
+    R = s.T * s.top_k
+    assert b == 16 * 4096 * 4096 * 2 + R * 4096 * 2 + R * 4096 * 2 + R * 32 * 4
+    f = synth.TINY_F32           # FP32 experts: FP32 weights, s and y
+    bf = bench.expert_gemm_bytes(f, f.E, f.T)["gemm2_down"]
+    Rf = f.T * f.top_k
+    assert bf == f.E * f.I * f.p * 4 + Rf * f.I * 4 + Rf * f.p * 4 + Rf * (f.p // 128) * 4
+
+
+def test_nvfp4_bytes_are_codes_plus_block_scales():
+    s = synth.PREFILL_SLICE_NVFP4
+    b = bench.expert_gemm_bytes(s, 16, s.T)["gemm1_gate_up_swiglu"]
+    R = s.T * s.top_k
+    per_elem = 0.5 + 1 / 16
+    assert b == (16 * 4096 * 8192 + R * 4096 + R * 4096) * per_elem
+
+
+def _intensity(shape, touched):
+    fl = bench.flops_per_token(shape)["gemm1_gate_up_swiglu"] * shape.T
+    return fl / bench.expert_gemm_bytes(shape, touched, shape.T)["gemm1_gate_up_swiglu"]
+
+
+def test_decode_streams_weights_and_prefill_is_compute_bound():
+    ridge_bf16 = 1700e12 / 6763e9
+    ridge_fp4 = 6 * ridge_bf16
+    # 64 tokens x top-8 over 256 experts touch about 221 experts
+    assert _intensity(synth.DECODE_BF16, 221) < 5 < ridge_bf16
+    assert _intensity(synth.DECODE_NVFP4, 221) < ridge_fp4
+    assert _intensity(synth.PREFILL_BF16, 256) > ridge_bf16
+    assert _intensity(synth.PREFILL_NVFP4, 256) > ridge_fp4
