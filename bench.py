@@ -340,7 +340,7 @@ def run_ours(args):
             raise SystemExit("end-to-end output differs from the device-resident run")
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        n_e2e = max(4, args.steps // 2)
+        n_e2e = max(4, args.steps)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()

@@ -287,16 +287,20 @@ __global__ void __launch_bounds__(MEM_THREADS)
 }
 
 // ---- combine -----------------------------------------------------------------------
-// One block per (token, slice of `cols` columns, at most 1024) with cols / 4 threads.
-// Expert output rows y are FP32, or BF16 when Y_BF16 (BF16 experts and NVFP4 experts).
-// The down GEMM's epilogue left, for every stored expert output row, the sum of squares
-// of each 128-column block (row_ssq, [rows, p / 128]).  Thread 0 bulk-copies the token's
-// k row slices into shared memory while the warps form r_j = rsqrt(sum / p + eps) from
-// row j's blocks (a fixed warp tree), so the rows are read once and each block keeps up
-// to 32 KB in flight with few registers; then c = sum_j w_j * r_j * g_exp[e_j] * y_j is accumulated in FP32
-// in slot order j = 0..k-1 and stored as the unpooler's operand: FP16
-// (|c_i| <= sum_j |w_j| * sqrt(p) * max|g_exp|), or TF32-rounded FP32.
+// One block per (token, slice of `cols` columns, at most 1024), 8 columns per thread.
+// Expert output rows y are FP32, or BF16 when Y_BF16 (BF16 and NVFP4 experts).  The down
+// GEMM's epilogue left, for every stored expert output row, the sum of squares of each
+// 128-column block (row_ssq, [rows, p / 128]).  Thread 0 bulk-copies the token's k row
+// slices into shared memory while the warps form r_j = rsqrt(sum / p + eps) from row
+// j's blocks (a fixed warp tree); then c = sum_j w_j * r_j * g_exp[e_j] * y_j is
+// accumulated in FP32 in slot order j = 0..k-1 and stored as the unpooler's operand:
+// FP16 (|c_i| <= sum_j |w_j| * sqrt(p) * max|g_exp|), or TF32-rounded FP32.  Blocks of
+// 128 threads and 16 KB (BF16) let 13 of them, and so 13 tokens' copies, be resident
+// per SM: measured on GB300 at 4.5 TB/s for the prefill chunk against 3.2 TB/s with
+// 256-thread blocks of 4 columns per thread and 2.0-3.0 TB/s for persistent variants
+// whose block- or warp-wide steps serialised the dependent reads.
 constexpr int COMBINE_MAX_COLS = 1024;
+constexpr int COMBINE_VEC = 8;                 // columns per thread
 
 // Columns per block: the largest multiple of 128 that divides p, at most 1024.
 inline int combine_cols(int p) {
@@ -304,9 +308,13 @@ inline int combine_cols(int p) {
     if (p % c == 0) return c;
   return 128;
 }
+inline int combine_threads(int cols) { return cols / COMBINE_VEC < 32 ? 32 : cols / COMBINE_VEC; }
+inline size_t combine_smem_bytes(int cols, bool y_bf16) {
+  return size_t(MAX_TOPK) * cols * (y_bf16 ? 2 : 4);
+}
 
 template <bool C_F32, bool Y_BF16>
-__global__ void __launch_bounds__(MEM_THREADS)
+__global__ void __launch_bounds__(COMBINE_MAX_COLS / COMBINE_VEC)
     combine_kernel(const void* __restrict__ y, const float* __restrict__ row_ssq,
                    const int* __restrict__ inv, const int32_t* __restrict__ ids,
                    const float* __restrict__ wts, const float* __restrict__ g_exp,
@@ -316,10 +324,10 @@ __global__ void __launch_bounds__(MEM_THREADS)
   __shared__ uint64_t landed;
   __shared__ float sj[MAX_TOPK];     // w_j * r_j
   __shared__ int srow[MAX_TOPK], seid[MAX_TOPK];
+  constexpr int YB = Y_BF16 ? 2 : 4;  // bytes per stored y value
   const int nq = p / cols;
   const size_t t = blockIdx.x / nq;
   const int col0 = static_cast<int>(blockIdx.x % nq) * cols;
-  constexpr int YB = Y_BF16 ? 2 : 4;          // bytes per stored y value
   const uint32_t slice = static_cast<uint32_t>(cols) * YB;
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   if (threadIdx.x < MAX_TOPK) {
@@ -361,35 +369,49 @@ __global__ void __launch_bounds__(MEM_THREADS)
     mbar_wait_bounded(&landed, 0, &never, status, WAIT_COMBINE, timeout_ns);
   }
   __syncthreads();
-  // each thread: 4 consecutive columns of the quarter
-  const int cl = 4 * threadIdx.x;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  const int cl = COMBINE_VEC * threadIdx.x;    // this thread's first column of the slice
+  if (cl >= cols) return;
+  float acc[COMBINE_VEC];
+#pragma unroll
+  for (int i = 0; i < COMBINE_VEC; ++i) acc[i] = 0.f;
   for (int j = 0; j < k; ++j) {
     if (srow[j] < 0) continue;
-    float4 v;
+    const uint8_t* src = cmb_smem + j * slice + cl * YB;
+    float v[COMBINE_VEC];
     if constexpr (Y_BF16) {
-      const uint2 b = *reinterpret_cast<const uint2*>(cmb_smem + j * slice + 2 * cl);
-      const float2 lo = unpack_bf16x2(b.x), hi = unpack_bf16x2(b.y);
-      v = make_float4(lo.x, lo.y, hi.x, hi.y);
+      const uint4 b = *reinterpret_cast<const uint4*>(src);
+      const float2 f0 = unpack_bf16x2(b.x), f1 = unpack_bf16x2(b.y);
+      const float2 f2 = unpack_bf16x2(b.z), f3 = unpack_bf16x2(b.w);
+      v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
+      v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
     } else {
-      v = *reinterpret_cast<const float4*>(cmb_smem + j * slice + 4 * cl);
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 b = *reinterpret_cast<const float4*>(src + 16);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     }
-    const float4 g = *reinterpret_cast<const float4*>(g_exp + size_t(seid[j]) * p + col0 + cl);
+    const float* gp = g_exp + size_t(seid[j]) * p + col0 + cl;
+    const float4 g0 = *reinterpret_cast<const float4*>(gp);
+    const float4 g1 = *reinterpret_cast<const float4*>(gp + 4);
+    const float g[COMBINE_VEC] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
     const float sc = sj[j];
-    acc[0] = fmaf(sc, v.x * g.x, acc[0]);
-    acc[1] = fmaf(sc, v.y * g.y, acc[1]);
-    acc[2] = fmaf(sc, v.z * g.z, acc[2]);
-    acc[3] = fmaf(sc, v.w * g.w, acc[3]);
+#pragma unroll
+    for (int i = 0; i < COMBINE_VEC; ++i) acc[i] = fmaf(sc, v[i] * g[i], acc[i]);
   }
   const size_t off = t * p + col0 + cl;
   if constexpr (C_F32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(c_out) + off) =
-        make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]), tf32_rna(acc[2]), tf32_rna(acc[3]));
+    float* o = static_cast<float*>(c_out) + off;
+    *reinterpret_cast<float4*>(o) = make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]),
+                                                tf32_rna(acc[2]), tf32_rna(acc[3]));
+    *reinterpret_cast<float4*>(o + 4) = make_float4(tf32_rna(acc[4]), tf32_rna(acc[5]),
+                                                    tf32_rna(acc[6]), tf32_rna(acc[7]));
   } else {
-    uint2 o;
+    uint4 o;
     o.x = pack_f16x2(acc[0], acc[1]);
     o.y = pack_f16x2(acc[2], acc[3]);
-    *reinterpret_cast<uint2*>(static_cast<__half*>(c_out) + off) = o;
+    o.z = pack_f16x2(acc[4], acc[5]);
+    o.w = pack_f16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(static_cast<__half*>(c_out) + off) = o;
   }
 }
 

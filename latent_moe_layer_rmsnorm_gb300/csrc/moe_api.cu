@@ -613,10 +613,10 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
 
   // ---- stage: per-expert RMSNorm + FP32 weighted sum -------------------------------------
   void* c_buf = base + L.c;
-  const int ccols = combine_cols(p);
   {
-    const int cgrid = T * (p / ccols), cthreads = ccols / 4;
-    const size_t csmem = size_t(MAX_TOPK) * ccols * (y_bf16 ? 2 : 4);
+    const int ccols = combine_cols(p);
+    const int cgrid = T * (p / ccols), cthreads = combine_threads(ccols);
+    const size_t csmem = combine_smem_bytes(ccols, y_bf16);
     const unsigned long long tmo = base_params(status, c.flags).timeout_ns;
 #define LMOE_COMBINE(CF, YB)                                                              \
   combine_kernel<CF, YB><<<cgrid, cthreads, csmem, st>>>(y_buf, ssq, inv, ids, wts, W->g_exp, \
