@@ -25,7 +25,8 @@
 // measured).  TMEM then holds one 256-column accumulator (columns [0, 256)) and a ring
 // of per-stage scale columns after it, so the epilogue of a tile runs before the next
 // tile's MMAs start; eight epilogue warps (two per lane quadrant, one per 128-column
-// half) keep that gap short.
+// half) keep that gap short, each taking 32 SwiGLU columns or a 64-column y box per
+// TMEM wait.
 // A rows are 128-aligned per expert (padded dispatch), so a tile's scales are whole chunks.
 #pragma once
 
@@ -92,68 +93,71 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
     const float inv_g = gam > 0.f ? 1.0f / gam : 0.f;
     const int I = P.ld_out;
     uint8_t* codes = static_cast<uint8_t*>(P.out) + row * (I / 2);
+    // 32 output columns (two quantisation blocks) per TMEM wait: the two blocks' SwiGLU
+    // and quantisation chains are independent, so one warp overlaps them
 #pragma unroll 1
-    for (int c0 = 0; c0 < 64; c0 += 16) {
-      uint32_t g[16], u[16];
-      tmem_ld16(taddr + c0, g);
-      tmem_ld16(taddr + 64 + c0, u);
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t g0[16], g1[16], u0[16], u1[16];
+      tmem_ld16(taddr + c0, g0);
+      tmem_ld16(taddr + c0 + 16, g1);
+      tmem_ld16(taddr + 64 + c0, u0);
+      tmem_ld16(taddr + 64 + c0 + 16, u1);
       tmem_ld_wait();
-      float s[16];
+      float s0[16], s1[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float a = __uint_as_float(g[i]) * sc;
-        const float b = __uint_as_float(u[i]) * sc;
-        s[i] = __fdividef(a, 1.0f + __expf(-a)) * b;     // silu(a) * b
+        const float a0 = __uint_as_float(g0[i]) * sc, b0 = __uint_as_float(u0[i]) * sc;
+        const float a1 = __uint_as_float(g1[i]) * sc, b1 = __uint_as_float(u1[i]) * sc;
+        s0[i] = __fdividef(a0, 1.0f + __expf(-a0)) * b0;   // silu(a) * b
+        s1[i] = __fdividef(a1, 1.0f + __expf(-a1)) * b1;
       }
-      uint2 q;
-      const uint32_t code = quantize16(s, six_g, inv_g, q, recip);
+      uint2 q0, q1;
+      const uint32_t code0 = quantize16(s0, six_g, inv_g, q0, recip);
+      const uint32_t code1 = quantize16(s1, six_g, inv_g, q1, recip);
       if (row_ok) {
         const int col = tc.n_blk * (NV_BN / 2) + hh * 64 + c0;
-        *reinterpret_cast<uint2*>(codes + col / 2) = q;
-        P.out_sf[sf_offset(row, col / 16, I)] = static_cast<uint8_t>(code);
+        *reinterpret_cast<uint4*>(codes + col / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
+        P.out_sf[sf_offset(row, col / 16, I)] = static_cast<uint8_t>(code0);
+        P.out_sf[sf_offset(row, col / 16 + 1, I)] = static_cast<uint8_t>(code1);
       }
     }
   } else {
     const float sc = P.grp_scale[tc.e] * P.out_scale[tc.e];
     const int lane = r & 31;
     float ss = 0.f;     // the half is one 128-column block of the row (row_ssq)
+    // one 32-row x 64-column BF16 staging box per TMEM wait: row `lane`, 16-byte chunk j
+    // (columns 8j..8j+7) at chunk (j ^ lane % 8), the 128-byte swizzle of the tensor map
 #pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 32) {
-      uint32_t a[16], b[16];
-      tmem_ld16(taddr + c0, a);
-      tmem_ld16(taddr + c0 + 16, b);
+    for (int c0 = 0; c0 < 128; c0 += 64) {
+      uint32_t a0[16], a1[16], a2[16], a3[16];
+      tmem_ld16(taddr + c0, a0);
+      tmem_ld16(taddr + c0 + 16, a1);
+      tmem_ld16(taddr + c0 + 32, a2);
+      tmem_ld16(taddr + c0 + 48, a3);
       tmem_ld_wait();
-      float va[16], vb[16];
+      float v[64];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        va[i] = __uint_as_float(a[i]) * sc;
-        vb[i] = __uint_as_float(b[i]) * sc;
+        v[i] = __uint_as_float(a0[i]) * sc;
+        v[16 + i] = __uint_as_float(a1[i]) * sc;
+        v[32 + i] = __uint_as_float(a2[i]) * sc;
+        v[48 + i] = __uint_as_float(a3[i]) * sc;
       }
-      // this warp's 32 rows x 64 BF16 columns fill one staging box over two passes (the
-      // first pass chunks 0-3 of each 128-byte row, the second chunks 4-7): row `lane`,
-      // 16-byte chunk j at chunk (j ^ lane % 8) (the 128-byte swizzle of the tensor map)
-      const int half = (c0 >> 5) & 1;
-      if (half == 0) {
-        if (lane == 0) tma_store_wait_read();
-        __syncwarp();
-      }
+      if (lane == 0) tma_store_wait_read();      // the box's previous store has read it
+      __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float* v = j < 2 ? va + 8 * j : vb + 8 * (j - 2);
-        const uint4 o = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-        *reinterpret_cast<uint4*>(ybox + lane * 128 + (((4 * half + j) ^ (lane & 7)) << 4)) = o;
+      for (int j = 0; j < 8; ++j) {
+        const float* w = v + 8 * j;
+        const uint4 o = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                   pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+        *reinterpret_cast<uint4*>(ybox + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
       }
-      if (half == 1) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0)
-          tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0 - 32, tc.a_row + (r - lane));
-      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0, tc.a_row + (r - lane));
 #pragma unroll
-      for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], true); ss = fmaf(q, q, ss); }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], true); ss = fmaf(q, q, ss); }
+      for (int i = 0; i < 64; ++i) { const float q = stored_value(v[i], true); ss = fmaf(q, q, ss); }
     }
     if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + 2 * tc.n_blk + hh] = ss;
   }
