@@ -108,6 +108,38 @@ def expert_gemm_bytes(s, n_experts_touched: int, T: int) -> dict:
 
 # ---- clocks --------------------------------------------------------------------------------
 
+def parse_clock_samples(out: str):
+    """Median SM clock under load, the maximum clock and the throttle reasons seen, from
+    `nvidia-smi --query-gpu=<ClockSampler.FIELDS> --format=csv,noheader,nounits` lines."""
+    sm, pw, smax, reasons = [], [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in out.splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            smax = float(f[2])
+        except ValueError:
+            continue
+        try:
+            pw.append(float(f[3]))
+        except ValueError:
+            pw.append(float("nan"))
+        for name, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return None
+    # under load = the samples drawing at least half the highest power seen (the
+    # idle lead-in before the timed region is left out of the median)
+    top = max((w for w in pw if w == w), default=None)
+    load = [c for c, w in zip(sm, pw) if top is None or (w == w and w >= 0.5 * top)]
+    return {"sm_mhz": statistics.median(load or sm), "sm_max_mhz": smax,
+            "samples": len(sm), "load_samples": len(load),
+            "power_w_max": top, "reasons": sorted(reasons)}
+
+
 class ClockSampler:
     """nvidia-smi sampling (100 ms) of SM clock and throttle reasons while running."""
 
@@ -135,33 +167,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, pw, smax, reasons = [], [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax = float(f[2])
-            except ValueError:
-                continue
-            try:
-                pw.append(float(f[3]))
-            except ValueError:
-                pw.append(float("nan"))
-            for name, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return None
-        # under load = the samples drawing at least half the highest power seen (the
-        # idle lead-in before the timed region is left out of the median)
-        top = max((w for w in pw if w == w), default=None)
-        load = [c for c, w in zip(sm, pw) if top is None or (w == w and w >= 0.5 * top)]
-        return {"sm_mhz": statistics.median(load or sm), "sm_max_mhz": smax,
-                "samples": len(sm), "load_samples": len(load),
-                "power_w_max": top, "reasons": sorted(reasons)}
+        return parse_clock_samples(out)
 
 
 # ---- ncu traffic record ----------------------------------------------------------------

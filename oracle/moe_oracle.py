@@ -34,8 +34,8 @@ Two modes:
 * chain=True ("precision chain", the parity gate): float64 arithmetic, with every
   value rounded where the GPU path stores it (see `storage_kinds`): h (FP32 for
   the router; FP16, or TF32 in FP32 mode, for the pooler), pooled (FP32), u and c
-  (FP16 / TF32), s (BF16 / TF32), y (FP32: the expert outputs only feed the
-  per-expert norm, so they keep accumulator precision) and out; the weights meet
+  (FP16 / TF32), s (BF16 / TF32), y (BF16, FP32 for FP32 experts: the format the
+  SGLang page's fused post-per-expert norm stores and squares) and out; the weights meet
   the GEMMs in the same formats (FP16 copies of the pooler, gate/up and unpooler
   weights).  The page fixes the FP32 route-weighted sum; the storage types are the
   kernel's.
