@@ -74,21 +74,38 @@ constexpr size_t nvf4_smem_bytes() {
 
 
 
+// The tile's scalars for row r, read before the epilogue waits for the accumulator so
+// their latency hides behind the tile's MMAs.  SwiGLU: x0 = per-token activation scale x
+// the expert's W13 scale, x1 = the expert's static scale of s.  Down: x0 = the expert's
+// W2 scale x the scale of s.  Every row of a tile lies inside the expert's 128-row
+// padded block, so the per-row scale array (one entry per padded row) covers it even
+// when the row holds no token.
+template <int EPI>
+__device__ __forceinline__ void nvf4_scalars(const GemmParams& P, const TileCoord& tc, int r,
+                                             float& x0, float& x1) {
+  if constexpr (EPI == NV_EPI_SWIGLU_Q) {
+    x0 = P.row_scale[static_cast<size_t>(tc.a_row + r)] * P.grp_scale[tc.e];
+    x1 = P.out_scale[tc.e];
+  } else {
+    x0 = P.grp_scale[tc.e] * P.out_scale[tc.e];
+    x1 = 0.f;
+  }
+}
+
 // One warp's 32 rows of one 128-column half `hh` of the tile (taddr points at the
-// half's first column).
+// half's first column); x0, x1 from nvf4_scalars.
 template <int EPI>
 __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoord& tc,
                                               uint32_t taddr, int r, int hh, const float* recip,
-                                              const CUtensorMap* tmY, uint8_t* ybox) {
+                                              const CUtensorMap* tmY, uint8_t* ybox, float x0,
+                                              float x1) {
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
     // columns [0, 64) of the half gate, [64, 128) up, of output features
     // n_blk * 128 + hh * 64 ..
-    // every row of a tile lies inside the expert's 128-row padded block, so the scale
-    // array (one entry per padded row) covers it even when the row holds no token
-    const float sc = P.row_scale[row] * P.grp_scale[tc.e];
-    const float gam = P.out_scale[tc.e];
+    const float sc = x0;
+    const float gam = x1;
     const float six_g = 6.0f * gam;
     const float inv_g = gam > 0.f ? 1.0f / gam : 0.f;
     const int I = P.ld_out;
@@ -122,7 +139,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       }
     }
   } else {
-    const float sc = P.grp_scale[tc.e] * P.out_scale[tc.e];
+    const float sc = x0;
     const int lane = r & 31;
     float ss = 0.f;     // the half is one 128-column block of the row (row_ssq)
     // one 32-row x 64-column BF16 staging box per TMEM wait: row `lane`, 16-byte chunk j
@@ -347,13 +364,16 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     const int r = q * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const TileCoord tc = gemm_tile(P, S, t);
+      float x0, x1;
+      nvf4_scalars<EPI>(P, tc, r, x0, x1);        // in flight while the MMAs run
       if (!mbar_wait_bounded(&S->tfull[0], it & 1, abort_flag, P.status, WAIT_EPI_TMEM_FULL,
                              limit))
         break;
       tc_fence_after();
-      const TileCoord tc = gemm_tile(P, S, t);
       const uint32_t taddr = tmem_base + hh * 128 + (static_cast<uint32_t>(q * 32) << 16);
-      nvf4_epilogue<EPI>(P, tc, taddr, r, hh, N->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX);
+      nvf4_epilogue<EPI>(P, tc, taddr, r, hh, N->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
+                         x0, x1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S->tempty[0]);
