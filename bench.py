@@ -77,8 +77,23 @@ def bytes_per_token(s, act_bytes=2) -> dict:
     yb = 4 if s.expert == "f32" else 2          # expert outputs y: BF16 unless FP32 experts
     return {
         "norm": s.d * act_bytes + s.d * 4 + s.d * act_bytes,            # x in; h32, h16 out
-        "dispatch": s.p * 4 + k * s.p * act_bytes + 16 * k,             # pooled in; k rows out
+        # pooled in; k rows of u out (NVFP4: codes + block scales + a per-row scale)
+        "dispatch": s.p * 4 + (k * s.p * (0.5 + 1 / 16) + 4 * k if s.expert == "nvfp4"
+                               else k * s.p * act_bytes) + 16 * k,
         "combine": k * s.p * yb + k * (s.p // 128) * 4 + s.p * act_bytes + 8 * k,  # y, sums in; c out
+    }
+
+
+def projection_bytes(s, T: int) -> dict:
+    """Compulsory HBM bytes of one launch of the router, pooler and unpooler GEMMs: the
+    weights once plus the rows in and out.  Router: TF32-rounded FP32 h and W_r in,
+    ids and weights out.  Pooler: FP16 h and W_pool in, FP32 pooled out.  Unpooler: FP16
+    c and W_unpool in, out in the activation format.  FP32 activations: FP32 operands."""
+    a = 4 if s.act == "f32" else 2
+    return {
+        "router": s.E * s.d * 4 + T * s.d * 4 + T * s.top_k * 8,
+        "pool": s.p * s.d * a + T * s.d * a + T * s.p * 4,
+        "unpool": s.d * s.p * a + T * s.p * a + T * s.d * a,
     }
 
 
@@ -401,6 +416,9 @@ def run_ours(args):
     stage_tflops = {n: fl[n] * T / (stage_ms[n] / 1e3) / 1e12 for n in fl if stage_ms.get(n)}
     stage_gbs = {n: by[n] * T / (stage_ms[n] / 1e3) / 1e9 for n in by if stage_ms.get(n)}
     gb = expert_gemm_bytes(shape, n_touched, T)
+    for n, b in projection_bytes(shape, T).items():   # weight streams at decode sizes
+        if stage_ms.get(n):
+            stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9
     for n, b in gb.items():
         if stage_ms.get(n):
             stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9

@@ -45,3 +45,13 @@ def test_decode_streams_weights_and_prefill_is_compute_bound():
     assert _intensity(synth.DECODE_NVFP4, 221) < ridge_fp4
     assert _intensity(synth.PREFILL_BF16, 256) > ridge_bf16
     assert _intensity(synth.PREFILL_NVFP4, 256) > ridge_fp4
+
+
+def test_projection_bytes_at_decode_are_the_weights():
+    s = synth.DECODE_BF16
+    b = bench.projection_bytes(s, s.T)
+    assert b["pool"] == 4096 * 8192 * 2 + 64 * 8192 * 2 + 64 * 4096 * 4
+    assert b["unpool"] == 8192 * 4096 * 2 + 64 * 4096 * 2 + 64 * 8192 * 2
+    assert b["router"] == 256 * 8192 * 4 + 64 * 8192 * 4 + 64 * 8 * 8
+    # at 64 tokens the weights are more than 95 % of each projection's bytes
+    assert 4096 * 8192 * 2 / b["pool"] > 0.95
