@@ -187,10 +187,12 @@ class ClockSampler:
 
 # ---- ncu traffic record ----------------------------------------------------------------
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(files=None) -> str:
+    """Hash of the kernel sources: every file under csrc/, or only `files` (the sources a
+    profiled kernel and its launch are built from), in name order."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "latent_moe_layer_rmsnorm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(os.listdir(csrc) if files is None else files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -198,14 +200,22 @@ def kernel_source_sha() -> str:
 
 def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the summary
-    is missing or was taken on different kernel sources."""
+    is missing or any source it was taken on has changed since.  The summary's line
+    `kernel_source_sha: <hash> (<files>)` names the csrc files the hash covers (all of
+    them when no list is given)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    if not m or not sha or sha.group(1) != kernel_source_sha():
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)(?:\s*\(([^)]*)\))?", text)
+    if not m or not sha:
+        return None
+    files = sha.group(2).split() if sha.group(2) else None
+    try:
+        if sha.group(1) != kernel_source_sha(files):
+            return None
+    except OSError:
         return None
     return float(m.group(1))
 
