@@ -351,6 +351,23 @@ def test_chain_stays_close_to_exact():
     assert 1e-5 < err < 2e-2
 
 
+def test_chain_stores_expert_outputs_where_the_kernels_do():
+    """The chain keeps y, the per-expert norm's input, on the BF16 grid for BF16 experts
+    (the format the SGLang page's fused post-per-expert norm stores) and in FP32 for FP32
+    experts, and the norm then reads those stored values."""
+    shape, inp = tiny(T=16, d=64, p=32, E=6, k=2, I=48, act="bf16", expert="bf16")
+    parts = fwd(inp, shape, chain=True, return_parts=True)
+    y = parts["y"]
+    assert np.array_equal(F.bf16(y), y)
+    assert not np.array_equal(F.bf16(parts["u"]), parts["u"])      # u is FP16, finer
+    shape32, inp32 = tiny(T=16, d=64, p=32, E=6, k=2, I=48)
+    y32 = fwd(inp32, shape32, chain=True, return_parts=True)["y"]
+    assert np.array_equal(F.fp32(y32), y32) and not np.array_equal(F.bf16(y32), y32)
+    # the combine normalises exactly the stored rows
+    c = oracle.combine(y, parts["ids"], parts["w"], oracle_view(inp)["g_exp"], shape.eps)
+    assert np.allclose(c, parts["c"], rtol=1e-3, atol=1e-3 * float(np.abs(c).max()))
+
+
 def test_margin_repair_makes_routes_unique():
     shape, inp = tiny(T=64, E=8, k=2)
     fix_margins(inp, shape, seed=0, min_gap=1e-3)
