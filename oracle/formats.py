@@ -95,12 +95,15 @@ def e2m1_encode(v) -> np.ndarray:
     2.5->2, 3.5->4, 5->4).
     """
     v = np.asarray(v, dtype=np.float64)
-    a = np.minimum(np.abs(v), 6.0)
-    # distance to every grid point (exact: the grid is dyadic); among the nearest
-    # points take the one with an even index, i.e. mantissa bit 0
-    dist = np.abs(a[..., None] - E2M1_MAGNITUDES)
-    nearest = dist == dist.min(axis=-1, keepdims=True)
-    best = np.argmin(np.where(nearest, np.arange(8) & 1, 2), axis=-1)
+    a = np.abs(v)
+    # The magnitude index is the number of midpoints between neighbouring grid values
+    # that |v| has passed.  At a midpoint itself the neighbour with an even index
+    # (mantissa bit 0) wins: the index moves up at the midpoints below the even
+    # indices 2, 4, 6 (0.75, 1.75, 3.5: ">=") and stays at the midpoints above the
+    # even indices 0, 2, 4, 6 (0.25, 1.25, 2.5, 5: ">").  Values above 5 give index 7
+    # (6), so magnitudes beyond 6 saturate.
+    best = ((a > 0.25).astype(np.int64) + (a >= 0.75) + (a > 1.25) + (a >= 1.75)
+            + (a > 2.5) + (a >= 3.5) + (a > 5.0))
     # the sign bit follows the input's sign, also when the magnitude rounds to zero
     # (as for IEEE conversions: -0.1 -> -0)
     return (best | np.where(np.signbit(v), 8, 0)).astype(np.uint8)

@@ -241,10 +241,45 @@ def nvfp4_expert_weights(w_gate_e, w_up_e, w_down_e):
                 g13=g13, q2=q2, sf2=sf2, g2=g2)
 
 
+def nvfp4_expert_rows(u_rows: np.ndarray, wq: dict, gamma: float) -> dict:
+    """One NVFP4 expert on its dispatched rows ("SGLang and Miles Add Day-0 Support for
+    Muse Spark Open", section "NVFP4 as a third MMA kind").
+
+    u_rows are the stored (dequantised) NVFP4 activations, so the per-token scale is
+    already inside them: a and b are the first GEMM's accumulators times that scale
+    and the weights' shared W13 scale (both carried by the dequantised operands).
+        s     = fp32(silu(a) * b),  a = W_gate u, b = W_up u
+        s_q   = NVFP4 of s with the static global scale gamma (scale codes per 16)
+        y     = bf16(W_down s_q)   (W_down dequantised with its own global scale)
+    Returns s (FP32 values before the requantisation), its codes qs / scale codes sfs,
+    the dequantised s_deq and y.
+    """
+    s = F.fp32(expert_swiglu(u_rows, wq["gate"], wq["up"]))
+    qs, sfs = Q.quantize_static(s, gamma)
+    s_deq = Q.dequantize(qs, sfs, np.float32(gamma))
+    y = F.bf16(expert_down(s_deq, wq["down"]))
+    return dict(s=s, qs=qs, sfs=sfs, s_deq=s_deq, y=y)
+
+
+def nvfp4_expert(w_gate_e, w_up_e, w_down_e, u_rows, gamma) -> dict:
+    """nvfp4_expert_rows with expert e's weights quantised by nvfp4_expert_weights."""
+    return nvfp4_expert_rows(u_rows, nvfp4_expert_weights(w_gate_e, w_up_e, w_down_e), gamma)
+
+
+def chain_expert(w_gate_e, w_up_e, w_down_e, u_rows, st: dict) -> dict:
+    """One BF16 / FP32 expert on its rows, rounded where the GPU path stores values:
+    s = store(silu(W_gate u) * W_up u), y = store(W_down s) (storage kinds `st`)."""
+    wg = _store(as_f64(w_gate_e), st["w_gate_up"])
+    wu = _store(as_f64(w_up_e), st["w_gate_up"])
+    wd = _store(as_f64(w_down_e), st["w_down"])
+    s = _store(expert_swiglu(u_rows, wg, wu), st["s"])
+    return dict(s=s, y=_store(expert_down(s, wd), st["y"]))
+
+
 def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
                 expert: str = "bf16", out: str = "f32", chain: bool = True,
                 tokens=None, ids=None, weights=None, norm_after_sum: bool = False,
-                return_parts: bool = False):
+                return_parts: bool = False, expert_map=None):
     """The latent-MoE block for the rows `tokens` of inp["x"] (all rows if None).
 
     inp holds x [T,d], g_in [d], w_router [E,d], w_pool [p,d], g_pool [p],
@@ -261,10 +296,17 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
     dequantised; the expert input u is quantised per token on the fly and the SwiGLU
     output s is requantised with the static per-expert global scale inp["gs_act2"][e]
     (the page gives no rule for that scale; see the design notes), as the kernels do.
+
+    expert_map (optional) evaluates the per-expert step elsewhere (e.g. in worker
+    processes): it receives a list of tasks (e, u_rows, arg) and must return, in the
+    same order, what `chain_expert(w_gate[e], w_up[e], w_down[e], u_rows, arg)` (or,
+    for NVFP4 experts, `nvfp4_expert(..., u_rows, arg)`) returns for expert e's
+    weights.  It only decides where the step runs; None runs it here on inp's weights.
     """
     if expert == "nvfp4":
         return _forward_nvfp4(inp, top_k=top_k, eps=eps, out=out, tokens=tokens, ids=ids,
-                              weights=weights, return_parts=return_parts)
+                              weights=weights, return_parts=return_parts,
+                              expert_map=expert_map)
     st = storage_kinds(act, expert, out, chain)
     x = as_f64(inp["x"])
     if tokens is not None:
@@ -288,19 +330,22 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
 
     p = u.shape[1]
     g_exp = as_f64(inp["g_exp"])
+    experts = [int(e) for e in np.unique(ids)]
+    tasks = [(e, u[np.nonzero(ids == e)[0]], st) for e in experts]
+    if expert_map is None:
+        results = [chain_expert(inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], ur, a)
+                   for e, ur, a in tasks]
+    else:
+        results = expert_map(tasks)
     y_all = np.zeros((n, top_k, p))
     s_all = None
-    for e in np.unique(ids):
+    for e, r in zip(experts, results):
         rows, slots = np.nonzero(ids == e)
-        wg = _store(as_f64(inp["w_gate"][e]), st["w_gate_up"])
-        wu = _store(as_f64(inp["w_up"][e]), st["w_gate_up"])
-        wd = _store(as_f64(inp["w_down"][e]), st["w_down"])
-        s = _store(expert_swiglu(u[rows], wg, wu), st["s"])
         if return_parts:
             if s_all is None:
-                s_all = np.zeros((n, top_k, s.shape[1]))
-            s_all[rows, slots] = s
-        y_all[rows, slots] = _store(expert_down(s, wd), st["y"])
+                s_all = np.zeros((n, top_k, r["s"].shape[1]))
+            s_all[rows, slots] = r["s"]
+        y_all[rows, slots] = r["y"]
 
     if not norm_after_sum:
         c = combine(y_all, ids, wts, g_exp, eps)
@@ -328,9 +373,11 @@ def route(inp: dict, *, top_k: int, eps: float, tokens=None):
     return ids, w, logits
 
 
-def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts):
+def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts,
+                   expert_map=None):
     """The block with NVFP4 experts; storage points as in the BF16 chain except the
-    expert operands: u and s are NVFP4 (u quantised from its FP32 value); y BF16."""
+    expert operands: u and s are NVFP4 (u quantised from its FP32 value with a per-token
+    scale, s with the static per-expert scale inp["gs_act2"]); y BF16."""
     st = storage_kinds("bf16", "bf16", out, True)
     x = as_f64(inp["x"])
     if tokens is not None:
@@ -350,22 +397,30 @@ def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts):
     u = Q.dequantize(qu, sfu, alpha)
     p = u.shape[1]
     gs2 = as_f64(inp["gs_act2"])
+    experts = [int(e) for e in np.unique(ids)]
+    tasks = [(e, u[np.nonzero(ids == e)[0]], float(gs2[e])) for e in experts]
+    if expert_map is None:
+        results = [nvfp4_expert(inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e], ur, g)
+                   for e, ur, g in tasks]
+    else:
+        results = expert_map(tasks)
     y_all = np.zeros((n, top_k, p))
-    s_all = None
-    for e in np.unique(ids):
+    s_all = qs_all = sfs_all = None
+    for e, r in zip(experts, results):
         rows, slots = np.nonzero(ids == e)
-        wq = nvfp4_expert_weights(inp["w_gate"][e], inp["w_up"][e], inp["w_down"][e])
-        s = F.fp32(expert_swiglu(u[rows], wq["gate"], wq["up"]))
-        qs, sfs = Q.quantize_static(s, gs2[e])
-        s_deq = Q.dequantize(qs, sfs, np.float32(gs2[e]))
         if return_parts:
             if s_all is None:
-                s_all = np.zeros((n, top_k, s.shape[1]))
-            s_all[rows, slots] = s
-        y_all[rows, slots] = F.bf16(expert_down(s_deq, wq["down"]))
+                I = r["s"].shape[1]
+                s_all = np.zeros((n, top_k, I))
+                qs_all = np.zeros((n, top_k, I), dtype=np.uint8)
+                sfs_all = np.zeros((n, top_k, I // Q.BLOCK), dtype=np.uint8)
+            s_all[rows, slots] = r["s"]
+            qs_all[rows, slots] = r["qs"]
+            sfs_all[rows, slots] = r["sfs"]
+        y_all[rows, slots] = r["y"]
     c = _store(combine(y_all, ids, wts, inp["g_exp"], eps), st["c"])
     res = _store(unpool(c, _store(as_f64(inp["w_unpool"]), st["w_proj"])), st["out"])
     if not return_parts:
         return res
-    return dict(out=res, h=h, ids=ids, w=wts, pooled=pooled, u32=u32, u=u, alpha=alpha,
-                s=s_all, y=y_all, c=c)
+    return dict(out=res, h=h, ids=ids, w=wts, pooled=pooled, u32=u32, qu=qu, sfu=sfu, u=u,
+                alpha=alpha, s=s_all, qs=qs_all, sfs=sfs_all, y=y_all, c=c)

@@ -94,3 +94,44 @@ def quantize_static(x: np.ndarray, g: float):
     x = np.asarray(x, dtype=F32)
     q, sf = quantize_blocks(x, np.full(x.shape[:-1], g, dtype=F32))
     return q, sf
+
+
+# ---- how close each rounding decision is to changing ---------------------------------
+
+_E2M1_MIDPOINTS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+_UE4M3_MIDPOINTS = (F.ue4m3_decode(np.arange(1, 0x7F)) + F.ue4m3_decode(np.arange(0, 0x7E))) / 2
+
+
+def decision_margins(x: np.ndarray, g: np.ndarray):
+    """Distances, in the units of x, from the two kinds of rounding decision that
+    quantize_blocks(x, g) takes to the points where those decisions would change.
+
+    elem [..., K]: for each element, |x * r - m| / r, where r is the element's block
+    multiplier (recip(scale) / g, as in quantize_blocks) and m is the E2M1 rounding
+    midpoint nearest to |x * r|: how far x may move before its code changes (block
+    scale held).  inf where r = 0 (a zero block or g = 0).
+    block [..., K/16]: for each block, |bmax / (6 g) - m'| * 6 g, m' the UE4M3 midpoint
+    nearest to bmax / (6 g): how far the block maximum may move before the block's
+    scale code changes.  inf where g = 0.
+
+    When two computations of x differ by less than these distances, they quantise to
+    the same codes.  Arithmetic in float64 on the FP32 quantities of quantize_blocks.
+    """
+    x = np.asarray(x, dtype=F32)
+    K = x.shape[-1]
+    xb = x.reshape(*x.shape[:-1], K // BLOCK, BLOCK).astype(np.float64)
+    g32 = np.asarray(g, dtype=F32)[..., None]
+    bmax = np.max(np.abs(xb), axis=-1)
+    six_g = (F32(6.0) * g32).astype(F32).astype(np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(six_g > 0, bmax / six_g, 0.0)
+        inv_g = np.where(g32 > 0, F32(1.0) / g32, F32(0.0)).astype(F32)
+    sf = F.ue4m3_encode(ratio.astype(F32).astype(np.float64))
+    r = (_RECIP[sf] * inv_g).astype(F32).astype(np.float64)
+    v = np.abs(xb) * r[..., None]
+    d_elem = np.min(np.abs(v[..., None] - _E2M1_MIDPOINTS), axis=-1)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        elem = np.where(r[..., None] > 0, d_elem / r[..., None], np.inf)
+        d_blk = np.min(np.abs(ratio[..., None] - _UE4M3_MIDPOINTS), axis=-1)
+        block = np.where(six_g > 0, d_blk * six_g, np.inf)
+    return elem.reshape(x.shape), block

@@ -54,6 +54,26 @@ def test_e2m1_ties_and_saturation():
     assert F.e2m1_encode(np.array([0.1]))[0] == 0
 
 
+def test_e2m1_encode_is_nearest_even_on_a_dense_sweep():
+    """The encoder against the format's definition, applied by brute force: the nearest
+    of the eight magnitudes, ties to the one with an even index (mantissa bit 0),
+    saturating at 6.  The sweep covers every midpoint and its FP32 neighbours."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    mids = (grid[1:] + grid[:-1]) / 2
+    near = np.concatenate([np.nextafter(mids.astype(np.float32), np.float32(-1)),
+                           np.nextafter(mids.astype(np.float32), np.float32(9))])
+    v = np.concatenate([np.linspace(0, 8, 160001), mids, near.astype(np.float64), grid])
+    v = np.concatenate([v, -v])
+    a = np.minimum(np.abs(v), 6.0)
+    best = np.empty(len(v), dtype=np.int64)
+    for i, x in enumerate(a):
+        d = np.abs(grid - x)
+        cand = np.nonzero(d == d.min())[0]
+        best[i] = cand[0] if len(cand) == 1 else cand[cand % 2 == 0][0]
+    want = np.where(np.signbit(v), -grid[best], grid[best])
+    np.testing.assert_array_equal(F.e2m1_decode(F.e2m1_encode(v)), want)
+
+
 def test_ue4m3_table_and_round_trip():
     codes = np.arange(0x7F)
     vals = F.ue4m3_decode(codes)
