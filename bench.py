@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the headline workload")
     ap.add_argument("--no-boundary", action="store_true",
                     help="skip the separate timing of moe_boundary on the step's output")
     return ap.parse_args()
@@ -238,14 +240,234 @@ def max_over_ranks(v: float, device) -> float:
     return float(t.item())
 
 
+# ---- roofline ---------------------------------------------------------------------------
+
+# A kernel timed inside a short region runs at the boost clock: its tensor peak is the
+# burst figure.  Only a timed region of at least this many seconds of back-to-back GEMMs
+# runs at the power-capped clock the sustained figure was measured at.
+SUSTAINED_MIN_S = 2.0
+# The FP4 MMA issue rate measured on a GB300 (a 128 x 128 x 64 block-scaled MMA every 64
+# cycles per SM = 16384 MAC/clk, 4x the BF16 kind's 4096): reported beside the nominal
+# 6x ratio, which sets the peak.
+FP4_MEASURED_ISSUE_PER_BF16 = 4.0
+
+
+def tensor_peak(peaks: dict, peak_src: str, timed_s: float, nvfp4: bool):
+    """(peak TFLOP/s, description) for a contraction timed inside a region of timed_s
+    seconds: burst BF16 below SUSTAINED_MIN_S, sustained at or above it; NVFP4 GEMMs
+    take FP4_PER_BF16 times that (the nominal dense ratio)."""
+    if timed_s >= SUSTAINED_MIN_S:
+        key, why = "bf16_tflops_sustained", f"timed region {timed_s:.2f} s >= {SUSTAINED_MIN_S:g} s"
+    else:
+        key, why = "bf16_tflops", f"timed region {timed_s:.2f} s < {SUSTAINED_MIN_S:g} s (boost clock)"
+    bf16 = float(peaks.get(key, FALLBACK_PEAKS[key]))
+    if nvfp4:
+        return bf16 * FP4_PER_BF16, (f"nvfp4 = {FP4_PER_BF16:g} x {key} ({peak_src}; nominal "
+                                     f"13.5 / 2.25 PFLOP/s ratio; measured FP4 MMA issue rate "
+                                     f"{FP4_MEASURED_ISSUE_PER_BF16:g} x bf16); {why}")
+    return bf16, f"{key} ({peak_src}); {why}"
+
+
+def roofline_of(shape, T, stage_ms, n_touched, timed_s, peaks, peak_src, workload):
+    """Roofline of the dominant GEMM stage, plus every stage's TFLOP/s and GB/s."""
+    fl = flops_per_token(shape)
+    by = bytes_per_token(shape)
+    stage_tflops = {n: fl[n] * T / (stage_ms[n] / 1e3) / 1e12 for n in fl if stage_ms.get(n)}
+    stage_gbs = {n: by[n] * T / (stage_ms[n] / 1e3) / 1e9 for n in by if stage_ms.get(n)}
+    gb = expert_gemm_bytes(shape, n_touched, T)
+    for n, b in projection_bytes(shape, T).items():   # weight streams at decode sizes
+        if stage_ms.get(n):
+            stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9
+    for n, b in gb.items():
+        if stage_ms.get(n):
+            stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9
+    dominant = max(fl, key=lambda n: stage_ms.get(n, 0.0))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    nv = shape.expert == "nvfp4" and dominant.startswith("gemm")
+    peak, kind = tensor_peak(peaks, peak_src, timed_s, nv)
+    traffic = recorded_traffic(workload, dominant)
+    flops_launch = fl[dominant] * T
+    bytes_launch = gb.get(dominant)
+    ridge = peak * 1e12 / (hbm_peak * 1e9)          # FLOP per byte where the bounds meet
+    intensity = flops_launch / bytes_launch if bytes_launch else None
+    if intensity is not None and intensity < ridge:
+        # too few rows per expert to reuse a weight tile: the launch streams the weights
+        achieved = stage_gbs[dominant]
+        roof = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
+                "peak": round(hbm_peak, 1), "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                "peak_kind": f"hbm_gbs ({peak_src}, copy bandwidth)",
+                "bytes_per_launch": bytes_launch, "flops_per_launch": flops_launch,
+                "experts_touched": n_touched,
+                "intensity_flop_per_byte": round(intensity, 2), "ridge": round(ridge, 1),
+                "tensor_tflops": round(stage_tflops[dominant], 1)}
+    else:
+        achieved = stage_tflops[dominant]
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
+                "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic, "peak_kind": kind, "flops_per_launch": flops_launch,
+                "bytes_per_launch": bytes_launch, "experts_touched": n_touched,
+                "intensity_flop_per_byte": round(intensity, 1) if intensity else None,
+                "ridge": round(ridge, 1)}
+        if nv:
+            meas = peak / FP4_PER_BF16 * FP4_MEASURED_ISSUE_PER_BF16
+            roof["frac_of_measured_fp4_issue_rate"] = round(achieved / meas, 4)
+    return roof, stage_tflops, stage_gbs
+
+
 # ---- our arm -----------------------------------------------------------------------------
+
+class Runner:
+    """One latent-MoE layer of a workload, with its inputs resident on the device."""
+
+    def __init__(self, shape, seed, experts=None):
+        import torch
+
+        from latent_moe_layer_rmsnorm_gb300 import synth
+        from latent_moe_layer_rmsnorm_gb300 import _lib as nst
+        from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+        self.shape = shape
+        inp = synth.make_dense(shape, seed, "cuda")
+        if experts is None:
+            experts = make_experts(shape, seed)
+        inp.update(experts)
+        if shape.expert == "nvfp4":
+            inp["gs_act2"] = synth.nvfp4_act2_scales(shape, "cuda")
+        self.out_kind = "bf16" if shape.act == "bf16" else "f32"
+        self.layer = LatentMoE(shape, inp, out=self.out_kind, keep_canonical=False)
+        self.x = inp["x"]
+        self.out = torch.empty((shape.T, shape.d), dtype=self.layer.out_dtype(), device="cuda")
+        self.stream = torch.cuda.current_stream()
+        self.stage_names = [nst.moe_stage_name(i) for i in range(nst.moe_num_stages())]
+
+    def forward(self, ids=None, w=None, events=None):
+        return self.layer.forward(self.x, ids=ids, w=w, out=self.out, events=events)
+
+    def touched(self):
+        import torch
+        ids, _ = self.layer.route(self.x)
+        return int(torch.unique(ids).numel())
+
+    def time(self, steps, warmup, world, replay=False):
+        """K steps bracketed by a barrier and synchronisations (plain calls: the kernels
+        of consecutive steps overlap their launches); then the same steps again with
+        CUDA events between the stages for the per-stage times.  Events between kernels
+        stop each kernel from starting before the previous one ends, so the stage times
+        come from that second pass and sum to a little more than a timed step.  Returns
+        (elapsed ms of the timed pass, mean ms per stage)."""
+        import torch
+        import torch.distributed as dist
+        ids = w = None
+        if replay:
+            ids, w = self.layer.route(self.x)
+        for _ in range(warmup):
+            self.forward(ids, w)
+        torch.cuda.synchronize()
+        st = self.layer.read_status()
+        if st != (0, 0):
+            raise SystemExit(f"device status after warm-up: {st}")
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(self.stream)
+        for _ in range(steps):
+            self.forward(ids, w)
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        elapsed = max_over_ranks(t0.elapsed_time(t1), "cuda")
+        st = self.layer.read_status()
+        if st != (0, 0):
+            raise SystemExit(f"device status after the timed steps: {st}")
+        n = len(self.stage_names)
+        np_ = min(steps, PROFILED_STEPS)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(np_)]
+        for row in evs:
+            for e in row:
+                e.record(self.stream)       # create the handles; re-recorded by the library
+        torch.cuda.synchronize()
+        for k in range(np_):
+            self.forward(ids, w, events=[e.cuda_event for e in evs[k]])
+        torch.cuda.synchronize()
+        stage_ms = {nm: 0.0 for nm in self.stage_names}
+        for row in evs:
+            for i, nm in enumerate(self.stage_names):
+                stage_ms[nm] += row[i].elapsed_time(row[i + 1]) / np_
+        if replay:
+            stage_ms.pop("router", None)
+        return elapsed, stage_ms
+
+
+# steps of the second, event-bracketed pass that gives the per-stage times
+PROFILED_STEPS = 20
+
+
+def make_experts(shape, seed):
+    """Expert matrices of a workload, drawn on the device."""
+    import torch
+
+    from latent_moe_layer_rmsnorm_gb300 import synth
+    dt = synth.storage_dtype(shape.expert)
+    E, p, I = shape.E, shape.p, shape.I
+    out = {"w_gate": torch.empty((E, I, p), dtype=dt, device="cuda"),
+           "w_up": torch.empty((E, I, p), dtype=dt, device="cuda"),
+           "w_down": torch.empty((E, p, I), dtype=dt, device="cuda")}
+    for e in range(E):
+        m = synth.make_expert(shape, seed, e, "cuda")
+        for k in out:
+            out[k][e].copy_(m[k])
+    return out
+
+
+def workload_line(shape, runner, steps, warmup, world, peaks, peak_src, local, replay=False):
+    """Throughput, stage times and roofline of one more workload (not the headline)."""
+    import torch
+    t0 = time.perf_counter()
+    for _ in range(2):
+        runner.forward()
+    torch.cuda.synchronize()
+    est_ms = (time.perf_counter() - t0) * 1e3 / 2
+    steps = max(steps, min(2000, int(WORKLOAD_MIN_MS / max(est_ms, 1e-3)) + 1))
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    elapsed, stage_ms = runner.time(steps, warmup, world, replay=replay)
+    clocks = sampler.stop()
+    T = shape.T
+    roof, tfl, gbs = roofline_of(shape, T, stage_ms, runner.touched(), elapsed / 1e3, peaks,
+                                 peak_src, shape.name)
+    return {"workload": describe(shape, runner.out_kind) + (" (routing replayed: ids and "
+                                                            "weights passed in)" if replay else ""),
+            "tokens_per_s": round(T * steps * world / (elapsed / 1e3), 1),
+            "ms_per_step": round(elapsed / steps, 4), "steps": steps, "warmup": warmup,
+            "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+            "stages_tflops": {k: round(v, 1) for k, v in tfl.items()},
+            "stages_gbs": {k: round(v, 1) for k, v in gbs.items()},
+            "roofline": roof, "gpu_launches": runner.layer.launches(T, not replay) * steps,
+            "clocks": clocks}
+
+
+def describe(shape, out_kind):
+    return (f"{shape.name}: T={shape.T} d={shape.d} p={shape.p} E={shape.E} "
+            f"top_k={shape.top_k} I={shape.I} act={shape.act} expert={shape.expert} "
+            f"out={out_kind}")
+
+
+# the other workloads reported beside the headline (BF16 prefill chunk), in order; the
+# replay entry runs the prefill chunk with routing passed in
+EXTRA_WORKLOADS = ("decode_bf16", "skewed_bf16", "prefill_nvfp4", "decode_nvfp4", "replay")
+# each extra workload's timed region is at least this long (more steps for short ones),
+# so the clock sampler sees it under load
+WORKLOAD_MIN_MS = 500.0
+
 
 def run_ours(args):
     import torch
     import torch.distributed as dist
 
     from latent_moe_layer_rmsnorm_gb300 import build, synth
-    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,63 +481,16 @@ def run_ours(args):
         dist.barrier()
     shape = synth.WORKLOADS[args.workload]
     seed = rank_seed(args.seed, rank)
-    inp = synth.make_inputs(shape, seed=seed, device="cuda")
-    out_kind = "bf16" if shape.act == "bf16" else "f32"
-    layer = LatentMoE(shape, inp, out=out_kind, keep_canonical=False)
-    del inp["w_gate"], inp["w_up"]
-    if shape.expert == "nvfp4":
-        del inp["w_down"]           # the NVFP4 codes replace the BF16 expert weights
-    x = inp["x"]
+    experts = make_experts(shape, seed)
+    run = Runner(shape, seed, experts)
+    layer, x, out, stream = run.layer, run.x, run.out, run.stream
     T = shape.T
-    out = torch.empty((T, shape.d), dtype=layer.out_dtype(), device="cuda")
-    stream = torch.cuda.current_stream()
-    from latent_moe_layer_rmsnorm_gb300 import _lib as nst
-    n_stages = nst.moe_num_stages()
-    stage_names = [nst.moe_stage_name(i) for i in range(n_stages)]
+    n_touched = run.touched()
 
-    def make_events(n):
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        for e in evs:
-            e.record(stream)           # create the handles; re-recorded by the library
-        return evs
-
-    for _ in range(args.warmup):
-        layer.forward(x, out=out)
-    ids_probe, _ = layer.route(x)       # experts this batch touches (for the byte count)
-    n_touched = int(torch.unique(ids_probe).numel())
-    del ids_probe
-    torch.cuda.synchronize()
-    st = layer.read_status()
-    if st != (0, 0):
-        raise SystemExit(f"device status after warm-up: {st}")
-
-    # timed region: K steps, stage events recorded between the kernels
-    step_events = [make_events(n_stages + 1) for _ in range(args.steps)]
-    torch.cuda.synchronize()
+    # ---- timed region: K steps, stage events recorded between the kernels ---------------
     sampler = ClockSampler(local)
     time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for k in range(args.steps):
-        layer.forward(x, out=out, events=[e.cuda_event for e in step_events[k]])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), "cuda")
-    st = layer.read_status()
-    if st != (0, 0):
-        raise SystemExit(f"device status after the timed steps: {st}")
-
-    stage_ms = {n: 0.0 for n in stage_names}
-    for evs in step_events:
-        for i, n in enumerate(stage_names):
-            stage_ms[n] += evs[i].elapsed_time(evs[i + 1]) / args.steps
-
+    elapsed_ms, stage_ms = run.time(args.steps, args.warmup, world)
     ms_per_step = elapsed_ms / args.steps
     tokens = T * args.steps * world
     value = tokens / (elapsed_ms / 1e3)
@@ -413,69 +588,44 @@ def run_ours(args):
                     "bytes": b_bytes}
         del xo, hn
 
+    # ---- roofline of the dominant kernel -------------------------------------------------
+    peaks, peak_src = load_peaks()
+    roofline, stage_tflops, stage_gbs = roofline_of(shape, T, stage_ms, n_touched,
+                                                    elapsed_ms / 1e3, peaks, peak_src,
+                                                    args.workload)
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    out_kind = run.out_kind
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline_from_gpu_inputs(shape, layer, x, seed)
+
+    # ---- the other workloads, each on its own layer (the headline's is freed first) ------
+    workloads = {}
+    if not args.no_workloads and shape.name == "prefill_bf16":
+        workloads["replay_prefill_bf16"] = workload_line(shape, run, args.steps, args.warmup,
+                                                         world, peaks, peak_src, local,
+                                                         replay=True)
+    launches = layer.launches(T) * args.steps
+    if workloads:
+        del run, layer, x, out
+        torch.cuda.empty_cache()
+        for name in EXTRA_WORKLOADS:
+            if name == "replay":
+                continue
+            sh = synth.WORKLOADS[name]
+            r = Runner(sh, seed, experts)
+            workloads[name] = workload_line(sh, r, args.steps, args.warmup, world, peaks,
+                                            peak_src, local)
+            del r
+            torch.cuda.empty_cache()
+
     if rank != 0:
         if world > 1:
             dist.barrier()
             dist.destroy_process_group()
         return
 
-    # ---- roofline of the dominant kernel -------------------------------------------------
-    peaks, peak_src = load_peaks()
-    fl = flops_per_token(shape)
-    by = bytes_per_token(shape)
-    stage_tflops = {n: fl[n] * T / (stage_ms[n] / 1e3) / 1e12 for n in fl if stage_ms.get(n)}
-    stage_gbs = {n: by[n] * T / (stage_ms[n] / 1e3) / 1e9 for n in by if stage_ms.get(n)}
-    gb = expert_gemm_bytes(shape, n_touched, T)
-    for n, b in projection_bytes(shape, T).items():   # weight streams at decode sizes
-        if stage_ms.get(n):
-            stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9
-    for n, b in gb.items():
-        if stage_ms.get(n):
-            stage_gbs[n] = b / (stage_ms[n] / 1e3) / 1e9
-    dominant = max(fl, key=lambda n: stage_ms.get(n, 0.0))
-    bf16_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    bf16_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    traffic = recorded_traffic(args.workload, dominant)
-    if shape.expert == "nvfp4" and dominant.startswith("gemm"):
-        # a contraction takes the peak of its own dtype: dense FP4 = 6 x dense BF16
-        # (nominal 13.5 vs 2.25 PFLOP/s), applied to the measured BF16 figure
-        peak = bf16_peak * FP4_PER_BF16
-        kind = (f"nvfp4 = {FP4_PER_BF16:g} x bf16_tflops_sustained ({peak_src}, nominal "
-                f"ratio); the kernel runs inside a {ms_per_step:.1f} ms step")
-    else:
-        peak = bf16_peak
-        kind = (f"bf16_tflops_sustained ({peak_src}); the kernel runs inside a "
-                f"{ms_per_step:.1f} ms step, back to back")
-    flops_launch = fl[dominant] * T
-    bytes_launch = gb.get(dominant)
-    ridge = peak * 1e12 / (hbm_peak * 1e9)          # FLOP per byte where the two bounds meet
-    intensity = flops_launch / bytes_launch if bytes_launch else None
-    if intensity is not None and intensity < ridge:
-        # too few rows per expert to reuse a weight tile: the launch streams the weights
-        achieved = stage_gbs[dominant]
-        roofline = {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
-                    "peak": round(hbm_peak, 1), "unit": "GB/s",
-                    "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
-                    "peak_kind": f"hbm_gbs ({peak_src}, copy bandwidth)",
-                    "bytes_per_launch": bytes_launch, "flops_per_launch": flops_launch,
-                    "experts_touched": n_touched,
-                    "intensity_flop_per_byte": round(intensity, 2), "ridge": round(ridge, 1),
-                    "tensor_tflops": round(stage_tflops[dominant], 1)}
-    else:
-        achieved = stage_tflops[dominant]
-        roofline = {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 1),
-                    "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "traffic": traffic, "peak_kind": kind, "flops_per_launch": flops_launch,
-                    "bytes_per_launch": bytes_launch, "experts_touched": n_touched,
-                    "intensity_flop_per_byte": round(intensity, 1) if intensity else None,
-                    "ridge": round(ridge, 1), "peak_burst_bf16": bf16_burst}
-
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline_from_gpu_inputs(shape, layer, x, seed)
-
-    launches = layer.launches(T) * args.steps
     dtype = "bf16+fp16" if shape.act == "bf16" else "f32(tf32)"
     if shape.expert == "nvfp4":
         dtype = "nvfp4 experts, bf16+fp16 projections"
@@ -496,6 +646,8 @@ def run_ours(args):
         "hbm_peak_gbs": hbm_peak,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
+    if workloads:
+        line["workloads"] = workloads
     if boundary is not None:
         # not part of the step: the pass that follows the block (moe_boundary), timed alone
         hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))

@@ -373,6 +373,22 @@ def route(inp: dict, *, top_k: int, eps: float, tokens=None):
     return ids, w, logits
 
 
+def expert_input(inp: dict, *, eps: float, tokens=None, h=None):
+    """The NVFP4 experts' input before quantisation, on the BF16 chain: h = RMSNorm(x),
+    stored FP16 for the pooler; pooled = W_pool h (FP16 weights), stored FP32; u32 =
+    RMSNorm_{g_pool}(pooled) rounded to FP32, the value the activation quantiser reads.
+    Returns (h, pooled, u32) for the rows `tokens` (all if None); h may be given."""
+    st = storage_kinds("bf16", "bf16", "f32", True)
+    if h is None:
+        x = as_f64(inp["x"])
+        if tokens is not None:
+            x = x[np.asarray(tokens)]
+        h = rmsnorm(x, inp["g_in"], eps)
+    h_pool = _store(F.fp32(h), st["h_pool"])
+    pooled = _store(pool(h_pool, _store(as_f64(inp["w_pool"]), st["w_proj"])), st["pooled"])
+    return h, pooled, F.fp32(rmsnorm(pooled, inp["g_pool"], eps))
+
+
 def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts,
                    expert_map=None):
     """The block with NVFP4 experts; storage points as in the BF16 chain except the
@@ -390,9 +406,7 @@ def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts,
         ids = np.asarray(ids, dtype=np.int32)
         wts = as_f64(weights)
         top_k = ids.shape[1]
-    h_pool = _store(F.fp32(h), st["h_pool"])
-    pooled = _store(pool(h_pool, _store(as_f64(inp["w_pool"]), st["w_proj"])), st["pooled"])
-    u32 = F.fp32(rmsnorm(pooled, inp["g_pool"], eps))
+    _, pooled, u32 = expert_input(inp, eps=eps, h=h)
     qu, sfu, alpha = Q.quantize_rows(u32)
     u = Q.dequantize(qu, sfu, alpha)
     p = u.shape[1]

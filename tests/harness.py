@@ -83,3 +83,41 @@ def rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     ref = np.asarray(ref, dtype=np.float64)
     rms = float(np.sqrt(np.mean(ref * ref)))
     return float(np.max(np.abs(gpu - ref)) / max(rms, 1e-300))
+
+
+# ---- full-size inputs --------------------------------------------------------------------
+# Expert matrices are drawn on the CPU one expert at a time with the generator's
+# per-expert recipe (the draw the oracle's worker processes repeat) and kept on the GPU
+# for the session: the full-size tests share one expert set per (seed, widths, dtype).
+_EXPERTS = {}
+
+
+def gpu_experts(shape: synth.Shape, seed: int) -> dict:
+    key = (seed, shape.E, shape.p, shape.I, synth.storage_dtype(shape.expert))
+    if key not in _EXPERTS:
+        _EXPERTS.clear()
+        torch.cuda.empty_cache()
+        dt = synth.storage_dtype(shape.expert)
+        E, p, I = shape.E, shape.p, shape.I
+        out = {"w_gate": torch.empty((E, I, p), dtype=dt, device="cuda"),
+               "w_up": torch.empty((E, I, p), dtype=dt, device="cuda"),
+               "w_down": torch.empty((E, p, I), dtype=dt, device="cuda")}
+        for e in range(E):
+            m = synth.make_expert(shape, seed, e, "cpu")
+            for k in out:
+                out[k][e].copy_(m[k])
+        _EXPERTS[key] = out
+    return _EXPERTS[key]
+
+
+def fullsize_inputs(shape: synth.Shape, seed: int, expert_seed: int = 0):
+    """(host inputs without the expert matrices, device inputs with them).  The dense
+    inputs are drawn on the CPU and their router margins repaired there; the experts
+    come from gpu_experts(shape, expert_seed)."""
+    host = synth.make_dense(shape, seed, "cpu")
+    fix_margins(host, shape, seed=seed)
+    if shape.expert == "nvfp4":
+        host["gs_act2"] = synth.nvfp4_act2_scales(shape, "cpu")
+    dev = {k: v.cuda() for k, v in host.items()}
+    dev.update(gpu_experts(shape, expert_seed))
+    return host, dev

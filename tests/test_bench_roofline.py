@@ -55,3 +55,30 @@ def test_projection_bytes_at_decode_are_the_weights():
     assert b["router"] == 256 * 8192 * 4 + 64 * 8192 * 4 + 64 * 8 * 8
     # at 64 tokens the weights are more than 95 % of each projection's bytes
     assert 4096 * 8192 * 2 / b["pool"] > 0.95
+
+
+def test_peak_follows_the_timed_region():
+    """A kernel timed in a region shorter than SUSTAINED_MIN_S runs at the boost clock
+    and is measured against the burst BF16 peak; a region of at least that long, against
+    the sustained one.  NVFP4 GEMMs take the nominal FP4/BF16 ratio of either."""
+    peaks = {"bf16_tflops": 1876.1, "bf16_tflops_sustained": 1706.8, "hbm_gbs": 6778.7}
+    p, why = bench.tensor_peak(peaks, "measured", 0.24, nvfp4=False)
+    assert p == 1876.1 and "bf16_tflops (" in why
+    p, why = bench.tensor_peak(peaks, "measured", bench.SUSTAINED_MIN_S, nvfp4=False)
+    assert p == 1706.8 and "sustained" in why
+    p, why = bench.tensor_peak(peaks, "measured", 0.5, nvfp4=True)
+    assert p == 1876.1 * bench.FP4_PER_BF16 and "measured FP4 MMA issue rate" in why
+
+
+def test_roofline_frac_is_achieved_over_peak():
+    """The line's frac is reproducible from its own achieved and peak."""
+    s = synth.PREFILL_BF16
+    stage_ms = {"norm": 0.2, "router": 0.14, "pool": 0.65, "dispatch": 0.26,
+                "gemm1_gate_up_swiglu": 6.6, "gemm2_down": 3.2, "combine": 0.33, "unpool": 0.64}
+    peaks = {"bf16_tflops": 1876.1, "bf16_tflops_sustained": 1706.8, "hbm_gbs": 6778.7}
+    roof, tfl, _ = bench.roofline_of(s, s.T, stage_ms, 256, 0.25, peaks, "measured", "x")
+    assert roof["bound"] == "tensor" and roof["kernel"] == "gemm1_gate_up_swiglu"
+    assert roof["peak"] == 1876.1
+    assert abs(roof["frac"] - roof["achieved"] / roof["peak"]) < 1e-3
+    fl = bench.flops_per_token(s)["gemm1_gate_up_swiglu"] * s.T
+    assert abs(roof["achieved"] - fl / 6.6e-3 / 1e12) < 0.1

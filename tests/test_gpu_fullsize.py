@@ -3,24 +3,31 @@ times (one moe_forward over the whole batch).
 
 * prefill chunk (T=16384, d=8192, p=4096, E=256, k=8, I=4096, BF16): expert ids of
   ALL tokens exactly (router margins >= 1e-3 after redraws), route weights, and the
-  full output of sampled tokens (the oracle computes them one by one; rows are
-  independent), including tokens routed to the busiest and the rarest expert.
+  full output of 256 sampled tokens (the oracle computes them one by one, rows being
+  independent): spread over the batch, plus tokens routed to the busiest and to the
+  rarest expert.
 * decode batch (T=64, same widths): every token in full.
+* skewed routing (T=8192): ids of all tokens; 256 sampled tokens including the busiest
+  expert's first and last rows and the least-loaded non-empty expert's.
 
 Bound: max|gpu - ref| / rms(ref) <= 1e-2 (BF16 storage; the rounding-chain oracle).
+The oracle's per-expert steps run in worker processes (tests/oracle_pool.py).
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from harness import fix_margins, oracle_view, rel_err, to_np
+import oracle_pool
+from harness import fullsize_inputs, oracle_view, rel_err, to_np
 from latent_moe_layer_rmsnorm_gb300 import synth
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 TOL = 1e-2
 TOL_W = 5e-4
+EXPERT_SEED = 0          # one expert set for every full-size test (drawn once per session)
+SAMPLE = 256
 
 
 def need_gpu():
@@ -32,79 +39,90 @@ def need_gpu():
 
 def run_full(shape, seed):
     from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
-    inp = synth.make_inputs(shape, seed=seed, device="cuda")
-    fix_margins(inp, shape, seed=seed)
-    layer = LatentMoE(shape, inp, out="f32")
-    out = layer.forward(inp["x"])
-    ids, w = layer.route(inp["x"])
+    host, dev = fullsize_inputs(shape, seed, EXPERT_SEED)
+    layer = LatentMoE(shape, dev, out="f32", keep_canonical=False)
+    out = layer.forward(dev["x"])
+    ids, w = layer.route(dev["x"])
     torch.cuda.synchronize()
     assert layer.read_status() == (0, 0)
-    return inp, layer, out, ids.cpu().numpy(), to_np(w)
+    return host, layer, out, ids.cpu().numpy(), to_np(w)
 
 
-def oracle_rows(inp, shape, tokens):
-    view = oracle_view(inp, lazy=True)
-    return oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act=shape.act,
-                              expert=shape.expert, out="f32", chain=True, tokens=tokens,
-                              return_parts=True)
+def all_routes(host, shape):
+    h = oracle.rmsnorm(to_np(host["x"]), to_np(host["g_in"]), shape.eps)
+    return oracle.topk_route(oracle.router_logits(h, to_np(host["w_router"])), shape.top_k)
+
+
+def sample_tokens(ids: np.ndarray, n: int, E: int) -> list:
+    """n tokens: the first and last 4 rows of the busiest expert, up to 8 rows of the
+    least-loaded non-empty expert, the rest spread evenly over the batch."""
+    T = ids.shape[0]
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    busiest = int(np.argmax(counts))
+    nonempty = np.nonzero(counts)[0]
+    rarest = int(nonempty[np.argmin(counts[nonempty])])
+    tb = np.nonzero((ids == busiest).any(1))[0]
+    tr = np.nonzero((ids == rarest).any(1))[0]
+    out = set(tb[:4].tolist() + tb[-4:].tolist() + tr[:8].tolist())
+    for t in np.linspace(0, T - 1, n).round().astype(int).tolist():
+        if len(out) >= n:
+            break
+        out.add(t)
+    t = 0
+    while len(out) < n:          # fill up (a spread point may repeat an extreme's row)
+        out.add(t)
+        t += 1
+    return sorted(out)
+
+
+def compare(layer, host, shape, out, ids, tok, label):
+    view = oracle_view(host)
+    emap = oracle_pool.ExpertMap(shape, EXPERT_SEED)
+    ref = oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act=shape.act,
+                             expert=shape.expert, out="f32", chain=True, tokens=tok,
+                             return_parts=True, expert_map=emap)
+    np.testing.assert_array_equal(ref["ids"], ids[tok])
+    sel = torch.as_tensor(tok, device=out.device)
+    err = rel_err(to_np(out[sel]), ref["out"])
+    c_err = rel_err(to_np(layer.intermediate("c", shape.T)[sel]), ref["c"])
+    per_tok = np.max(np.abs(to_np(out[sel]) - ref["out"]), axis=1) / np.sqrt(np.mean(ref["out"] ** 2))
+    print(f"{label}: {len(tok)} sampled tokens, out err {err:.2e} (median token "
+          f"{np.median(per_tok):.2e}), c err {c_err:.2e}")
+    assert err <= TOL
 
 
 def test_prefill_chunk():
     need_gpu()
     shape = synth.PREFILL_BF16
-    inp, layer, out, ids, w = run_full(shape, seed=0)
-    # routing of every token
-    x = to_np(inp["x"])
-    h = oracle.rmsnorm(x, to_np(inp["g_in"]), shape.eps)
-    logits = oracle.router_logits(h, to_np(inp["w_router"]))
-    del x, h
-    rid, rw = oracle.topk_route(logits, shape.top_k)
+    host, layer, out, ids, w = run_full(shape, seed=0)
+    rid, rw = all_routes(host, shape)
     np.testing.assert_array_equal(ids, rid)
     np.testing.assert_allclose(w, rw, rtol=0, atol=TOL_W)
     counts = np.bincount(ids.reshape(-1), minlength=shape.E)
-    busiest, rarest = int(np.argmax(counts)), int(np.argmin(counts))
     print("expert load: mean", counts.mean(), "max", counts.max(), "min", counts.min())
-    # sampled tokens, spread over the batch and the M tiles, plus the extremes
-    tok = [0, 1, 127, 128, 5000, 9999, 16383]
-    tok.append(int(np.nonzero((ids == busiest).any(1))[0][0]))
-    tok.append(int(np.nonzero((ids == rarest).any(1))[0][-1]))
-    tok = sorted(set(tok))
-    ref = oracle_rows(inp, shape, tok)
-    np.testing.assert_array_equal(ref["ids"], ids[tok])
-    got = to_np(out[torch.as_tensor(tok, device=out.device)])
-    err = rel_err(got, ref["out"])
-    c_gpu = to_np(layer.intermediate("c", shape.T)[torch.as_tensor(tok, device=out.device)])
-    c_err = rel_err(c_gpu, ref["c"])
-    print(f"prefill sampled tokens {tok}: out err {err:.2e}, c err {c_err:.2e}")
-    assert err <= TOL
+    tok = sample_tokens(ids, SAMPLE, shape.E)
+    assert len(tok) >= SAMPLE
+    compare(layer, host, shape, out, ids, tok, "prefill")
 
 
 def test_decode_batch():
     need_gpu()
     shape = synth.DECODE_BF16
-    inp, layer, out, ids, w = run_full(shape, seed=1)
-    tok = list(range(shape.T))
-    ref = oracle_rows(inp, shape, tok)
-    np.testing.assert_array_equal(ids, ref["ids"])
-    np.testing.assert_allclose(w, ref["w"], rtol=0, atol=TOL_W)
-    err = rel_err(to_np(out), ref["out"])
-    touched = len(np.unique(ids))
-    print(f"decode: {touched} experts touched, out err {err:.2e}")
-    assert err <= TOL
+    host, layer, out, ids, w = run_full(shape, seed=1)
+    rid, rw = all_routes(host, shape)
+    np.testing.assert_array_equal(ids, rid)
+    np.testing.assert_allclose(w, rw, rtol=0, atol=TOL_W)
+    print(f"decode: {len(np.unique(ids))} experts touched")
+    compare(layer, host, shape, out, ids, list(range(shape.T)), "decode")
 
 
 def test_skewed_routing():
     """Zipf-skewed routing (T=8192): the busiest expert spans tens of 128-row tiles,
-    many experts are empty.  Ids of all tokens exactly; sampled tokens in full,
-    including tokens of the busiest and of the least-loaded non-empty expert."""
+    many experts are empty."""
     need_gpu()
     shape = synth.SKEWED_BF16
-    inp, layer, out, ids, w = run_full(shape, seed=2)
-    x = to_np(inp["x"])
-    h = oracle.rmsnorm(x, to_np(inp["g_in"]), shape.eps)
-    logits = oracle.router_logits(h, to_np(inp["w_router"]))
-    del x, h
-    rid, rw = oracle.topk_route(logits, shape.top_k)
+    host, layer, out, ids, w = run_full(shape, seed=2)
+    rid, rw = all_routes(host, shape)
     np.testing.assert_array_equal(ids, rid)
     np.testing.assert_allclose(w, rw, rtol=0, atol=TOL_W)
     counts = np.bincount(ids.reshape(-1), minlength=shape.E)
@@ -112,15 +130,56 @@ def test_skewed_routing():
     empty = float(np.mean(counts == 0))
     print(f"skewed load: max/mean {ratio:.1f}, empty experts {empty:.2f}")
     assert ratio >= 10 and empty >= 0.05
-    busiest = int(np.argmax(counts))
-    nonempty = np.nonzero(counts)[0]
-    rarest = int(nonempty[np.argmin(counts[nonempty])])
-    tok = [0, 4095, 8191]
-    tok += [int(t) for t in np.nonzero((ids == busiest).any(1))[0][[0, -1]]]
-    tok.append(int(np.nonzero((ids == rarest).any(1))[0][0]))
-    tok = sorted(set(tok))
-    ref = oracle_rows(inp, shape, tok)
-    got = to_np(out[torch.as_tensor(tok, device=out.device)])
-    err = rel_err(got, ref["out"])
-    print(f"skewed sampled tokens {tok}: out err {err:.2e}")
+    tok = sample_tokens(ids, SAMPLE, shape.E)
+    compare(layer, host, shape, out, ids, tok, "skewed")
+
+
+def zipf_routes(T: int, E: int, k: int, s: float, seed: int):
+    """External routes for T tokens: k distinct experts per token drawn without
+    replacement from a Zipf(s) popularity over a seeded permutation of the expert ids
+    (Gumbel top-k on the log probabilities), with positive weights that sum to 1.  The
+    ordering within a token is by weight, largest first."""
+    rng = np.random.default_rng(seed)
+    rank = rng.permutation(E) + 1
+    logp = -s * np.log(rank.astype(np.float64))
+    g = logp[None, :] + rng.gumbel(size=(T, E))
+    ids = np.argsort(-g, axis=1)[:, :k].astype(np.int32)
+    w = rng.dirichlet(np.ones(k), size=T)
+    w = -np.sort(-w, axis=1)
+    return ids, w.astype(np.float32)
+
+
+def test_routing_replay_and_external_routes_at_scale():
+    """The prefill chunk with routing passed in ("vLLM 对 Muse Spark Open 的 Day 0 支持",
+    section "vLLM 中的强化学习": rollout routing replay): the router's own ids and
+    weights replayed give bit-identical output; Zipf-skewed external routes (no token's
+    experts from the router) match the oracle on 64 sampled tokens, including the
+    most- and least-loaded experts' tokens, and are deterministic."""
+    need_gpu()
+    shape = synth.PREFILL_BF16
+    host, layer, out, ids, w = run_full(shape, seed=0)
+    dev_x = host["x"].cuda()
+    ids_t = torch.as_tensor(ids, device="cuda")
+    w_t = torch.as_tensor(w, device="cuda")
+    rep = layer.forward(dev_x, ids=ids_t, w=w_t)
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    assert torch.equal(rep, out)
+    ext_ids, ext_w = zipf_routes(shape.T, shape.E, shape.top_k, 1.2, seed=99)
+    ei, ew = torch.as_tensor(ext_ids, device="cuda"), torch.as_tensor(ext_w, device="cuda")
+    a = layer.forward(dev_x, ids=ei, w=ew).clone()
+    b = layer.forward(dev_x, ids=ei, w=ew)
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    assert torch.equal(a, b)
+    counts = np.bincount(ext_ids.reshape(-1), minlength=shape.E)
+    print(f"external routes: busiest expert {counts.max()} rows ({counts.max() / counts.mean():.1f}x "
+          f"mean), {int(np.sum(counts == 0))} experts empty")
+    tok = sample_tokens(ext_ids, 64, shape.E)
+    view = oracle_view(host)
+    ref = oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act="bf16", expert="bf16",
+                             out="f32", chain=True, tokens=tok, ids=ext_ids[tok],
+                             weights=ext_w[tok], expert_map=oracle_pool.ExpertMap(shape, EXPERT_SEED))
+    err = rel_err(to_np(a[torch.as_tensor(tok, device="cuda")]), ref)
+    print(f"external routes: {len(tok)} sampled tokens, out err {err:.2e}")
     assert err <= TOL

@@ -174,28 +174,3 @@ def test_nvfp4_stages_and_layer(shape):
     print(f"nvfp4: u codes {code_match:.4f} equal, s codes {s_match / s_total:.4f} equal, "
           f"y {y_err:.1e}, end to end {e2e:.2e}")
     assert e2e <= TOL_NVFP4
-
-
-@pytest.mark.slow
-def test_nvfp4_prefill_chunk_sampled():
-    """The NVFP4 prefill chunk at full size: ids of all tokens exactly, sampled tokens in
-    full against the NVFP4 oracle."""
-    need_gpu()
-    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
-    shape = synth.PREFILL_NVFP4
-    inp = synth.make_inputs(shape, seed=3, device="cuda")
-    fix_margins(inp, shape, seed=3)
-    layer = LatentMoE(shape, inp, out="f32")
-    out = layer.forward(inp["x"])
-    ids, _ = layer.route(inp["x"])
-    torch.cuda.synchronize()
-    assert layer.read_status() == (0, 0)
-    tok = [0, 4097, 9000, 16383]
-    view = oracle_view(inp, lazy=True)
-    ref = oracle.moe_forward(view, top_k=shape.top_k, eps=shape.eps, act="bf16",
-                             expert="nvfp4", out="f32", tokens=tok, return_parts=True)
-    np.testing.assert_array_equal(ids.cpu().numpy()[tok], ref["ids"])
-    err = rel_err(to_np(out[torch.as_tensor(tok, device=out.device)]), ref["out"])
-    print(f"nvfp4 prefill sampled {tok}: {err:.2e}")
-    assert err <= TOL_NVFP4
-
