@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--nvfp4-pair", action="store_true",
+                    help="NVFP4 expert GEMMs on CTA pairs (MOE_FLAG_NVFP4_PAIR)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="time only the headline workload")
     ap.add_argument("--no-boundary", action="store_true",
@@ -320,7 +322,7 @@ def roofline_of(shape, T, stage_ms, n_touched, timed_s, peaks, peak_src, workloa
 class Runner:
     """One latent-MoE layer of a workload, with its inputs resident on the device."""
 
-    def __init__(self, shape, seed, experts=None):
+    def __init__(self, shape, seed, experts=None, flags=0):
         import torch
 
         from latent_moe_layer_rmsnorm_gb300 import synth
@@ -339,9 +341,11 @@ class Runner:
         self.out = torch.empty((shape.T, shape.d), dtype=self.layer.out_dtype(), device="cuda")
         self.stream = torch.cuda.current_stream()
         self.stage_names = [nst.moe_stage_name(i) for i in range(nst.moe_num_stages())]
+        self.flags = flags
 
     def forward(self, ids=None, w=None, events=None):
-        return self.layer.forward(self.x, ids=ids, w=w, out=self.out, events=events)
+        return self.layer.forward(self.x, ids=ids, w=w, out=self.out, events=events,
+                                  flags=self.flags)
 
     def touched(self):
         import torch
@@ -482,7 +486,9 @@ def run_ours(args):
     shape = synth.WORKLOADS[args.workload]
     seed = rank_seed(args.seed, rank)
     experts = make_experts(shape, seed)
-    run = Runner(shape, seed, experts)
+    from latent_moe_layer_rmsnorm_gb300 import _lib as nst
+    run_flags = nst.MOE_FLAG_NVFP4_PAIR if args.nvfp4_pair else 0
+    run = Runner(shape, seed, experts, run_flags)
     layer, x, out, stream = run.layer, run.x, run.out, run.stream
     T = shape.T
     n_touched = run.touched()
@@ -614,7 +620,7 @@ def run_ours(args):
             if name == "replay":
                 continue
             sh = synth.WORKLOADS[name]
-            r = Runner(sh, seed, experts)
+            r = Runner(sh, seed, experts, run_flags)
             workloads[name] = workload_line(sh, r, args.steps, args.warmup, world, peaks,
                                             peak_src, local)
             del r

@@ -56,7 +56,7 @@ typedef enum {
   MOE_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small          */
   MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed                */
   MOE_ERR_TIMEOUT = 5,       /* device: a pipeline wait ran past its time limit     */
-  MOE_ERR_DEVICE_CHECK = 6   /* device: an index check failed                       */
+  MOE_ERR_DEVICE_CHECK = 6   /* device: an index or value-range check failed        */
 } moe_status_t;
 
 typedef enum {
@@ -78,7 +78,8 @@ typedef enum {
  *   expert MOE_BF16 or MOE_F32 (equal to act), or MOE_NVFP4 with act = MOE_BF16
  *          (then p and I must be multiples of 256)
  *   out    MOE_BF16 or MOE_F32: dtype of the layer output
- *   flags  0, MOE_FLAG_TEST_TIMEOUT, MOE_FLAG_WEIGHT_TILES (other bits must be zero) */
+ *   flags  0 or MOE_FLAG_TEST_TIMEOUT, MOE_FLAG_WEIGHT_TILES, MOE_FLAG_NVFP4_PAIR
+ *          (other bits must be zero) */
 /* Test hook for the error path: the gate/up GEMM never issues its first operand load,
  * so its MMA wait runs out after 20 ms; the call's kernels then end early and
  * moe_read_status reports MOE_ERR_TIMEOUT.  Outputs are undefined.  Tests only. */
@@ -89,6 +90,12 @@ typedef enum {
  * tile of each expert, but on a GB300 the expert GEMMs are bound by operand delivery
  * into shared memory, not by MMA work, and the default is faster at prefill sizes. */
 #define MOE_FLAG_WEIGHT_TILES 0x40000000u
+/* NVFP4 experts: run the expert GEMMs on CTA pairs over 256 x 256 output tiles (each
+ * CTA of a pair stages half of the weight tile, so fewer bytes per MAC reach its shared
+ * memory) instead of the default one CTA per 128 x 256 tile.  Same results, bit for bit;
+ * on a GB300 the pairs measure about half as fast (their per-stage hand-off of the block
+ * scales between the two CTAs limits them), so they are not the default. */
+#define MOE_FLAG_NVFP4_PAIR 0x20000000u
 typedef struct {
   int32_t T, d, p, E, top_k, I;
   float eps;
@@ -103,15 +110,18 @@ typedef struct {
  *   w_pool    [p,d]      packed: FP16 (BF16 configs) or TF32-rounded FP32
  *   g_pool    [p]        FP32 gain of the pooled-input norm
  *   w13       packed gate/up rows of every expert: FP16 or TF32-rounded FP32
- *   w2        [E,p,I]    down projections: the BF16 checkpoint tensor as given, or (FP32
- *                        configs) a packed TF32-rounded copy
+ *   w2        [E,p,I]    packed down projections: FP16 or TF32-rounded FP32
  *   g_exp     [E,p]      FP32 per-expert output-norm gains
  *   w_unpool  [d,p]      packed: FP16 or TF32-rounded FP32
- * BF16 configurations run the pooler, gate/up and unpooler GEMMs on FP16 operands: the
- * activations they read (h, u, c) are RMS-normalised, hence bounded by
- * sqrt(width) * max|gain|, and FP16 keeps 3 more significand bits than BF16 at the same
- * tensor-core rate.  The down GEMM reads s = silu(a) * b, which has no such bound, in
- * BF16.  The BF16 -> FP16 weight copies are exact for |w| >= 2^-17.                   */
+ * BF16 configurations run every GEMM on FP16 operands and store every activation between
+ * the GEMMs (h, u, s, y, c) in FP16: FP16 keeps 3 more significand bits than BF16 at the
+ * same size and tensor-core rate, which keeps the rounding flips that FP32 accumulation
+ * noise causes at storage points 8x rarer and 8x smaller.  h, u and c are RMS-normalised,
+ * hence bounded by sqrt(width) * max|gain|; s and y are not bounded by construction.  The
+ * BF16 -> FP16 weight copies are exact for |w| >= 2^-17.  A value of h, u or c that would
+ * not fit FP16 (gains of extreme size, replayed weights with a large absolute sum), or an
+ * s or y that overflowed it (and so made c non-finite), is reported through
+ * moe_read_status (MOE_ERR_DEVICE_CHECK).                                            */
 typedef struct {
   const float* g_in;
   const float* w_router;
@@ -177,7 +187,7 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which);
  *    256-row tile of the gate/up GEMM holds gate rows i..i+G and the matching up rows;
  *    converted to FP16 (BF16 configs) or rounded to TF32 (FP32 configs).
  *  - w_pool_out, w_unpool_out: FP16 copies (BF16 configs) or TF32-rounded copies.
- *  - w2_out: FP32 configs only, a TF32-rounded copy; pass NULL for BF16 configs.
+ *  - w2_out: FP16 copy (BF16 configs) or TF32-rounded copy (FP32 configs).
  *  - NVFP4 configs: w13_out and w2_out must be NULL (moe_quantize_nvfp4 writes them);
  *    src->w_gate / w_up / w_down are not read.
  * Output buffers are caller-allocated with moe_packed_bytes; none may alias a source. */
@@ -208,23 +218,31 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_weights_t* W, const vo
 /* moe_route for callers that cannot allocate device memory at all -- code running where
  * no allocator is reachable, such as an engine that reserves all of its memory at start-up,
  * a plugin host that forbids device allocations, or a replayed CUDA graph that must not
- * grow its memory pool.  It takes no workspace: its scratch (status word, h32 and h16)
- * lives in a fixed 12 MiB + 256 B array inside the library, which every GPU that loads the
- * library holds until the process exits.  The pages describe nothing like it; it is an
- * addition of this library.
+ * grow its memory pool.  It takes no workspace: its scratch (status word, h32 and the
+ * router's split-K partial logits) lives in a fixed 12 MiB + 256 B array inside the
+ * library, which every GPU that loads the library holds until the process exits.  The
+ * pages describe nothing like it; it is an addition of this library.
  *   Same arguments and results as moe_route, minus the workspace.
  *   Limit: T * d <= 2^21 (e.g. T <= 256 at d = 8192); larger calls return
- *   MOE_ERR_WORKSPACE before anything is launched.
+ *   MOE_ERR_WORKSPACE before anything is launched.  Small T splits the router's
+ *   reduction over up to 32 slices (as moe_route does), as many as 4 MiB of partial
+ *   logits allow, so a decode batch does not stream the router weights through one CTA.
  *   The first call on a device looks up the array's device address (once per device,
  *   with that device current); make that first call before any stream capture.
  *   No cudaMalloc, cudaFree or allocating library routine is called.
  *   All calls share the one array, which keeps the previous call's contents (each call
  *   clears the status word it needs at zero): calls that overlap on the GPU -- on
  *   different streams, or from different threads -- race, so serialise them.
- *   Device-side wait failures of these calls are recorded only in the array's status
- *   word, which moe_read_status cannot reach. */
+ *   Device-side failures of these calls are recorded in the array's status word:
+ *   moe_read_noalloc_status reads it. */
 moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
                                int32_t* ids, float* w, moe_stream_t stream);
+
+/* The device-side status of the moe_route_noalloc calls on the current device since the
+ * last read, like moe_read_status: synchronises `stream`, returns MOE_OK, MOE_ERR_TIMEOUT
+ * or MOE_ERR_DEVICE_CHECK, writes the detail code to *detail (may be NULL) and clears
+ * the status.  Allocates nothing. */
+moe_status_t moe_read_noalloc_status(moe_stream_t stream, int32_t* detail);
 
 /* The whole block for T tokens.
  *   x    [T,d] act dtype (device)
@@ -260,7 +278,7 @@ moe_status_t moe_boundary(const moe_config_t* cfg, const void* x, const void* y,
                           const float* g_post, const float* gate, const float* g_next,
                           void* x_out, void* h_next, moe_stream_t stream);
 
-/* moe_forward with CUDA events recorded on `stream` at each stage boundary:/* moe_forward with CUDA events recorded on `stream` at each stage boundary:
+/* moe_forward with CUDA events recorded on `stream` at each stage boundary:
  * events[0] before the first kernel and events[i] after stage i-1 (i = 1..n_events-1,
  * at most moe_num_stages()+1 events).  For measurement only; same results. */
 moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* W,
@@ -280,19 +298,31 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally);
  *   0 h32 [T,d] FP32 (TF32-rounded)   1 h16 [T,d] FP16     2 ids [T,k] int32
  *   3 w [T,k] FP32                    4 pooled [T,p] FP32   5 row_off [E+1] int32
  *   6 src [T*k] int32 (dispatched row -> t*k+j)              7 inv [T*k] int32
- *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (BF16 / FP32)
- *  10 y [T*k,p] (BF16 / FP32: FP32 for FP32 experts only)
+ *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (FP16 / FP32)
+ *  10 y [T*k,p] (FP16 / FP32: FP32 for FP32 experts only)
  *  11 c [T,p] (FP16 / FP32)
  * NVFP4 configs: dispatched rows start at a 128-row boundary per expert (R rows in all,
  * R = 128 * (ceil(T*k/128) + E)); 8 A_perm [R, p/2] E2M1 codes, 9 s [R, I/2] codes,
- * 10 y [R, p] BF16, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
+ * 10 y [R, p] FP16, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
  * FP32 per-row scales.  All configs: 15 row_cnt [E+1] int32 rows per expert.
  * Writes min(n, 16) offsets and returns how many it wrote (0 for an invalid config). */
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n);
 
 /* Synchronises `stream`, returns the device-side status of every call since the last
  * read (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears it.  detail (may
- * be NULL) receives a code naming the wait or check that failed. */
+ * be NULL) receives a code naming the wait or check that failed first:
+ *   1-6   a pipeline wait ran out (MOE_ERR_TIMEOUT): 1 producer slot, 2 MMA operands,
+ *         3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain, 6 combine rows;
+ *   16    a replayed expert id outside [0, E) (its slot is skipped);
+ *   17    a row index check;
+ *   18    the full-width norm: a non-finite input row, or an h value beyond the FP16
+ *         range (BF16 configurations store h in FP16 for the pooler);
+ *   19    the pooled-input norm: a non-finite row, or a u value beyond the FP16 range;
+ *   20    the combine: a non-finite c, or (BF16 configurations) a c value beyond the
+ *         FP16 range, e.g. from replayed weights whose absolute sum is large;
+ *   21    NVFP4 experts: a requantised SwiGLU block whose scale saturated because its
+ *         static global scale (gs_act2) is too small for it, or a non-finite s.
+ *   Codes 18-21 report MOE_ERR_DEVICE_CHECK; the call's outputs are then undefined. */
 moe_status_t moe_read_status(void* ws, size_t ws_bytes, moe_stream_t stream,
                              int32_t* detail);
 

@@ -26,13 +26,15 @@ MOE_NVFP4 = 2
 
 MOE_FLAG_TEST_TIMEOUT = 0x80000000
 MOE_FLAG_WEIGHT_TILES = 0x40000000
+MOE_FLAG_NVFP4_PAIR = 0x20000000
 
 PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL, PACK_SF13, PACK_SF2, PACK_GS13, \
     PACK_GS2 = range(9)
 
 # every symbol the header declares
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_packed_bytes", "moe_pack_weights",
-           "moe_quantize_nvfp4", "moe_route", "moe_route_noalloc", "moe_forward",
+           "moe_quantize_nvfp4", "moe_route", "moe_route_noalloc",
+           "moe_read_noalloc_status", "moe_forward",
            "moe_boundary", "moe_forward_profiled",
            "moe_num_stages",
            "moe_stage_name", "moe_forward_launches", "moe_workspace_offsets",
@@ -100,6 +102,8 @@ def lib() -> ctypes.CDLL:
     L.moe_route.restype = i32
     L.moe_route_noalloc.argtypes = [cfgp, wp, vp, vp, vp, vp]
     L.moe_route_noalloc.restype = i32
+    L.moe_read_noalloc_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    L.moe_read_noalloc_status.restype = i32
     L.moe_forward.argtypes = [cfgp, wp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_boundary.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_boundary.restype = i32
@@ -198,6 +202,12 @@ def moe_workspace_offsets(cfg) -> dict:
 def moe_read_status(ws, ws_bytes, stream):
     detail = ctypes.c_int32(0)
     st = int(lib().moe_read_status(ws, ws_bytes, stream, ctypes.byref(detail)))
+    return st, int(detail.value)
+
+
+def moe_read_noalloc_status(stream):
+    detail = ctypes.c_int32(0)
+    st = int(lib().moe_read_noalloc_status(stream, ctypes.byref(detail)))
     return st, int(detail.value)
 
 

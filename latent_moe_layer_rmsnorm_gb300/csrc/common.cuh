@@ -24,11 +24,36 @@ enum : int {
   WAIT_COMBINE = 6,
   CHECK_EXPERT_ID = 16,
   CHECK_ROW = 17,
+  // a stored intermediate left its format's range: a non-finite row, a value above the
+  // FP16 maximum (h, u, c), or an s block whose NVFP4 scale saturated under its static
+  // global scale
+  CHECK_H_RANGE = 18,
+  CHECK_U_RANGE = 19,
+  CHECK_C_RANGE = 20,
+  CHECK_S_RANGE = 21,
 };
+
+// Largest finite FP16 value: the FP16 intermediates (h, u, c) are checked against it.
+constexpr float F16_MAX = 65504.0f;
 
 __device__ __forceinline__ void report_error(int* status, int code, int detail) {
   if (status == nullptr) return;
   if (atomicCAS(status, 0, code) == 0) status[1] = detail;
+}
+
+// ---- programmatic dependent launch ----------------------------------------------------
+// The kernels of one forward are launched so that each may start while its predecessor
+// in the stream is still finishing (prologue: barrier set-up, tensor-map prefetch, TMEM
+// allocation).  pdl_wait() blocks until every earlier grid of the stream has completed
+// and its memory is visible: each kernel calls it before its first access to global
+// memory, so no kernel completes before its predecessors and every read sees the
+// writes before it.  pdl_allow_next() lets the next grid be scheduled (it then waits in
+// its own pdl_wait).  Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_allow_next() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -307,10 +332,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// The value an output row holds once stored: BF16 rounds to nearest even, FP32 keeps it.
-// Epilogues square this value, so a row's sums of squares describe the stored row.
-__device__ __forceinline__ float stored_value(float v, bool bf16) {
-  return bf16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+// Storage formats of GEMM outputs.  FP16 holds the expert GEMMs' outputs (s, y) of BF16
+// configurations: 3 more significand bits than BF16 at the same size.
+enum OutFmt : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_TF32 = 2, OUT_F16 = 3 };
+
+// The value an output holds once stored in format `fmt` (round to nearest even for BF16
+// and FP16; FP32 keeps it).  Epilogues square this value, so a row's sums of squares
+// describe the stored row.
+__device__ __forceinline__ float stored_value(float v, int fmt) {
+  if (fmt == OUT_BF16) return __bfloat162float(__float2bfloat16_rn(v));
+  if (fmt == OUT_F16) return __half2float(__float2half_rn(v));
+  return v;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -350,13 +382,17 @@ __device__ __forceinline__ float recip_ue4m3(uint32_t c) {
 // 6*g and inv_g = 1/g in FP32, both 0 when g == 0): returns the scale code and writes
 // 8 bytes of E2M1 codes (element 2i in the low nibble of byte i).  The op order is
 // the reference order: sf = ue4m3(bmax / six_g); r = recip(sf) * inv_g;
-// code = e2m1(x * r).
+// code = e2m1(x * r).  ratio_out (optional) receives bmax / six_g: above 464 the scale
+// saturated at 448 (the largest UE4M3 value) instead of rounding.
 __device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float six_g, float inv_g,
-                                               uint2& codes, const float* recip_tab) {
+                                               uint2& codes, const float* recip_tab,
+                                               float* ratio_out = nullptr) {
   float bmax = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(x[i]));
-  const uint32_t sf = encode_ue4m3(six_g > 0.f ? bmax / six_g : 0.f);
+  const float ratio = six_g > 0.f ? bmax / six_g : 0.f;
+  if (ratio_out) *ratio_out = ratio;
+  const uint32_t sf = encode_ue4m3(ratio);
   const float r = (recip_tab ? recip_tab[sf] : recip_ue4m3(sf)) * inv_g;
   uint32_t w0 = 0, w1 = 0;
 #pragma unroll
@@ -374,6 +410,11 @@ __device__ __forceinline__ uint32_t quantize16(const float (&x)[16], float six_g
 __device__ __forceinline__ size_t sf_offset(size_t r, int g, int K) {
   const size_t chunk = (r >> 7) * static_cast<size_t>(K >> 6) + (g >> 2);
   return chunk * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (g & 3);
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  __half2 h = *reinterpret_cast<__half2*>(&v);
+  return __half22float2(h);
 }
 
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {

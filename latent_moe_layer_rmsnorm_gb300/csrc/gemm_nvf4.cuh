@@ -8,7 +8,7 @@
 //   gate/up  u [rows, p] x W13_e [2I, p] (gate/up rows interleaved in blocks of 64)
 //            epilogue: a, b = acc * alpha[row] * beta13[e]; s = silu(a) * b; s -> NVFP4
 //            with the static global scale gamma[e] (codes + chunked scales)
-//   down     s [rows, I] x W2_e [p, I]; epilogue y = acc * gamma[e] * beta2[e] (BF16)
+//   down     s [rows, I] x W2_e [p, I]; epilogue y = acc * gamma[e] * beta2[e] (FP16)
 //
 // Same pipeline as gemm_tcgen05.cuh (TMA producer warp, one MMA-issuing thread, four
 // epilogue warps, double-buffered TMEM accumulators, bounded waits), with per-stage
@@ -54,7 +54,7 @@ constexpr int NV_THREADS = 512;
 // writes and include/latent_moe.h documents)
 constexpr int NV_W13_GROUP = 64;
 
-enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_BF16 = 1 };
+enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_Y = 1 };
 
 struct NvSmem {
   GemmSmem g;                // barriers and schedule (its `full`/`empty` sized for GEMM_STAGES)
@@ -65,7 +65,7 @@ struct NvSmem {
 };
 
 // The down GEMM's epilogue writes y through shared memory: each epilogue warp stages a
-// 32-row x 64-column BF16 box (4 KB, 128-byte swizzle) and stores it with TMA, instead of
+// 32-row x 64-column FP16 box (4 KB, 128-byte swizzle) and stores it with TMA, instead of
 // 32 rows of 16-byte pieces per store instruction (those stores cost about a third of
 // the kernel's time, measured).  Expert rows are padded to 128 per expert, so a box never
 // reaches another expert's rows; rows past an expert's last token are padding.
@@ -84,9 +84,9 @@ constexpr size_t nvf4_smem_bytes_for() {
 }
 // one dynamic shared-memory size for both kernels: the larger of the two
 constexpr size_t nvf4_smem_bytes() {
-  return nvf4_smem_bytes_for<NV_EPI_SWIGLU_Q>() > nvf4_smem_bytes_for<NV_EPI_STORE_BF16>()
+  return nvf4_smem_bytes_for<NV_EPI_SWIGLU_Q>() > nvf4_smem_bytes_for<NV_EPI_STORE_Y>()
              ? nvf4_smem_bytes_for<NV_EPI_SWIGLU_Q>()
-             : nvf4_smem_bytes_for<NV_EPI_STORE_BF16>();
+             : nvf4_smem_bytes_for<NV_EPI_STORE_Y>();
 }
 static_assert(nvf4_smem_bytes() <= 232448, "more than 227 KB of shared memory per CTA");
 static_assert(NV_SF_COL0 + NV_MAX_STAGES * NV_SF_COLS <= GEMM_TMEM_COLS, "scale ring past TMEM");
@@ -148,8 +148,15 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
         s1[i] = __fdividef(a1, 1.0f + __expf(-a1)) * b1;
       }
       uint2 q0, q1;
-      const uint32_t code0 = quantize16(s0, six_g, inv_g, q0, recip);
-      const uint32_t code1 = quantize16(s1, six_g, inv_g, q1, recip);
+      float ratio0, ratio1, fin = 0.f;
+      const uint32_t code0 = quantize16(s0, six_g, inv_g, q0, recip, &ratio0);
+      const uint32_t code1 = quantize16(s1, six_g, inv_g, q1, recip, &ratio1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) fin = fmaf(s0[i] + s1[i], 0.f, fin);   // NaN unless finite
+      // a block whose ratio passed 464 saturated its scale at 448 instead of rounding: its
+      // static global scale is too small for it (or s is not finite)
+      if (row_ok && !(fmaxf(ratio0, ratio1) <= 464.f && fin == 0.f))
+        report_error(P.status, ST_DEVICE_CHECK, CHECK_S_RANGE);
       if (row_ok) {
         const int col = tc.n_blk * (NV_BN / 2) + hh * 64 + c0;
         *reinterpret_cast<uint4*>(codes + col / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
@@ -161,7 +168,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
     const float sc = x0;
     const int lane = r & 31;
     float ss = 0.f;     // the half is one 128-column block of the row (row_ssq)
-    // one 32-row x 64-column BF16 staging box per TMEM wait: row `lane`, 16-byte chunk j
+    // one 32-row x 64-column FP16 staging box per TMEM wait: row `lane`, 16-byte chunk j
     // (columns 8j..8j+7) at chunk (j ^ lane % 8), the 128-byte swizzle of the tensor map
 #pragma unroll 1
     for (int c0 = 0; c0 < 128; c0 += 64) {
@@ -184,8 +191,8 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const float* w = v + 8 * j;
-        const uint4 o = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
-                                   pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
+        const uint4 o = make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]),
+                                   pack_f16x2(w[4], w[5]), pack_f16x2(w[6], w[7]));
         *reinterpret_cast<uint4*>(ybox + lane * 128 + ((j ^ (lane & 7)) << 4)) = o;
       }
       fence_proxy_async_smem();
@@ -193,7 +200,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       if (lane == 0)
         tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0, tc.a_row + (r - lane));
 #pragma unroll
-      for (int i = 0; i < 64; ++i) { const float q = stored_value(v[i], true); ss = fmaf(q, q, ss); }
+      for (int i = 0; i < 64; ++i) { const float q = stored_value(v[i], OUT_F16); ss = fmaf(q, q, ss); }
     }
     if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + 2 * tc.n_blk + hh] = ss;
   }
@@ -235,12 +242,14 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) N->recip[i] = recip_ue4m3(i);
+  pdl_wait();          // the inputs and tables are the previous kernels' outputs
+  pdl_allow_next();
   for (int i = threadIdx.x; i <= P.groups; i += blockDim.x) {
     S->mt_off[i] = P.mt_off[i];
     S->row_off[i] = P.row_off[i];
     S->row_cnt[i] = P.row_cnt[i];
   }
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) N->recip[i] = recip_ue4m3(i);
   if (warp == 2) tmem_alloc(&S->tmem_base, GEMM_TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -398,7 +407,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S->tempty[0]);
     }
-    if (EPI == NV_EPI_STORE_BF16 && lane == 0) tma_store_wait_all();   // y fully written
+    if (EPI == NV_EPI_STORE_Y && lane == 0) tma_store_wait_all();   // y fully written
   }
 
   tc_fence_before();

@@ -195,7 +195,7 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
         store16(P.out, base + c0, P.out_fmt, va);
         store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
-      const bool rb = P.out_fmt == OUT_BF16;       // squared as stored
+      const int rb = P.out_fmt;                    // squared as stored
 #pragma unroll
       for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
 #pragma unroll
@@ -212,13 +212,17 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
 __device__ __forceinline__ void box_put16(uint8_t* box, int lane, int off, int fmt,
                                           const float (&v)[16]) {
   uint8_t* row = box + lane * 128;
-  if (fmt == OUT_BF16) {
+  if (fmt == OUT_BF16 || fmt == OUT_F16) {
+    const bool h16 = fmt == OUT_F16;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int j = (off >> 4) + h;
+      const float* w = v + 8 * h;
       uint4 o;
-      o.x = pack_bf16x2(v[8 * h], v[8 * h + 1]);     o.y = pack_bf16x2(v[8 * h + 2], v[8 * h + 3]);
-      o.z = pack_bf16x2(v[8 * h + 4], v[8 * h + 5]); o.w = pack_bf16x2(v[8 * h + 6], v[8 * h + 7]);
+      o.x = h16 ? pack_f16x2(w[0], w[1]) : pack_bf16x2(w[0], w[1]);
+      o.y = h16 ? pack_f16x2(w[2], w[3]) : pack_bf16x2(w[2], w[3]);
+      o.z = h16 ? pack_f16x2(w[4], w[5]) : pack_bf16x2(w[4], w[5]);
+      o.w = h16 ? pack_f16x2(w[6], w[7]) : pack_bf16x2(w[6], w[7]);
       *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
     }
   } else {
@@ -242,7 +246,7 @@ template <int EPI>
 __device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const TileCoord& tc,
                                                     uint32_t taddr, int q, int lane,
                                                     const CUtensorMap* tmOut, uint8_t* box) {
-  const int es = P.out_fmt == OUT_BF16 ? 2 : 4;
+  const int es = (P.out_fmt == OUT_BF16 || P.out_fmt == OUT_F16) ? 2 : 4;
   const int per_box = 128 / es;                       // values per box row
   const int row0 = tc.a_row + 32 * q;
   const size_t row = static_cast<size_t>(row0 + lane);
@@ -273,7 +277,7 @@ __device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const T
       put(col_base + c0, va, col_base);
       put(col_base + c0 + 16, vb, col_base);
       if (P.row_ssq) {                                // squared as stored
-        const bool rb = P.out_fmt == OUT_BF16;
+        const int rb = P.out_fmt;
 #pragma unroll
         for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
 #pragma unroll
@@ -341,6 +345,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmB64);
     }
   }
+  pdl_wait();          // the inputs and tables are the previous kernels' outputs
+  pdl_allow_next();
   if (warp == 2) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&S->tmem_base)),

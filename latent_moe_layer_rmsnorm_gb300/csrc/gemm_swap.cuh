@@ -84,7 +84,9 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& P, const SwapTil
           const float b = __uint_as_float(u[jj]);
           const float s = __fdividef(a, 1.0f + __expf(-a)) * b;      // silu(a) * b
           const size_t idx = static_cast<size_t>(tc.tok_row + c0 + jj) * P.ld_out + f;
-          if (P.out_fmt == OUT_BF16)
+          if (P.out_fmt == OUT_F16)
+            reinterpret_cast<__half*>(P.out)[idx] = __float2half_rn(s);
+          else if (P.out_fmt == OUT_BF16)
             reinterpret_cast<__nv_bfloat16*>(P.out)[idx] = __float2bfloat16_rn(s);
           else
             reinterpret_cast<float*>(P.out)[idx] = tf32_rna(s);
@@ -100,7 +102,9 @@ __device__ __forceinline__ void swap_epilogue(const GemmParams& P, const SwapTil
       for (int jj = 0; jj < 16; ++jj) {
         if (c0 + jj < tc.valid) {
           const size_t idx = static_cast<size_t>(tc.tok_row + c0 + jj) * P.ld_out + f;
-          if (P.out_fmt == OUT_BF16)
+          if (P.out_fmt == OUT_F16)
+            reinterpret_cast<__half*>(P.out)[idx] = __float2half_rn(__uint_as_float(v[jj]));
+          else if (P.out_fmt == OUT_BF16)
             reinterpret_cast<__nv_bfloat16*>(P.out)[idx] = __float2bfloat16_rn(__uint_as_float(v[jj]));
           else
             reinterpret_cast<float*>(P.out)[idx] = __uint_as_float(v[jj]);
@@ -140,6 +144,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
   }
+  pdl_wait();          // the inputs and tables are the previous kernels' outputs
+  pdl_allow_next();
   for (int i = threadIdx.x; i <= P.groups; i += blockDim.x) {
     S->mt_off[i] = P.mt_off[i];    // token tiles (of TN) per expert, prefix sums
     S->row_off[i] = P.row_off[i];

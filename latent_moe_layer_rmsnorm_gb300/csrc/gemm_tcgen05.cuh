@@ -38,7 +38,6 @@ constexpr int GEMM_TMEM_COLS = 512;
 constexpr int ROUTER_MAX_K = 8;
 
 enum EpiKind : int { EPI_ROUTER = 0, EPI_STORE = 1, EPI_SWIGLU = 2 };
-enum OutFmt : int { OUT_BF16 = 0, OUT_F32 = 1, OUT_TF32 = 2 };
 // Operand kinds; the values of the first three are the instruction-descriptor format
 // codes of kind::f16 / kind::tf32.  OP_NVF4: packed E2M1 operands (gemm_nvf4.cuh).
 enum OpKind : int { OP_F16 = 0, OP_BF16 = 1, OP_TF32 = 2, OP_NVF4 = 3 };
@@ -151,7 +150,16 @@ __device__ __forceinline__ TileCoord gemm_tile(const GemmParams& P, const GemmSm
 
 // ---- epilogue stores ------------------------------------------------------------------
 __device__ __forceinline__ void store16(void* out, size_t idx, int fmt, const float (&v)[16]) {
-  if (fmt == OUT_BF16) {
+  if (fmt == OUT_F16) {
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(out) + idx);
+    uint4 a, b;
+    a.x = pack_f16x2(v[0], v[1]);   a.y = pack_f16x2(v[2], v[3]);
+    a.z = pack_f16x2(v[4], v[5]);   a.w = pack_f16x2(v[6], v[7]);
+    b.x = pack_f16x2(v[8], v[9]);   b.y = pack_f16x2(v[10], v[11]);
+    b.z = pack_f16x2(v[12], v[13]); b.w = pack_f16x2(v[14], v[15]);
+    dst[0] = a;
+    dst[1] = b;
+  } else if (fmt == OUT_BF16) {
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + idx);
     uint4 a, b;
     a.x = pack_bf16x2(v[0], v[1]);   a.y = pack_bf16x2(v[2], v[3]);
@@ -210,7 +218,7 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
         if (two) store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
       if (P.row_ssq) {          // expert outputs (bn is 128 or 256), squared as stored
-        const bool rb = P.out_fmt == OUT_BF16;
+        const int rb = P.out_fmt;
 #pragma unroll
         for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
 #pragma unroll
@@ -310,6 +318,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  pdl_wait();          // the inputs and tables are the previous kernels' outputs
+  pdl_allow_next();
   if (P.groups > 0) {
     for (int i = threadIdx.x; i <= P.groups; i += blockDim.x) {
       S->mt_off[i] = P.mt_off[i];

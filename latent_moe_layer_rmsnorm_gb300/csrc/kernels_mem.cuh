@@ -37,12 +37,17 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // ---- full-width RMSNorm ---------------------------------------------------------------
 // One block per token.  Pass 1 sums squares; pass 2 re-reads the row (L1-resident) and
-// writes h = x * rsqrt(mean(x^2) + eps) * g twice: TF32-rounded FP32 and FP16.  FP16 is
-// safe for h: |h_i| <= sqrt(d) * max|g| (e.g. 91 * 1.5 at d = 8192).
+// writes h = x * rsqrt(mean(x^2) + eps) * g twice: TF32-rounded FP32 and FP16 (h16 may be
+// null: router-only calls).  |h_i| <= sqrt(d) * max|g| (e.g. 91 * 1.5 at d = 8192) keeps
+// h inside FP16 for gains of ordinary size; a row that is not finite, or an h16 value
+// above the FP16 maximum (very large gains), is reported as CHECK_H_RANGE.
 template <bool ACT_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     norm_in_kernel(const void* __restrict__ x, const float* __restrict__ g,
-                   float* __restrict__ h32, __half* __restrict__ h16, int d, float eps) {
+                   float* __restrict__ h32, __half* __restrict__ h16, int d, float eps,
+                   int* status) {
+  pdl_wait();
+  pdl_allow_next();
   __shared__ float red[32];
   const size_t t = blockIdx.x;
   const int nchunk = d >> 3;  // 8 elements per chunk
@@ -66,6 +71,7 @@ __global__ void __launch_bounds__(MEM_THREADS)
   }
   const float total = block_sum(ss, red);
   const float rs = rsqrtf(total / static_cast<float>(d) + eps);
+  float hmax = 0.f;
   for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
     float v[8];
     if constexpr (ACT_F32) {
@@ -90,12 +96,19 @@ __global__ void __launch_bounds__(MEM_THREADS)
     o32[0] = make_float4(tf32_rna(h[0]), tf32_rna(h[1]), tf32_rna(h[2]), tf32_rna(h[3]));
     o32[1] = make_float4(tf32_rna(h[4]), tf32_rna(h[5]), tf32_rna(h[6]), tf32_rna(h[7]));
     if constexpr (!ACT_F32) {
-      uint4 o;
-      o.x = pack_f16x2(h[0], h[1]); o.y = pack_f16x2(h[2], h[3]);
-      o.z = pack_f16x2(h[4], h[5]); o.w = pack_f16x2(h[6], h[7]);
-      reinterpret_cast<uint4*>(h16 + t * d)[c] = o;
+      if (h16 != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hmax = fmaxf(hmax, fabsf(h[i]));
+        uint4 o;
+        o.x = pack_f16x2(h[0], h[1]); o.y = pack_f16x2(h[2], h[3]);
+        o.z = pack_f16x2(h[4], h[5]); o.w = pack_f16x2(h[6], h[7]);
+        reinterpret_cast<uint4*>(h16 + t * d)[c] = o;
+      }
     }
   }
+  // total is the same in every thread: a non-finite row is reported once, by thread 0
+  if ((threadIdx.x == 0 && !(fabsf(total) < INFINITY)) || !(hmax <= F16_MAX))
+    report_error(status, ST_DEVICE_CHECK, CHECK_H_RANGE);
 }
 
 // ---- dispatch: counting sort of (token, slot) pairs by expert -------------------------
@@ -103,6 +116,8 @@ __global__ void __launch_bounds__(MEM_THREADS)
 __global__ void __launch_bounds__(MEM_THREADS)
     dispatch_hist_kernel(const int32_t* __restrict__ ids, int n, int E,
                          int* __restrict__ chunk_counts, int* status) {
+  pdl_wait();
+  pdl_allow_next();
   __shared__ int hist[256];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -151,6 +166,8 @@ __global__ void __launch_bounds__(256)
     dispatch_scan_kernel(int* __restrict__ chunk_counts, int nchunks, int E,
                          int* __restrict__ row_off, int* __restrict__ mt_off,
                          int* __restrict__ mt2_off, int* __restrict__ row_cnt, int padded) {
+  pdl_wait();
+  pdl_allow_next();
   __shared__ int sh[32];
   const int e = threadIdx.x;
   int running = 0;
@@ -192,6 +209,8 @@ __global__ void __launch_bounds__(32)
     dispatch_scatter_kernel(const int32_t* __restrict__ ids, int n, int E,
                             const int* __restrict__ chunk_base, int* __restrict__ inv,
                             int* __restrict__ src) {
+  pdl_wait();
+  pdl_allow_next();
   __shared__ int cnt[256];
   const int lane = threadIdx.x;
   for (int e = lane; e < E; e += 32) cnt[e] = chunk_base[blockIdx.x * E + e];
@@ -221,15 +240,89 @@ __global__ void __launch_bounds__(32)
   }
 }
 
+// The three dispatch steps in one block, for batches of at most DISPATCH_CHUNK (token,
+// slot) pairs (decode): counts in shared memory, the scan of dispatch_scan_kernel with
+// one chunk, then warp 0 places the pairs in (token, slot) order as
+// dispatch_scatter_kernel does.  Same maps as the three kernels.
+__global__ void __launch_bounds__(256)
+    dispatch_small_kernel(const int32_t* __restrict__ ids, int n, int E,
+                          int* __restrict__ row_off, int* __restrict__ mt_off,
+                          int* __restrict__ mt2_off, int* __restrict__ row_cnt,
+                          int* __restrict__ inv, int* __restrict__ src, int padded,
+                          int* status) {
+  pdl_wait();
+  pdl_allow_next();
+  __shared__ int cnt[256];
+  __shared__ int sh[32];
+  const int e = threadIdx.x;
+  if (e < 256) cnt[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int id = ids[i];
+    if (id >= 0 && id < E) atomicAdd(&cnt[id], 1);
+    else report_error(status, ST_DEVICE_CHECK, CHECK_EXPERT_ID);
+  }
+  __syncthreads();
+  const int running = e < E ? cnt[e] : 0;
+  int total;
+  const int off = block_excl_scan(running, sh, &total);
+  int mt_total;
+  const int mto = block_excl_scan(e < E ? (running + 127) / 128 : 0, sh, &mt_total);
+  int mt2_total;
+  const int mt2o = block_excl_scan(e < E ? (running + 255) / 256 : 0, sh, &mt2_total);
+  const int start = padded ? mto * 128 : off;
+  if (e < E) {
+    row_off[e] = start;
+    mt_off[e] = mto;
+    mt2_off[e] = mt2o;
+    row_cnt[e] = running;
+  }
+  if (e == 0) {
+    row_off[E] = padded ? mt_total * 128 : total;
+    mt_off[E] = mt_total;
+    mt2_off[E] = mt2_total;
+    row_cnt[E] = total;
+  }
+  __syncthreads();                       // every thread has read its count
+  if (e < E) cnt[e] = start;             // next free position of each expert
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int i0 = 0; i0 < n; i0 += 32) {
+    const int i = i0 + lane;
+    int id = (i < n) ? ids[i] : -1;
+    if (id >= E) id = -1;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, id);
+    const int rank = __popc(peers & lt);
+    const int pos0 = (id >= 0) ? cnt[id] : 0;
+    __syncwarp();
+    if (id >= 0 && (__ffs(peers) - 1) == lane) cnt[id] = pos0 + __popc(peers);
+    __syncwarp();
+    if (i < n) {
+      if (id >= 0) {
+        const int pos = pos0 + rank;
+        inv[i] = pos;
+        src[pos] = i;
+      } else {
+        inv[i] = -1;
+      }
+    }
+  }
+}
+
 // ---- pooled-input RMSNorm + cast + permute ---------------------------------------------
 // One block per token: u = pooled * rsqrt(mean(pooled^2) + eps) * g_pool, written in the
 // GEMM operand format (FP16, or TF32-rounded FP32) to the token's k dispatched rows.
-// FP16 is safe for u: |u_i| <= sqrt(p) * max|g_pool|.
+// |u_i| <= sqrt(p) * max|g_pool| keeps u inside FP16 for gains of ordinary size; a row
+// that is not finite, or an FP16 value above its maximum, is reported as CHECK_U_RANGE.
 template <bool OUT_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     pool_permute_kernel(const float* __restrict__ pooled, const float* __restrict__ g,
                         const int* __restrict__ inv, void* __restrict__ a_perm, int p, int k,
-                        float eps) {
+                        float eps, int* status) {
+  pdl_wait();
+  pdl_allow_next();
   __shared__ float red[32];
   __shared__ int rows[MAX_TOPK];
   const size_t t = blockIdx.x;
@@ -252,6 +345,7 @@ __global__ void __launch_bounds__(MEM_THREADS)
   }
   const float total = block_sum(ss, red);   // also orders rows[] before its use
   const float rs = rsqrtf(total / static_cast<float>(p) + eps);
+  float umax = 0.f;
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
     const int c = threadIdx.x + j * MEM_THREADS;
@@ -273,6 +367,8 @@ __global__ void __launch_bounds__(MEM_THREADS)
           dst[1] = o1;
         }
       } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) umax = fmaxf(umax, fabsf(u[i]));
         uint4 o;
         o.x = pack_f16x2(u[0], u[1]); o.y = pack_f16x2(u[2], u[3]);
         o.z = pack_f16x2(u[4], u[5]); o.w = pack_f16x2(u[6], u[7]);
@@ -284,11 +380,13 @@ __global__ void __launch_bounds__(MEM_THREADS)
       }
     }
   }
+  if ((threadIdx.x == 0 && !(fabsf(total) < INFINITY)) || !(umax <= F16_MAX))
+    report_error(status, ST_DEVICE_CHECK, CHECK_U_RANGE);
 }
 
 // ---- combine -----------------------------------------------------------------------
 // One block per (token, slice of `cols` columns, at most 1024), 8 columns per thread.
-// Expert output rows y are FP32, or BF16 when Y_BF16 (BF16 and NVFP4 experts).  The down
+// Expert output rows y are FP32, or FP16 when Y_F16 (BF16 and NVFP4 experts).  The down
 // GEMM's epilogue left, for every stored expert output row, the sum of squares of each
 // 128-column block (row_ssq, [rows, p / 128]).  Thread 0 bulk-copies the token's k row
 // slices into shared memory while the warps form r_j = rsqrt(sum / p + eps) from row
@@ -309,22 +407,24 @@ inline int combine_cols(int p) {
   return 128;
 }
 inline int combine_threads(int cols) { return cols / COMBINE_VEC < 32 ? 32 : cols / COMBINE_VEC; }
-inline size_t combine_smem_bytes(int cols, bool y_bf16) {
-  return size_t(MAX_TOPK) * cols * (y_bf16 ? 2 : 4);
+inline size_t combine_smem_bytes(int cols, bool y_f16) {
+  return size_t(MAX_TOPK) * cols * (y_f16 ? 2 : 4);
 }
 
-template <bool C_F32, bool Y_BF16>
+template <bool C_F32, bool Y_F16>
 __global__ void __launch_bounds__(COMBINE_MAX_COLS / COMBINE_VEC)
     combine_kernel(const void* __restrict__ y, const float* __restrict__ row_ssq,
                    const int* __restrict__ inv, const int32_t* __restrict__ ids,
                    const float* __restrict__ wts, const float* __restrict__ g_exp,
                    void* __restrict__ c_out, int p, int cols, int k, int E, float eps,
                    int* status, unsigned long long timeout_ns) {
+  pdl_wait();
+  pdl_allow_next();
   extern __shared__ __align__(16) uint8_t cmb_smem[];
   __shared__ uint64_t landed;
   __shared__ float sj[MAX_TOPK];     // w_j * r_j
   __shared__ int srow[MAX_TOPK], seid[MAX_TOPK];
-  constexpr int YB = Y_BF16 ? 2 : 4;  // bytes per stored y value
+  constexpr int YB = Y_F16 ? 2 : 4;   // bytes per stored y value
   const int nq = p / cols;
   const size_t t = blockIdx.x / nq;
   const int col0 = static_cast<int>(blockIdx.x % nq) * cols;
@@ -378,10 +478,10 @@ __global__ void __launch_bounds__(COMBINE_MAX_COLS / COMBINE_VEC)
     if (srow[j] < 0) continue;
     const uint8_t* src = cmb_smem + j * slice + cl * YB;
     float v[COMBINE_VEC];
-    if constexpr (Y_BF16) {
+    if constexpr (Y_F16) {
       const uint4 b = *reinterpret_cast<const uint4*>(src);
-      const float2 f0 = unpack_bf16x2(b.x), f1 = unpack_bf16x2(b.y);
-      const float2 f2 = unpack_bf16x2(b.z), f3 = unpack_bf16x2(b.w);
+      const float2 f0 = unpack_f16x2(b.x), f1 = unpack_f16x2(b.y);
+      const float2 f2 = unpack_f16x2(b.z), f3 = unpack_f16x2(b.w);
       v[0] = f0.x; v[1] = f0.y; v[2] = f1.x; v[3] = f1.y;
       v[4] = f2.x; v[5] = f2.y; v[6] = f3.x; v[7] = f3.y;
     } else {
@@ -399,6 +499,16 @@ __global__ void __launch_bounds__(COMBINE_MAX_COLS / COMBINE_VEC)
     for (int i = 0; i < COMBINE_VEC; ++i) acc[i] = fmaf(sc, v[i] * g[i], acc[i]);
   }
   const size_t off = t * p + col0 + cl;
+  // c must fit its store: finite, and inside FP16 for BF16 configurations (|c_i| <=
+  // sum_j |w_j| * sqrt(p) * max|g_exp|; replayed weights with a large sum can leave it)
+  float cmax = 0.f, fin = 0.f;
+#pragma unroll
+  for (int i = 0; i < COMBINE_VEC; ++i) {
+    cmax = fmaxf(cmax, fabsf(acc[i]));
+    fin = fmaf(acc[i], 0.f, fin);           // NaN unless every value is finite
+  }
+  if (!(fin == 0.f && (C_F32 || cmax <= F16_MAX)))
+    report_error(status, ST_DEVICE_CHECK, CHECK_C_RANGE);
   if constexpr (C_F32) {
     float* o = static_cast<float*>(c_out) + off;
     *reinterpret_cast<float4*>(o) = make_float4(tf32_rna(acc[0]), tf32_rna(acc[1]),
@@ -415,26 +525,28 @@ __global__ void __launch_bounds__(COMBINE_MAX_COLS / COMBINE_VEC)
   }
 }
 
-// Block sums of squares of stored expert output rows (FP32, or BF16 when Y_BF16), for the
+// Block sums of squares of stored expert output rows (FP32, or FP16 when Y_F16), for the
 // down GEMM variants whose epilogue does not produce them (weight-row tiles): one thread
 // per (row, 128 columns), summed in column order like the GEMM epilogues.
-template <bool Y_BF16>
+template <bool Y_F16>
 __global__ void __launch_bounds__(MEM_THREADS)
     row_ssq_kernel(const void* __restrict__ y, int rows, int p, float* __restrict__ row_ssq) {
+  pdl_wait();
+  pdl_allow_next();
   const int parts = p >> 7;
   const size_t n = size_t(rows) * parts;
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n;
        i += size_t(gridDim.x) * blockDim.x) {
     const size_t e0 = (i / parts) * p + (i % parts) * 128;
     float ss = 0.f;
-    if constexpr (Y_BF16) {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y) + e0);
+    if constexpr (Y_F16) {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __half*>(y) + e0);
       for (int q = 0; q < 16; ++q) {
         const uint4 v = src[q];
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float2 f = unpack_bf16x2(w[h]);
+          const float2 f = unpack_f16x2(w[h]);
           ss = fmaf(f.x, f.x, ss);
           ss = fmaf(f.y, f.y, ss);
         }
@@ -675,6 +787,8 @@ __global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __res
 // BF16 or TF32-rounded FP32.  n % 4 == 0.
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int ksplit, size_t n,
                                      void* __restrict__ out, int fmt) {
+  pdl_wait();
+  pdl_allow_next();
   for (size_t i = (blockIdx.x * size_t(blockDim.x) + threadIdx.x) * 4; i < n;
        i += size_t(gridDim.x) * blockDim.x * 4) {
     // slices in groups of 4 (loads in flight together), summed in a fixed order
@@ -714,6 +828,8 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int ksplit,
 __global__ void router_reduce_topk_kernel(const float* __restrict__ part, int ksplit, int T,
                                           int ld, int E, int k, int32_t* __restrict__ ids,
                                           float* __restrict__ wts) {
+  pdl_wait();
+  pdl_allow_next();
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -721,8 +837,26 @@ __global__ void router_reduce_topk_kernel(const float* __restrict__ part, int ks
   float v[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) v[j] = 0.f;
-  // all of this lane's experts per slice: 8 independent loads in flight
-  for (int s = 0; s < ksplit; ++s) {
+  // this lane's experts of four slices at a time: 32 independent loads in flight, then
+  // the sums in slice order
+  int s = 0;
+  for (; s + 4 <= ksplit; s += 4) {
+    float q[4][PER];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float* row = part + (size_t(s + u) * T + t) * ld;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int e = lane + 32 * j;
+        q[u][j] = e < E ? row[e] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < PER; ++j) v[j] += q[u][j];
+  }
+  for (; s < ksplit; ++s) {
     const float* row = part + (size_t(s) * T + t) * ld;
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
@@ -857,12 +991,15 @@ __global__ void quantize_weight_kernel(const __nv_bfloat16* __restrict__ gate,
 // Pooled-input RMSNorm fused with the per-token NVFP4 quantiser: one block per token;
 // u = pooled * rsqrt(mean(pooled^2) + eps) * g_pool in FP32, alpha = max|u| / 2688,
 // then E2M1 codes + UE4M3 scales written to each of the token's k dispatched rows
-// (alpha too, per row, for the gate/up GEMM's accumulators).  p <= 8192.
+// (alpha too, per row, for the gate/up GEMM's accumulators).  p <= 8192.  A row that is
+// not finite is reported as CHECK_U_RANGE.
 __global__ void __launch_bounds__(MEM_THREADS)
     pool_quant_kernel(const float* __restrict__ pooled, const float* __restrict__ g,
                       const int* __restrict__ inv, uint8_t* __restrict__ codes,
                       uint8_t* __restrict__ sf, float* __restrict__ alpha_rows, int p, int k,
-                      float eps) {
+                      float eps, int* status) {
+  pdl_wait();
+  pdl_allow_next();
   __shared__ float red[32];
   __shared__ int rows[MAX_TOPK];
   const size_t t = blockIdx.x;
@@ -914,6 +1051,9 @@ __global__ void __launch_bounds__(MEM_THREADS)
   amax = (threadIdx.x & 31) < (blockDim.x >> 5) ? red[threadIdx.x & 31] : 0.f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  // a row that is not finite cannot be quantised (its scale would be inf or NaN)
+  if (threadIdx.x == 0 && !(fabsf(total) < INFINITY && amax < INFINITY))
+    report_error(status, ST_DEVICE_CHECK, CHECK_U_RANGE);
   const float a = amax / NVFP4_AMAX_DIV;
   const float six_a = 6.0f * a;
   const float inv_a = a > 0.f ? 1.0f / a : 0.f;

@@ -6,6 +6,7 @@
 #include "../../include/latent_moe.h"
 #include "common.cuh"
 #include "gemm_nvf4.cuh"
+#include "gemm_nvf4_pair.cuh"
 #include "gemm_pair.cuh"
 #include "gemm_swap.cuh"
 #include "gemm_tcgen05.cuh"
@@ -99,13 +100,12 @@ moe_status_t device_ready(int* sms) {
     if (e == cudaSuccess) e = set_smem_attr<OP_TF32, EPI_SWIGLU>();
     if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_STORE>();
     if (e == cudaSuccess) e = set_smem_attr<OP_F16, EPI_SWIGLU>();
-    if (e == cudaSuccess) e = set_smem_attr<OP_BF16, EPI_STORE>();
     const int swap_smem = static_cast<int>(swap_smem_bytes());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_swap_kernel<OP_F16, SWAP_SWIGLU>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, swap_smem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_swap_kernel<OP_BF16, SWAP_STORE>,
+      e = cudaFuncSetAttribute(gemm_swap_kernel<OP_F16, SWAP_STORE>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, swap_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_swap_kernel<OP_TF32, SWAP_SWIGLU>,
@@ -118,18 +118,23 @@ moe_status_t device_ready(int* sms) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_smem_bytes()));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_BF16>,
+      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_Y>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_smem_bytes()));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<NV_EPI_SWIGLU_Q>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(nvf4_pair_smem_bytes()));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<NV_EPI_STORE_Y>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(nvf4_pair_smem_bytes()));
     const int pair_smem = static_cast<int>(pair_smem_bytes());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_pair_kernel<OP_F16, EPI_STORE>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_pair_kernel<OP_F16, EPI_SWIGLU>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_BF16, EPI_STORE>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_STORE>,
@@ -174,7 +179,8 @@ moe_status_t validate(const moe_config_t* c) {
   } else if (c->expert != c->act) {
     return MOE_ERR_UNSUPPORTED;
   }
-  if ((c->flags & ~(MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_WEIGHT_TILES)) != 0) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & ~(MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_WEIGHT_TILES | MOE_FLAG_NVFP4_PAIR)) != 0)
+    return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED;
   if (c->d % 128 || c->p % 128 || c->I % 128) return MOE_ERR_UNSUPPORTED;
   if (c->d > 32768 || c->p > 8192 || c->I > 32768) return MOE_ERR_UNSUPPORTED;
@@ -253,7 +259,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.inv = take(T * k * 4);
   L.a_perm = take(q ? R * p / 2 : R * p * ee);
   L.s = take(q ? R * I / 2 : R * I * ee);
-  L.y = take(R * p * (c.expert == MOE_F32 ? 4 : 2));   // expert outputs: BF16 (FP32 experts: FP32)
+  L.y = take(R * p * (c.expert == MOE_F32 ? 4 : 2));   // expert outputs: FP16 (FP32 experts: FP32)
   L.ssq = take(R * (p / 128) * 4);   // their sums of squares per 128-column block
   L.c = take(T * p * ea);
   L.sf_u = take(q ? R * p / 16 : 0);
@@ -288,12 +294,37 @@ inline moe_status_t last_launch() {
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// One kernel of a forward.  Programmatic stream serialisation lets the kernel be
+// scheduled while the previous kernel of the stream is finishing, so its prologue
+// (barrier set-up, tensor-map prefetch, TMEM allocation) and launch latency overlap the
+// predecessor's tail; every kernel of the step waits for its predecessors (pdl_wait)
+// before it touches global memory ("SGLang and Miles Add Day-0 Support for Muse Spark
+// Open", section "Kernel Optimizations": launch dependent kernels earlier).
+template <typename... KArgs, typename... Args>
+moe_status_t launch_step(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t st, Args... args) {
+  if (grid.x == 0) return MOE_OK;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 template <int KIND, int EPI>
 moe_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& P,
                          int grid, cudaStream_t st) {
   if (grid <= 0) return MOE_OK;
-  gemm_tcgen05_kernel<KIND, EPI><<<grid, GEMM_THREADS, gemm_smem_bytes(), st>>>(ta, tb, P);
-  return last_launch();
+  return launch_step(gemm_tcgen05_kernel<KIND, EPI>, dim3(grid), dim3(GEMM_THREADS),
+                     gemm_smem_bytes(), st, ta, tb, P);
 }
 
 // CTA-pair GEMM: one cluster of 2 CTAs per 256 x 256 tile, up to one cluster per 2 SMs.
@@ -308,9 +339,8 @@ moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& ta64, const C
   const int clusters = std::min(sms / 2, max_tiles);
   if (clusters <= 0) return MOE_OK;
   P.out_box = boxes ? 1 : 0;
-  gemm_pair_kernel<KIND, EPI><<<2 * clusters, GEMM_THREADS, pair_smem_bytes(), st>>>(
-      ta, ta64, tb, tb64, tout, P);
-  return last_launch();
+  return launch_step(gemm_pair_kernel<KIND, EPI>, dim3(2 * clusters), dim3(GEMM_THREADS),
+                     pair_smem_bytes(), st, ta, ta64, tb, tb64, tout, P);
 }
 
 GemmParams base_params(int* status, uint32_t flags) {
@@ -364,21 +394,23 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   __half* h16 = reinterpret_cast<__half*>(base + L.h16);
   const bool act_f32 = c.act == MOE_F32;
   const bool exp_f32 = c.expert == MOE_F32;
-  // operand kinds: FP32 configurations run on TF32; BF16 ones keep the norm-bounded
-  // operands (h, u, c) and the weights they meet in FP16, and s / W2 in BF16
+  // operand kinds: FP32 configurations run on TF32; BF16 ones store every activation
+  // between the GEMMs (h, u, s, y, c) in FP16 and meet FP16 copies of the weights
   const int k_proj = act_f32 ? OP_TF32 : OP_F16;      // pooler, unpooler
   const int k_up = exp_f32 ? OP_TF32 : OP_F16;        // gate/up GEMM
-  const int k_down = exp_f32 ? OP_TF32 : OP_BF16;     // down GEMM
+  const int k_down = exp_f32 ? OP_TF32 : OP_F16;      // down GEMM
   const int T = c.T, d = c.d, p = c.p, E_ = c.E, k = c.top_k, I = c.I;
   const int rows = T * k;
   const int mtiles = (T + GEMM_BM - 1) / GEMM_BM;
 
   // ---- stage: full-width RMSNorm ------------------------------------------------------
+  // a router-only call does not need the pooler's FP16 copy of h
   if (act_f32)
-    norm_in_kernel<true><<<T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, d, c.eps);
+    MOE_TRY(launch_step(norm_in_kernel<true>, dim3(T), dim3(MEM_THREADS), 0, st, x, W->g_in, h32,
+                        static_cast<__half*>(nullptr), d, c.eps, status));
   else
-    norm_in_kernel<false><<<T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, h16, d, c.eps);
-  MOE_TRY(last_launch());
+    MOE_TRY(launch_step(norm_in_kernel<false>, dim3(T), dim3(MEM_THREADS), 0, st, x, W->g_in, h32,
+                        route_only ? nullptr : h16, d, c.eps, status));
   E.mark(1);
 
   // ---- stage: router GEMM (TF32) + top-k ------------------------------------------------
@@ -398,8 +430,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       P.ksplit = sp.router; P.split_stride = size_t(T) * bn;
       P.out = part; P.ld_out = bn; P.out_fmt = OUT_F32;
       MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, std::min(sms, mtiles * sp.router), st)));
-      router_reduce_topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(part, sp.router, T, bn, E_, k, ids, wts);
-      MOE_TRY(last_launch());
+      MOE_TRY(launch_step(router_reduce_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, part,
+                          sp.router, T, bn, E_, k, ids, wts));
     } else if (bn == 256) {   // CTA pairs: each CTA loads 128 of the 256 router rows
       P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
       CUtensorMap tb2;
@@ -442,9 +474,10 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     if (sp.pool > 1) {
       const size_t n = size_t(T) * p;
-      splitk_reduce_kernel<<<static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096)), 256, 0, st>>>(
-          part, sp.pool, n, pooled, OUT_F32);
-      MOE_TRY(last_launch());
+      MOE_TRY(launch_step(splitk_reduce_kernel,
+                          dim3(static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096))),
+                          dim3(256), 0, st, part, sp.pool, n, static_cast<void*>(pooled),
+                          static_cast<int>(OUT_F32)));
     }
   }
   E.mark(3);
@@ -462,22 +495,32 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   uint8_t* sf_u = base + L.sf_u;
   uint8_t* sf_s = base + L.sf_s;
   float* alpha = reinterpret_cast<float*>(base + L.alpha);
-  dispatch_hist_kernel<<<L.nchunks, MEM_THREADS, 0, st>>>(ids, rows, E_, chunk, status);
-  MOE_TRY(last_launch());
-  dispatch_scan_kernel<<<1, 256, 0, st>>>(chunk, L.nchunks, E_, row_off, mt_off, mt2_off,
-                                          row_cnt, nvf4 ? 1 : 0);
-  MOE_TRY(last_launch());
-  dispatch_scatter_kernel<<<L.nchunks, 32, 0, st>>>(ids, rows, E_, chunk, inv, src);
-  MOE_TRY(last_launch());
+  if (L.nchunks == 1) {     // small batches (decode): the three steps in one block
+    MOE_TRY(launch_step(dispatch_small_kernel, dim3(1), dim3(256), 0, st,
+                        static_cast<const int32_t*>(ids), rows, E_, row_off, mt_off, mt2_off,
+                        row_cnt, inv, src, nvf4 ? 1 : 0, status));
+  } else {
+    MOE_TRY(launch_step(dispatch_hist_kernel, dim3(L.nchunks), dim3(MEM_THREADS), 0, st,
+                        static_cast<const int32_t*>(ids), rows, E_, chunk, status));
+    MOE_TRY(launch_step(dispatch_scan_kernel, dim3(1), dim3(256), 0, st, chunk, L.nchunks, E_,
+                        row_off, mt_off, mt2_off, row_cnt, nvf4 ? 1 : 0));
+    MOE_TRY(launch_step(dispatch_scatter_kernel, dim3(L.nchunks), dim3(32), 0, st,
+                        static_cast<const int32_t*>(ids), rows, E_,
+                        static_cast<const int*>(chunk), inv, src));
+  }
   if (nvf4)
-    pool_quant_kernel<<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv,
-                                                 static_cast<uint8_t*>(a_perm), sf_u, alpha, p,
-                                                 k, c.eps);
+    MOE_TRY(launch_step(pool_quant_kernel, dim3(T), dim3(MEM_THREADS), 0, st,
+                        static_cast<const float*>(pooled), W->g_pool,
+                        static_cast<const int*>(inv), static_cast<uint8_t*>(a_perm), sf_u, alpha,
+                        p, k, c.eps, status));
   else if (exp_f32)
-    pool_permute_kernel<true><<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv, a_perm, p, k, c.eps);
+    MOE_TRY(launch_step(pool_permute_kernel<true>, dim3(T), dim3(MEM_THREADS), 0, st,
+                        static_cast<const float*>(pooled), W->g_pool,
+                        static_cast<const int*>(inv), a_perm, p, k, c.eps, status));
   else
-    pool_permute_kernel<false><<<T, MEM_THREADS, 0, st>>>(pooled, W->g_pool, inv, a_perm, p, k, c.eps);
-  MOE_TRY(last_launch());
+    MOE_TRY(launch_step(pool_permute_kernel<false>, dim3(T), dim3(MEM_THREADS), 0, st,
+                        static_cast<const float*>(pooled), W->g_pool,
+                        static_cast<const int*>(inv), a_perm, p, k, c.eps, status));
   E.mark(4);
 
   // ---- stage: grouped gate/up GEMM + SwiGLU -------------------------------------------
@@ -495,9 +538,19 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = s_buf; P.ld_out = I;
     P.sf_a = sf_u; P.sf_b = W->sf13; P.row_scale = alpha; P.grp_scale = W->gs13;
     P.out_scale = W->gs_act2; P.out_sf = sf_s;
-    const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_SWIGLU_Q><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, ta, P);
-    MOE_TRY(last_launch());
+    if (!(c.flags & MOE_FLAG_NVFP4_PAIR)) {
+      const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
+      MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_SWIGLU_Q>, dim3(grid), dim3(NV_THREADS),
+                          nvf4_smem_bytes(), st, ta, tb, ta, P));
+    } else {   // CTA pairs over 256-row tiles of each expert (tile prefix: mt2_off)
+      CUtensorMap tb128;      // each CTA of a pair loads 128 of the tile's 256 weight rows
+      if (!make_tmap(&tb128, W->w13, OP_NVF4, p / 2, static_cast<uint64_t>(E_) * 2 * I, 128))
+        return MOE_ERR_CUDA;
+      P.mt_off = mt2_off;
+      const int clusters = std::min(sms / 2, (R / 256 + E_) * (2 * I / NV_BN));
+      MOE_TRY(launch_step(gemm_nvf4_pair_kernel<NV_EPI_SWIGLU_Q>, dim3(2 * clusters),
+                          dim3(NV_THREADS), nvf4_pair_smem_bytes(), st, ta, tb128, ta, P));
+    }
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on the MMA's M side (256-row W13 blocks: 128 gate + 128 up), tokens on N
     CUtensorMap tw, tx;
@@ -507,14 +560,15 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.N = 2 * I; P.K = p; P.bn = 256; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
-    P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
+    P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_F16;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
     const int grid = std::min(sms, max_mt * (2 * I / 256));
     if (exp_f32)
-      gemm_swap_kernel<OP_TF32, SWAP_SWIGLU><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
+      MOE_TRY(launch_step(gemm_swap_kernel<OP_TF32, SWAP_SWIGLU>, dim3(grid), dim3(GEMM_THREADS),
+                          swap_smem_bytes(), st, tw, tx, P));
     else
-      gemm_swap_kernel<OP_F16, SWAP_SWIGLU><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
-    MOE_TRY(last_launch());
+      MOE_TRY(launch_step(gemm_swap_kernel<OP_F16, SWAP_SWIGLU>, dim3(grid), dim3(GEMM_THREADS),
+                          swap_smem_bytes(), st, tw, tx, P));
   } else {
     // CTA pairs over 256-row tiles of each expert (M = 128 pair tiles for remainders);
     // each CTA of a pair loads half of a 256-row W13 block: 128 gate or 128 up rows
@@ -527,10 +581,10 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     GemmParams P = base_params(status, c.flags);
     P.N = 2 * I; P.K = p; P.bn = 2 * W13_GROUP; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt2_off; P.row_cnt = row_cnt;
-    P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_BF16;
+    P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_F16;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
     CUtensorMap to;
-    if (!make_tmap(&to, s_buf, exp_f32 ? OP_TF32 : OP_BF16, I, rows, 32)) return MOE_ERR_CUDA;
+    if (!make_tmap(&to, s_buf, exp_f32 ? OP_TF32 : OP_F16, I, rows, 32)) return MOE_ERR_CUDA;
     const int tiles = (rows / 256 + E_) * (2 * I / P.bn);
     if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_SWIGLU>(ta, ta64, tb, tb64, to, P, tiles, sms, st)));
     else MOE_TRY((launch_pair<OP_F16, EPI_SWIGLU>(ta, ta64, tb, tb64, to, P, tiles, sms, st)));
@@ -538,27 +592,37 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   E.mark(5);
 
   // ---- stage: grouped down GEMM -> y ------------------------------------------------------
-  // y: BF16 (FP32 only for FP32 experts), with FP32 sums of squares of the stored values
+  // y: FP16 (FP32 only for FP32 experts), with FP32 sums of squares of the stored values
   // per 128 columns beside it; the per-expert norm and the weighted sum run in FP32
   void* y_buf = base + L.y;
   float* ssq = reinterpret_cast<float*>(base + L.ssq);
-  const bool y_bf16 = !exp_f32;
-  const int y_fmt = y_bf16 ? OUT_BF16 : OUT_F32;
-  const int y_op = y_bf16 ? OP_BF16 : OP_TF32;
+  const bool y_f16 = !exp_f32;
+  const int y_fmt = y_f16 ? OUT_F16 : OUT_F32;
+  const int y_op = y_f16 ? OP_F16 : OP_TF32;
   if (nvf4) {
-    CUtensorMap ta, tb, ty;   // ty: y in 32-row x 64-column BF16 boxes for the epilogue
+    CUtensorMap ta, tb, ty;   // ty: y in 32-row x 64-column FP16 boxes for the epilogue
     if (!make_tmap(&ta, s_buf, OP_NVF4, I / 2, R, GEMM_BM) ||
         !make_tmap(&tb, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, NV_BN) ||
-        !make_tmap(&ty, y_buf, OP_BF16, p, R, 32))
+        !make_tmap(&ty, y_buf, OP_F16, p, R, 32))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = NV_BN; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
     P.out = y_buf; P.ld_out = p; P.row_ssq = ssq;
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
-    const int grid = std::min(sms, max_mt * (p / NV_BN));
-    gemm_nvf4_kernel<NV_EPI_STORE_BF16><<<grid, NV_THREADS, nvf4_smem_bytes(), st>>>(ta, tb, ty, P);
-    MOE_TRY(last_launch());
+    if (!(c.flags & MOE_FLAG_NVFP4_PAIR)) {
+      const int grid = std::min(sms, max_mt * (p / NV_BN));
+      MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_STORE_Y>, dim3(grid), dim3(NV_THREADS),
+                          nvf4_smem_bytes(), st, ta, tb, ty, P));
+    } else {
+      CUtensorMap tb128;      // each CTA of a pair loads 128 of the tile's 256 weight rows
+      if (!make_tmap(&tb128, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, 128))
+        return MOE_ERR_CUDA;
+      P.mt_off = mt2_off;
+      const int clusters = std::min(sms / 2, (R / 256 + E_) * (p / NV_BN));
+      MOE_TRY(launch_step(gemm_nvf4_pair_kernel<NV_EPI_STORE_Y>, dim3(2 * clusters),
+                          dim3(NV_THREADS), nvf4_pair_smem_bytes(), st, ta, tb128, ty, P));
+    }
   } else if (c.flags & MOE_FLAG_WEIGHT_TILES) {
     // weights on M (128 rows of p), up to 256 tokens on N
     CUtensorMap tw, tx;
@@ -572,15 +636,19 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     const int max_mt2 = (rows + 255) / 256 + E_;
     const int grid = std::min(sms, max_mt2 * (p / 128));
     if (exp_f32)
-      gemm_swap_kernel<OP_TF32, SWAP_STORE><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
+      MOE_TRY(launch_step(gemm_swap_kernel<OP_TF32, SWAP_STORE>, dim3(grid), dim3(GEMM_THREADS),
+                          swap_smem_bytes(), st, tw, tx, P));
     else
-      gemm_swap_kernel<OP_BF16, SWAP_STORE><<<grid, GEMM_THREADS, swap_smem_bytes(), st>>>(tw, tx, P);
-    MOE_TRY(last_launch());
+      MOE_TRY(launch_step(gemm_swap_kernel<OP_F16, SWAP_STORE>, dim3(grid), dim3(GEMM_THREADS),
+                          swap_smem_bytes(), st, tw, tx, P));
     const size_t n = rows * static_cast<size_t>(p / 128);
     const int ssq_grid = static_cast<int>(std::min<size_t>((n + MEM_THREADS - 1) / MEM_THREADS, 4096));
-    if (y_bf16) row_ssq_kernel<true><<<ssq_grid, MEM_THREADS, 0, st>>>(y_buf, rows, p, ssq);
-    else row_ssq_kernel<false><<<ssq_grid, MEM_THREADS, 0, st>>>(y_buf, rows, p, ssq);
-    MOE_TRY(last_launch());
+    if (y_f16)
+      MOE_TRY(launch_step(row_ssq_kernel<true>, dim3(ssq_grid), dim3(MEM_THREADS), 0, st,
+                          static_cast<const void*>(y_buf), rows, p, ssq));
+    else
+      MOE_TRY(launch_step(row_ssq_kernel<false>, dim3(ssq_grid), dim3(MEM_THREADS), 0, st,
+                          static_cast<const void*>(y_buf), rows, p, ssq));
   } else {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
@@ -598,7 +666,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       P.mt_off = mt2_off;
       const int tiles = (rows / 256 + E_) * (p / 256);
       if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
-      else MOE_TRY((launch_pair<OP_BF16, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
+      else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
     } else {
       if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
           !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, bn))
@@ -606,7 +674,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       P.mt_off = mt_off;
       const int grid = std::min(sms, max_mt * (p / bn));
       if (exp_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
-      else MOE_TRY((launch_gemm<OP_BF16, EPI_STORE>(ta, tb, P, grid, st)));
+      else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     }
   }
   E.mark(6);
@@ -616,16 +684,18 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   {
     const int ccols = combine_cols(p);
     const int cgrid = T * (p / ccols), cthreads = combine_threads(ccols);
-    const size_t csmem = combine_smem_bytes(ccols, y_bf16);
+    const size_t csmem = combine_smem_bytes(ccols, y_f16);
     const unsigned long long tmo = base_params(status, c.flags).timeout_ns;
-#define LMOE_COMBINE(CF, YB)                                                              \
-  combine_kernel<CF, YB><<<cgrid, cthreads, csmem, st>>>(y_buf, ssq, inv, ids, wts, W->g_exp, \
-                                                         c_buf, p, ccols, k, E_, c.eps, status, tmo)
-    if (act_f32) { if (y_bf16) LMOE_COMBINE(true, true); else LMOE_COMBINE(true, false); }
-    else { if (y_bf16) LMOE_COMBINE(false, true); else LMOE_COMBINE(false, false); }
+#define LMOE_COMBINE(CF, YB)                                                                  \
+  MOE_TRY(launch_step(combine_kernel<CF, YB>, dim3(cgrid), dim3(cthreads), csmem, st,          \
+                      static_cast<const void*>(y_buf), static_cast<const float*>(ssq),         \
+                      static_cast<const int*>(inv), static_cast<const int32_t*>(ids),           \
+                      static_cast<const float*>(wts), W->g_exp, c_buf, p, ccols, k, E_, c.eps, \
+                      status, tmo))
+    if (act_f32) { if (y_f16) LMOE_COMBINE(true, true); else LMOE_COMBINE(true, false); }
+    else { if (y_f16) LMOE_COMBINE(false, true); else LMOE_COMBINE(false, false); }
 #undef LMOE_COMBINE
   }
-  MOE_TRY(last_launch());
   E.mark(7);
 
   // ---- stage: unpooler GEMM -> out ----------------------------------------------------------
@@ -654,9 +724,10 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
     if (sp.unpool > 1) {
       const size_t n = size_t(T) * d;
-      splitk_reduce_kernel<<<static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096)), 256, 0, st>>>(
-          part, sp.unpool, n, out, c.out == MOE_F32 ? OUT_F32 : OUT_BF16);
-      MOE_TRY(last_launch());
+      MOE_TRY(launch_step(splitk_reduce_kernel,
+                          dim3(static_cast<int>(std::min<size_t>((n / 4 + 255) / 256, 4096))),
+                          dim3(256), 0, st, static_cast<const float*>(part), sp.unpool, n, out,
+                          static_cast<int>(c.out == MOE_F32 ? OUT_F32 : OUT_BF16)));
     }
   }
   E.mark(8);
@@ -669,11 +740,13 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
 // forbids device allocations after start-up, a replayed CUDA graph that must not grow
 // its pool).  moe_route_noalloc serves them from this file-scope array instead.  Every
 // GPU that loads the library keeps it until the process exits, so it is kept small:
-// status word, then h32 [T,d] FP32 and h16 [T,d] FP16 for T * d <= NOALLOC_MAX_ELEMS.
+// status word, h32 [T,d] FP32 for T * d <= NOALLOC_MAX_ELEMS, then the router's split-K
+// partial logits (small T: more CTAs share the router weights) in NOALLOC_PART_BYTES.
 constexpr size_t NOALLOC_MAX_ELEMS = size_t(1) << 21;   // e.g. T = 256 at d = 8192
 constexpr size_t NOALLOC_H32_OFF = 256;
-constexpr size_t NOALLOC_H16_OFF = NOALLOC_H32_OFF + NOALLOC_MAX_ELEMS * 4;
-constexpr size_t NOALLOC_BYTES = NOALLOC_H16_OFF + NOALLOC_MAX_ELEMS * 2;   // 12 MiB + 256
+constexpr size_t NOALLOC_PART_OFF = NOALLOC_H32_OFF + NOALLOC_MAX_ELEMS * 4;
+constexpr size_t NOALLOC_PART_BYTES = size_t(4) << 20;
+constexpr size_t NOALLOC_BYTES = NOALLOC_PART_OFF + NOALLOC_PART_BYTES;   // 12 MiB + 256
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
 struct NoAllocDev {
@@ -701,6 +774,15 @@ moe_status_t noalloc_scratch(void** out) {
   return MOE_OK;
 }
 
+// K slices of the no-workspace router: the workspace path's split, halved until its
+// partial logits fit the array's partial region.
+int noalloc_router_split(const moe_config_t& c) {
+  const size_t Ep = (c.E + 15) / 16 * 16;
+  int ks = split_plan(c).router;
+  while (ks > 1 && size_t(ks) * c.T * Ep * 4 > NOALLOC_PART_BYTES) ks /= 2;
+  return ks;
+}
+
 }  // namespace
 
 // =====================================================================================
@@ -726,8 +808,7 @@ size_t moe_packed_bytes(const moe_config_t* cfg, int which) {
   switch (which) {
     case 0: return size_t(c.E) * c.d * 4;
     case 1: return q ? size_t(c.E) * 2 * c.I * c.p / 2 : size_t(c.E) * 2 * c.I * c.p * ee;
-    case 2: return q ? size_t(c.E) * c.p * c.I / 2
-                     : (c.expert == MOE_F32 ? size_t(c.E) * c.p * c.I * ee : 0);
+    case 2: return q ? size_t(c.E) * c.p * c.I / 2 : size_t(c.E) * c.p * c.I * ee;
     case 3: return size_t(c.p) * c.d * ea;
     case 4: return size_t(c.d) * c.p * ea;
     case 5: return q ? size_t(c.E) * 2 * c.I * c.p / 16 : 0;
@@ -755,7 +836,7 @@ moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weigh
   if (!nvf4 && (!src->w_gate || !src->w_up || !w13_out || !aligned16(src->w_gate) ||
                 !aligned16(src->w_up) || !aligned16(w13_out)))
     return MOE_ERR_INVALID_ARG;
-  if (exp_f32 && (!src->w_down || !w2_out || !aligned16(src->w_down) || !aligned16(w2_out)))
+  if (!nvf4 && (!src->w_down || !w2_out || !aligned16(src->w_down) || !aligned16(w2_out)))
     return MOE_ERR_INVALID_ARG;
   auto copy = [&](const void* s, void* d, size_t bytes, bool tf32) {
     const size_t n16 = bytes / 16;
@@ -774,7 +855,7 @@ moe_status_t moe_pack_weights(const moe_config_t* cfg, const moe_canonical_weigh
       pack_w13_kernel<CONV_BF16_TO_F16><<<rows13, 256, 0, st>>>(src->w_gate, src->w_up, w13_out, c.I, c.p, W13_GROUP, es);
     MOE_TRY(last_launch());
   }
-  if (exp_f32) MOE_TRY(copy(src->w_down, w2_out, size_t(c.E) * c.p * c.I * 4, true));
+  if (!nvf4) MOE_TRY(copy(src->w_down, w2_out, size_t(c.E) * c.p * c.I * es, exp_f32));
   const size_t ea = act_f32 ? 4 : 2;
   MOE_TRY(copy(src->w_pool, w_pool_out, size_t(c.p) * c.d * ea, act_f32));
   MOE_TRY(copy(src->w_unpool, w_unpool_out, size_t(c.d) * c.p * ea, act_f32));
@@ -840,14 +921,14 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_weights_t* W, 
   uint8_t* base = static_cast<uint8_t*>(scratch);
   int* status = reinterpret_cast<int*>(base);
   float* h32 = reinterpret_cast<float*>(base + NOALLOC_H32_OFF);
-  __half* h16 = reinterpret_cast<__half*>(base + NOALLOC_H16_OFF);
+  float* part = reinterpret_cast<float*>(base + NOALLOC_PART_OFF);
   // the array keeps the previous call's contents: the status word must start at zero
   clear_status_kernel<<<1, 32, 0, st>>>(status);
   MOE_TRY(last_launch());
   if (c.act == MOE_F32)
-    norm_in_kernel<true><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, c.d, c.eps);
+    norm_in_kernel<true><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, c.d, c.eps, status);
   else
-    norm_in_kernel<false><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, h16, c.d, c.eps);
+    norm_in_kernel<false><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, c.d, c.eps, status);
   MOE_TRY(last_launch());
   const int bn = (c.E + 15) / 16 * 16;
   CUtensorMap ta, tb;
@@ -856,9 +937,32 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_weights_t* W, 
     return MOE_ERR_CUDA;
   GemmParams P = base_params(status, c.flags);
   P.M = c.T; P.N = bn; P.K = c.d; P.bn = bn; P.groups = 0;
-  P.E = c.E; P.top_k = c.top_k; P.ids = ids; P.wts = w;
   const int mtiles = (c.T + GEMM_BM - 1) / GEMM_BM;
+  const int ks = noalloc_router_split(c);
+  if (ks > 1) {     // small T: K slices -> partial logits in the array -> sum + top-k
+    P.ksplit = ks; P.split_stride = size_t(c.T) * bn;
+    P.out = part; P.ld_out = bn; P.out_fmt = OUT_F32;
+    MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, std::min(sms, mtiles * ks), st)));
+    router_reduce_topk_kernel<<<(c.T + 7) / 8, 256, 0, st>>>(part, ks, c.T, bn, c.E, c.top_k,
+                                                             ids, w);
+    return last_launch();
+  }
+  P.E = c.E; P.top_k = c.top_k; P.ids = ids; P.wts = w;
   return launch_gemm<OP_TF32, EPI_ROUTER>(ta, tb, P, std::min(sms, mtiles), st);
+}
+
+moe_status_t moe_read_noalloc_status(moe_stream_t stream, int32_t* detail) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  void* scratch = nullptr;
+  MOE_TRY(noalloc_scratch(&scratch));
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int h[2] = {0, 0};
+  if (cudaMemcpy(h, scratch, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  clear_status_kernel<<<1, 32, 0, st>>>(static_cast<int*>(scratch));
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (detail) *detail = h[1];
+  return static_cast<moe_status_t>(h[0]);
 }
 
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
@@ -928,13 +1032,14 @@ const char* moe_stage_name(int stage) {
 
 int moe_forward_launches(const moe_config_t* cfg, int route_internally) {
   if (validate(cfg) != MOE_OK || cfg->T == 0) return 0;
-  // norm, [router], pooler, 4 dispatch kernels, gate/up, down, combine, unpooler,
-  // plus one reduction per split-K GEMM
+  // norm, [router], pooler, 4 dispatch kernels (2 for one chunk of pairs), gate/up, down,
+  // combine, unpooler, plus one reduction per split-K GEMM
   const SplitPlan sp = split_plan(*cfg);
   // the weight-row down GEMM leaves the row sums of squares to one more kernel
   const int ssq_pass = (cfg->flags & MOE_FLAG_WEIGHT_TILES) && cfg->expert != MOE_NVFP4 ? 1 : 0;
-  return 10 + (route_internally ? 1 + (sp.router > 1) : 0) + (sp.pool > 1) + (sp.unpool > 1) +
-         ssq_pass;
+  const int one_chunk = ws_layout(*cfg).nchunks == 1 ? 2 : 0;
+  return 10 - one_chunk + (route_internally ? 1 + (sp.router > 1) : 0) + (sp.pool > 1) +
+         (sp.unpool > 1) + ssq_pass;
 }
 
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n) {

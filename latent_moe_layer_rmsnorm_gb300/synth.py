@@ -66,12 +66,19 @@ PREFILL_SLICE_BF16 = Shape("prefill_slice_bf16", T=1024, d=8192, p=4096, E=16, t
                            I=4096)
 
 PREFILL_SLICE_NVFP4 = PREFILL_SLICE_BF16.replace(name="prefill_slice_nvfp4", expert="nvfp4")
+# A 1/8 slice (512 rows per expert as well) whose expert outputs (16384 rows x 8 KB =
+# 134 MB) exceed L2, for captures of the memory-bound kernels between the GEMMs.
+PREFILL_EIGHTH_BF16 = Shape("prefill_eighth_bf16", T=2048, d=8192, p=4096, E=32, top_k=8,
+                            I=4096)
+# The block boundary on 4096 full-width rows (x, the block output, x' and h': 256 MB in
+# all) with narrow experts, for captures of moe_boundary.
+BOUNDARY_BF16 = Shape("boundary_bf16", T=4096, d=8192, p=256, E=8, top_k=2, I=256)
 # Decode with NVFP4 experts: the weight stream is 4.5 bits per weight instead of 16.
 DECODE_NVFP4 = DECODE_BF16.replace(name="decode_nvfp4", expert="nvfp4")
 
 WORKLOADS = {s.name: s for s in (TINY_F32, PREFILL_BF16, DECODE_BF16, PREFILL_NVFP4,
                                  SKEWED_BF16, PREFILL_SLICE_BF16, PREFILL_SLICE_NVFP4,
-                                 DECODE_NVFP4)}
+                                 DECODE_NVFP4, PREFILL_EIGHTH_BF16, BOUNDARY_BF16)}
 
 
 def storage_dtype(kind: str) -> torch.dtype:

@@ -34,11 +34,10 @@ Two modes:
 * chain=True ("precision chain", the parity gate): float64 arithmetic, with every
   value rounded where the GPU path stores it (see `storage_kinds`): h (FP32 for
   the router; FP16, or TF32 in FP32 mode, for the pooler), pooled (FP32), u and c
-  (FP16 / TF32), s (BF16 / TF32), y (BF16, FP32 for FP32 experts: the format the
-  SGLang page's fused post-per-expert norm stores and squares) and out; the weights meet
-  the GEMMs in the same formats (FP16 copies of the pooler, gate/up and unpooler
-  weights).  The page fixes the FP32 route-weighted sum; the storage types are the
-  kernel's.
+  (FP16 / TF32), s (FP16 / TF32), y (FP16, FP32 for FP32 experts: the values the fused
+  post-per-expert norm squares) and out; the weights meet the GEMMs in the same formats
+  (FP16 copies of the pooler, gate/up, down and unpooler weights).  The page fixes the
+  FP32 norm and route-weighted sum; the storage types are the kernel's.
 
 Readings of points the pages leave open (each is also listed with the design
 notes): softmax over all E logits, top-k, renormalised (= softmax over the k
@@ -208,22 +207,22 @@ def storage_kinds(act: str, expert: str, out: str, chain: bool) -> dict:
                     out="f64", w_proj="f64", w_gate_up="f64", w_down="f64")
     tc = act == "f32"            # FP32 activations run their GEMMs on TF32 operands
     te = expert == "f32"
-    # BF16 configurations: the norm-bounded GEMM operands h, u, c (and the weights they
-    # meet: pooler, gate/up, unpooler) are FP16; s and the down weights stay BF16.  The
-    # pages fix the per-expert norm and the weighted sum in FP32 but not the format the
-    # expert outputs y wait in before them: BF16 (FP32 for FP32 experts), normalised
-    # from the stored values.
+    # BF16 configurations store every activation between the GEMMs (h, u, s, y, c) in
+    # FP16 and meet FP16 copies of the weights (exact for |w| >= 2^-17).  The pages fix
+    # the per-expert norm and the weighted sum in FP32 but not the format the expert
+    # outputs y wait in before them: FP16 (FP32 for FP32 experts), normalised from the
+    # stored values.
     return dict(
         h_pool="tf32" if tc else "f16",
         pooled="f32",
         u="tf32" if te else "f16",
-        s="tf32" if te else "bf16",
-        y="f32" if te else "bf16",            # expert outputs, the per-expert norm's input
+        s="tf32" if te else "f16",
+        y="f32" if te else "f16",             # expert outputs, the per-expert norm's input
         c="tf32" if tc else "f16",
         out=out,
         w_proj="tf32" if tc else "f16",
         w_gate_up="tf32" if te else "f16",
-        w_down="tf32" if te else "f64",       # BF16 weights are exact as given
+        w_down="tf32" if te else "f16",
     )
 
 
@@ -250,14 +249,14 @@ def nvfp4_expert_rows(u_rows: np.ndarray, wq: dict, gamma: float) -> dict:
     and the weights' shared W13 scale (both carried by the dequantised operands).
         s     = fp32(silu(a) * b),  a = W_gate u, b = W_up u
         s_q   = NVFP4 of s with the static global scale gamma (scale codes per 16)
-        y     = bf16(W_down s_q)   (W_down dequantised with its own global scale)
+        y     = fp16(W_down s_q)   (W_down dequantised with its own global scale)
     Returns s (FP32 values before the requantisation), its codes qs / scale codes sfs,
     the dequantised s_deq and y.
     """
     s = F.fp32(expert_swiglu(u_rows, wq["gate"], wq["up"]))
     qs, sfs = Q.quantize_static(s, gamma)
     s_deq = Q.dequantize(qs, sfs, np.float32(gamma))
-    y = F.bf16(expert_down(s_deq, wq["down"]))
+    y = F.fp16(expert_down(s_deq, wq["down"]))
     return dict(s=s, qs=qs, sfs=sfs, s_deq=s_deq, y=y)
 
 
@@ -279,7 +278,7 @@ def chain_expert(w_gate_e, w_up_e, w_down_e, u_rows, st: dict) -> dict:
 def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
                 expert: str = "bf16", out: str = "f32", chain: bool = True,
                 tokens=None, ids=None, weights=None, norm_after_sum: bool = False,
-                return_parts: bool = False, expert_map=None):
+                return_parts: bool = False, expert_map=None, pooled=None):
     """The latent-MoE block for the rows `tokens` of inp["x"] (all rows if None).
 
     inp holds x [T,d], g_in [d], w_router [E,d], w_pool [p,d], g_pool [p],
@@ -302,11 +301,15 @@ def moe_forward(inp: dict, *, top_k: int, eps: float, act: str = "bf16",
     same order, what `chain_expert(w_gate[e], w_up[e], w_down[e], u_rows, arg)` (or,
     for NVFP4 experts, `nvfp4_expert(..., u_rows, arg)`) returns for expert e's
     weights.  It only decides where the step runs; None runs it here on inp's weights.
+
+    pooled (NVFP4 experts only, optional): the pooler's FP32 output rows [n, p] to start
+    the expert chain from, instead of computing them from x: a stage-wise comparison
+    starts each stage from the stored input of that stage.  Routing still comes from x.
     """
     if expert == "nvfp4":
         return _forward_nvfp4(inp, top_k=top_k, eps=eps, out=out, tokens=tokens, ids=ids,
                               weights=weights, return_parts=return_parts,
-                              expert_map=expert_map)
+                              expert_map=expert_map, pooled=pooled)
     st = storage_kinds(act, expert, out, chain)
     x = as_f64(inp["x"])
     if tokens is not None:
@@ -390,10 +393,10 @@ def expert_input(inp: dict, *, eps: float, tokens=None, h=None):
 
 
 def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts,
-                   expert_map=None):
+                   expert_map=None, pooled=None):
     """The block with NVFP4 experts; storage points as in the BF16 chain except the
     expert operands: u and s are NVFP4 (u quantised from its FP32 value with a per-token
-    scale, s with the static per-expert scale inp["gs_act2"]); y BF16."""
+    scale, s with the static per-expert scale inp["gs_act2"]); y FP16."""
     st = storage_kinds("bf16", "bf16", out, True)
     x = as_f64(inp["x"])
     if tokens is not None:
@@ -406,7 +409,11 @@ def _forward_nvfp4(inp, *, top_k, eps, out, tokens, ids, weights, return_parts,
         ids = np.asarray(ids, dtype=np.int32)
         wts = as_f64(weights)
         top_k = ids.shape[1]
-    _, pooled, u32 = expert_input(inp, eps=eps, h=h)
+    if pooled is None:
+        _, pooled, u32 = expert_input(inp, eps=eps, h=h)
+    else:
+        pooled = F.fp32(as_f64(pooled))
+        u32 = F.fp32(rmsnorm(pooled, inp["g_pool"], eps))
     qu, sfu, alpha = Q.quantize_rows(u32)
     u = Q.dequantize(qu, sfu, alpha)
     p = u.shape[1]

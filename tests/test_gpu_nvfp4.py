@@ -155,13 +155,13 @@ def test_nvfp4_stages_and_layer(shape):
         stp = np.maximum(F.ue4m3_decode(sfs), F.ue4m3_decode(sf_s[rows])).repeat(16, axis=1)
         assert np.all(np.abs(d_gpu - d_ref)
                       <= 2.0 * stp * gs_act2[e] * (1 + 1e-6) + 0.13 * np.abs(d_ref) + 1e-12)
-        # down GEMM, from the GPU's own s; y is stored in BF16: equal to the rounded exact
-        # sum, or one BF16 unit away where FP32 accumulation crossed a rounding boundary
+        # down GEMM, from the GPU's own s; y is stored in FP16: equal to the rounded exact
+        # sum, or one FP16 unit away where FP32 accumulation crossed a rounding boundary
         y_exact = oracle.expert_down(d_gpu, wq["down"])
-        y_ref = F.bf16(y_exact)
+        y_ref = F.fp16(y_exact)
         d = np.abs(y[rows] - y_ref)
         mag = np.maximum(np.maximum(np.abs(y[rows]), np.abs(y_ref)), 1e-30)
-        one = np.exp2(np.floor(np.log2(mag)) - 7)
+        one = np.maximum(np.exp2(np.floor(np.log2(mag)) - 10), 2.0 ** -24)
         floor = 3e-5 * float(np.sqrt(np.mean(y_exact * y_exact)))
         assert np.all(d <= one * (1 + 1e-9) + floor), (e, float(d.max()))
         y_flips += int(np.sum(d > 0))
@@ -174,3 +174,44 @@ def test_nvfp4_stages_and_layer(shape):
     print(f"nvfp4: u codes {code_match:.4f} equal, s codes {s_match / s_total:.4f} equal, "
           f"y {y_err:.1e}, end to end {e2e:.2e}")
     assert e2e <= TOL_NVFP4
+
+
+@pytest.mark.parametrize("shape", [SMALL, MID, DECODE_LIKE], ids=lambda s: s.name)
+def test_pair_kernel_matches_one_cta_kernel(shape):
+    """The CTA-pair NVFP4 GEMMs (MOE_FLAG_NVFP4_PAIR: 256 x 256 tiles, each CTA staging
+    half of the weight tile) against the one-CTA kernels (the default) on the same
+    inputs: requantised SwiGLU codes and scales, expert outputs and the layer output.
+    The shapes give experts with an odd number of 128-row blocks, whose last pair tile
+    has rows in one CTA only, and (decode-like) experts of one or two rows."""
+    need_gpu()
+    from latent_moe_layer_rmsnorm_gb300 import _lib as L
+    inp, dev, layer = build(shape, 2)
+    T, I = shape.T, shape.I
+    x = dev["x"]
+    one = layer.forward(x).clone()
+    s_one = layer.intermediate("s", T)
+    sf_one = layer.intermediate("sf_s", T)
+    y_one = layer.intermediate("y", T)
+    pair = layer.forward(x, flags=L.MOE_FLAG_NVFP4_PAIR).clone()
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    row_off = layer.intermediate("row_off", T).cpu().numpy().astype(np.int64)
+    row_cnt = layer.intermediate("row_cnt", T).cpu().numpy().astype(np.int64)
+    rows = np.concatenate([np.arange(row_off[e], row_off[e] + row_cnt[e])
+                           for e in range(shape.E)]).astype(np.int64)
+    odd = int(np.sum(((row_cnt[:shape.E] + 127) // 128) % 2 == 1))
+    s_pair, y_pair = layer.intermediate("s", T), layer.intermediate("y", T)
+    rs = torch.as_tensor(rows)
+    same_s = torch.equal(s_pair[rs], s_one[rs])
+    same_y = torch.equal(y_pair[rs], y_one[rs])
+    sf_rows_idx = unchunk_sf(np.arange(len(sf_one)), 128 * ((T * shape.top_k + 127) // 128 + shape.E),
+                             I)[rows].reshape(-1)
+    same_sf = np.array_equal(layer.intermediate("sf_s", T).cpu().numpy()[sf_rows_idx],
+                             sf_one.cpu().numpy()[sf_rows_idx])
+    err = rel_err(to_np(pair), to_np(one))
+    print(f"pair vs one-CTA ({shape.name}, {odd} experts with an odd block count): s codes "
+          f"{'equal' if same_s else 'differ'}, scales {'equal' if same_sf else 'differ'}, y "
+          f"{'equal' if same_y else 'differs'}, out {err:.1e}")
+    # same operands, same K order per output element: the pair MMA gives the same sums
+    assert same_s and same_sf and same_y
+    assert torch.equal(pair, one)

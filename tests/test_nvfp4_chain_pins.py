@@ -12,7 +12,7 @@ output has a static per-expert scale gamma.
   scale, the shared W13 scale, gamma and the W2 scale enter, value by value;
 * weights already on the NVFP4 grid come back unchanged (shared W13 scale, row layout);
 * on inputs that every quantisation represents exactly, the NVFP4 chain equals the BF16
-  chain;
+  experts' chain;
 * scaling one expert's W_down by 2^k moves only its W2 scale, and the per-expert norm
   cancels it: identical output;
 * scaling gamma by 2^k (block scales staying in the normal UE4M3 range) leaves the
@@ -77,15 +77,15 @@ def test_hand_worked_nvfp4_chain():
     np.testing.assert_allclose(parts["s"][0, 0], ex["s"], rtol=2e-7, atol=0)
     np.testing.assert_array_equal(F.e2m1_decode(parts["qs"][0, 0]), ex["s_codes"])
     np.testing.assert_array_equal(F.ue4m3_decode(parts["sfs"][0, 0]), [ex["s_scale"]])
-    # expert output, stored BF16, carries gamma and the W2 scale: exactly +-2016
+    # expert output, stored FP16, carries gamma and the W2 scale: exactly +-2016
     np.testing.assert_array_equal(parts["y"][0, 0], ex["y"])
     np.testing.assert_array_equal(parts["out"][0], ex["out"])
 
 
 def test_hand_worked_requantisation_changes_s():
     """The same case with gamma = 0.35: the block scale of s rounds to 72, the codes stay
-    s / 24 and the dequantised s is 1.05 s, so y = bf16(+-2016 * 1.05) = +-2112: the
-    down GEMM reads the requantised s, and y is stored in BF16."""
+    s / 24 and the dequantised s is 1.05 s, so y = fp16(+-2016 * 1.05) = +-2116: the
+    down GEMM reads the requantised s, and y is stored in FP16."""
     g, inp = hand_worked()
     var = g["variant_gamma_0_35"]
     inp["gs_act2"] = np.array([var["gamma"]], dtype=np.float32)
@@ -112,14 +112,14 @@ def test_hand_worked_scale_placement_is_visible():
     twice = oracle.nvfp4_expert_rows(u / 448.0, wq, g["gamma"])
     assert np.max(np.abs(twice["s"][0] - ex["s"])) > 100
     s_deq_no_gamma = Q.dequantize(good["qs"], good["sfs"], 1.0)
-    y_no_gamma = F.bf16(oracle.expert_down(s_deq_no_gamma, wq["down"]))
+    y_no_gamma = F.fp16(oracle.expert_down(s_deq_no_gamma, wq["down"]))
     np.testing.assert_array_equal(y_no_gamma[0], np.array(ex["y"]) / g["gamma"])
 
 
 def test_nvfp4_equals_bf16_chain_on_representable_inputs():
     """On the hand-worked inputs every NVFP4 quantisation is exact (u, s and the weights
-    on their grids), and the BF16 chain stores the same values exactly (FP16 u, BF16 s
-    and y): the two chains give the same expert outputs and the same layer output."""
+    on their grids), and the BF16 experts' chain stores the same values exactly (FP16 u,
+    s and y): the two chains give the same expert outputs and the same layer output."""
     g, inp = hand_worked()
     a = oracle.moe_forward(inp, top_k=1, eps=0.0, act="bf16", expert="nvfp4", out="f32",
                            return_parts=True)
@@ -132,7 +132,7 @@ def test_nvfp4_equals_bf16_chain_on_representable_inputs():
 def test_stored_values_lie_on_their_grids():
     """On random inputs the chain stores u and y in their formats: u re-quantises to
     itself with its own per-token scale (it is an NVFP4 value, not the FP32 norm
-    output), and y is a BF16 value."""
+    output), and y is an FP16 value."""
     shape, view = small_nvfp4(2)
     parts = oracle.moe_forward(view, top_k=2, eps=shape.eps, act="bf16", expert="nvfp4",
                                out="f32", return_parts=True)
@@ -141,7 +141,7 @@ def test_stored_values_lie_on_their_grids():
     np.testing.assert_array_equal(Q.dequantize(q, sf, alpha), u)
     assert np.mean(u != parts["u32"]) > 0.5
     y = parts["y"]
-    np.testing.assert_array_equal(F.bf16(y), y)
+    np.testing.assert_array_equal(F.fp16(y), y)
 
 
 def grid_weights(rng, rows, K, beta, top_scale):
@@ -192,7 +192,7 @@ def small_nvfp4(seed=0):
 
 def test_down_scale_moves_only_beta2_and_cancels():
     """W_down of one expert times 2^3: its E2M1 codes and block scales are unchanged, its
-    global scale is 8x, y is 8x (exact in BF16), and the per-expert norm (eps = 0)
+    global scale is 8x, y is 8x (exact in FP16), and the per-expert norm (eps = 0)
     returns identical output."""
     shape, view = small_nvfp4()
     e = int(oracle.route(view, top_k=2, eps=0.0)[0][0, 0])    # an expert that is used

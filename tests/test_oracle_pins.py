@@ -352,13 +352,14 @@ def test_chain_stays_close_to_exact():
 
 
 def test_chain_stores_expert_outputs_where_the_kernels_do():
-    """The chain keeps y, the per-expert norm's input, on the BF16 grid for BF16 experts
-    (the format the SGLang page's fused post-per-expert norm stores) and in FP32 for FP32
+    """The chain keeps y, the per-expert norm's input, on the FP16 grid for BF16 experts
+    (and s too: every activation between the GEMMs is FP16 there) and in FP32 for FP32
     experts, and the norm then reads those stored values."""
     shape, inp = tiny(T=16, d=64, p=32, E=6, k=2, I=48, act="bf16", expert="bf16")
     parts = fwd(inp, shape, chain=True, return_parts=True)
     y = parts["y"]
-    assert np.array_equal(F.bf16(y), y)
+    assert np.array_equal(F.fp16(y), y) and not np.array_equal(F.bf16(y), y)
+    assert np.array_equal(F.fp16(parts["s"]), parts["s"])
     assert not np.array_equal(F.bf16(parts["u"]), parts["u"])      # u is FP16, finer
     shape32, inp32 = tiny(T=16, d=64, p=32, E=6, k=2, I=48)
     y32 = fwd(inp32, shape32, chain=True, return_parts=True)["y"]
