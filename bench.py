@@ -44,8 +44,10 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--nvfp4-pair", action="store_true",
-                    help="NVFP4 expert GEMMs on CTA pairs (MOE_FLAG_NVFP4_PAIR)")
+    ap.add_argument("--nvfp4-kernels", default="auto", choices=["auto", "pair", "one-cta"],
+                    help="NVFP4 expert GEMMs: the library's choice, both on CTA pairs "
+                         "(MOE_FLAG_NVFP4_PAIR) or both on single CTAs "
+                         "(MOE_FLAG_NVFP4_ONE_CTA)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="time only the headline workload")
     ap.add_argument("--no-boundary", action="store_true",
@@ -78,7 +80,7 @@ def bytes_per_token(s, act_bytes=2) -> dict:
     """Compulsory HBM bytes per token of the memory-bound stages (each operand read
     once, each result written once)."""
     k = s.top_k
-    yb = 4 if s.expert == "f32" else 2          # expert outputs y: BF16 unless FP32 experts
+    yb = 4 if s.expert == "f32" else 2          # expert outputs y: FP16 unless FP32 experts
     return {
         "norm": s.d * act_bytes + s.d * 4 + s.d * act_bytes,            # x in; h32, h16 out
         # pooled in; k rows of u out (NVFP4: codes + block scales + a per-row scale)
@@ -487,7 +489,8 @@ def run_ours(args):
     seed = rank_seed(args.seed, rank)
     experts = make_experts(shape, seed)
     from latent_moe_layer_rmsnorm_gb300 import _lib as nst
-    run_flags = nst.MOE_FLAG_NVFP4_PAIR if args.nvfp4_pair else 0
+    run_flags = {"auto": 0, "pair": nst.MOE_FLAG_NVFP4_PAIR,
+                 "one-cta": nst.MOE_FLAG_NVFP4_ONE_CTA}[args.nvfp4_kernels]
     run = Runner(shape, seed, experts, run_flags)
     layer, x, out, stream = run.layer, run.x, run.out, run.stream
     T = shape.T
@@ -652,6 +655,8 @@ def run_ours(args):
         "hbm_peak_gbs": hbm_peak,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
     }
+    if shape.expert == "nvfp4":
+        line["config"]["nvfp4_kernels"] = args.nvfp4_kernels
     if workloads:
         line["workloads"] = workloads
     if boundary is not None:

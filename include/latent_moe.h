@@ -78,8 +78,8 @@ typedef enum {
  *   expert MOE_BF16 or MOE_F32 (equal to act), or MOE_NVFP4 with act = MOE_BF16
  *          (then p and I must be multiples of 256)
  *   out    MOE_BF16 or MOE_F32: dtype of the layer output
- *   flags  0 or MOE_FLAG_TEST_TIMEOUT, MOE_FLAG_WEIGHT_TILES, MOE_FLAG_NVFP4_PAIR
- *          (other bits must be zero) */
+ *   flags  0 or MOE_FLAG_TEST_TIMEOUT, MOE_FLAG_WEIGHT_TILES, one of MOE_FLAG_NVFP4_PAIR
+ *          and MOE_FLAG_NVFP4_ONE_CTA (other bits must be zero) */
 /* Test hook for the error path: the gate/up GEMM never issues its first operand load,
  * so its MMA wait runs out after 20 ms; the call's kernels then end early and
  * moe_read_status reports MOE_ERR_TIMEOUT.  Outputs are undefined.  Tests only. */
@@ -90,12 +90,18 @@ typedef enum {
  * tile of each expert, but on a GB300 the expert GEMMs are bound by operand delivery
  * into shared memory, not by MMA work, and the default is faster at prefill sizes. */
 #define MOE_FLAG_WEIGHT_TILES 0x40000000u
-/* NVFP4 experts: run the expert GEMMs on CTA pairs over 256 x 256 output tiles (each
- * CTA of a pair stages half of the weight tile, so fewer bytes per MAC reach its shared
- * memory) instead of the default one CTA per 128 x 256 tile.  Same results, bit for bit;
- * on a GB300 the pairs measure about half as fast (their per-stage hand-off of the block
- * scales between the two CTAs limits them), so they are not the default. */
+/* NVFP4 experts, kernel choice.  The expert GEMMs run either on one CTA per 128 x 256
+ * output tile or on CTA pairs over 256 x 256 tiles (each CTA of a pair stages half of
+ * the weight tile, so fewer bytes per MAC reach its shared memory).  Results are the
+ * same, bit for bit.  By default the gate/up GEMM runs on single CTAs and the down GEMM
+ * on pairs when T * top_k >= 256 * E (a full 256-row pair tile per expert on average),
+ * else on single CTAs: measured on a GB300 at T = 16384, d = 8192, p = I = 4096, E = 256,
+ * k = 8, the pairs take the down GEMM from 1.26 to 1.07 ms while the gate/up GEMM, whose
+ * SwiGLU + requantisation epilogue is longer, is faster on single CTAs (2.16 against
+ * 2.28 ms).  MOE_FLAG_NVFP4_PAIR puts both GEMMs on pairs, MOE_FLAG_NVFP4_ONE_CTA both on
+ * single CTAs; setting both is an error. */
 #define MOE_FLAG_NVFP4_PAIR 0x20000000u
+#define MOE_FLAG_NVFP4_ONE_CTA 0x10000000u
 typedef struct {
   int32_t T, d, p, E, top_k, I;
   float eps;

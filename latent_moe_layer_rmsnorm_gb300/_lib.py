@@ -27,6 +27,7 @@ MOE_NVFP4 = 2
 MOE_FLAG_TEST_TIMEOUT = 0x80000000
 MOE_FLAG_WEIGHT_TILES = 0x40000000
 MOE_FLAG_NVFP4_PAIR = 0x20000000
+MOE_FLAG_NVFP4_ONE_CTA = 0x10000000
 
 PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL, PACK_SF13, PACK_SF2, PACK_GS13, \
     PACK_GS2 = range(9)

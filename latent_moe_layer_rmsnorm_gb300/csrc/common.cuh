@@ -345,6 +345,25 @@ __device__ __forceinline__ float stored_value(float v, int fmt) {
   return v;
 }
 
+// ss + the sum of squares of 16 values as stored in format `fmt`, one branch on the
+// format for all 16 (the format is the same for every thread of a launch).
+__device__ __forceinline__ float add_stored_squares(float ss, const float (&v)[16], int fmt) {
+  if (fmt == OUT_F16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) { const float q = __half2float(__float2half_rn(v[i])); ss = fmaf(q, q, ss); }
+  } else if (fmt == OUT_BF16) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float q = __bfloat162float(__float2bfloat16_rn(v[i]));
+      ss = fmaf(q, q, ss);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ss = fmaf(v[i], v[i], ss);
+  }
+  return ss;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

@@ -111,18 +111,18 @@ __device__ __forceinline__ void nvf4_scalars(const GemmParams& P, const TileCoor
   }
 }
 
-// One warp's 32 rows of one 128-column half `hh` of the tile (taddr points at the
-// half's first column); x0, x1 from nvf4_scalars.
+// One warp's 32 rows of one 128-column block of the accumulator (taddr points at its
+// first column); `col0` is the block's first output column: of s (64 SwiGLU outputs per
+// block) for the gate/up GEMM, of y for the down GEMM.  x0, x1 from nvf4_scalars.
 template <int EPI>
 __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoord& tc,
-                                              uint32_t taddr, int r, int hh, const float* recip,
+                                              uint32_t taddr, int r, int col0, const float* recip,
                                               const CUtensorMap* tmY, uint8_t* ybox, float x0,
                                               float x1) {
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
-    // columns [0, 64) of the half gate, [64, 128) up, of output features
-    // n_blk * 128 + hh * 64 ..
+    // columns [0, 64) of the block gate, [64, 128) up, of output features col0 ..
     const float sc = x0;
     const float gam = x1;
     const float six_g = 6.0f * gam;
@@ -158,7 +158,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       if (row_ok && !(fmaxf(ratio0, ratio1) <= 464.f && fin == 0.f))
         report_error(P.status, ST_DEVICE_CHECK, CHECK_S_RANGE);
       if (row_ok) {
-        const int col = tc.n_blk * (NV_BN / 2) + hh * 64 + c0;
+        const int col = col0 + c0;
         *reinterpret_cast<uint4*>(codes + col / 2) = make_uint4(q0.x, q0.y, q1.x, q1.y);
         P.out_sf[sf_offset(row, col / 16, I)] = static_cast<uint8_t>(code0);
         P.out_sf[sf_offset(row, col / 16 + 1, I)] = static_cast<uint8_t>(code1);
@@ -198,11 +198,11 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0)
-        tma_store_2d(tmY, ybox, tc.n_blk * NV_BN + hh * 128 + c0, tc.a_row + (r - lane));
+        tma_store_2d(tmY, ybox, col0 + c0, tc.a_row + (r - lane));
 #pragma unroll
       for (int i = 0; i < 64; ++i) { const float q = stored_value(v[i], OUT_F16); ss = fmaf(q, q, ss); }
     }
-    if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + 2 * tc.n_blk + hh] = ss;
+    if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + (col0 >> 7)] = ss;
   }
 }
 
@@ -401,7 +401,9 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + hh * 128 + (static_cast<uint32_t>(q * 32) << 16);
-      nvf4_epilogue<EPI>(P, tc, taddr, r, hh, N->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
+      const int col0 = EPI == NV_EPI_SWIGLU_Q ? tc.n_blk * (NV_BN / 2) + hh * 64
+                                              : tc.n_blk * NV_BN + hh * 128;
+      nvf4_epilogue<EPI>(P, tc, taddr, r, col0, N->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
                          x0, x1);
       tc_fence_before();
       __syncwarp();

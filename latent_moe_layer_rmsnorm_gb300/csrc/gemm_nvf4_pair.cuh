@@ -7,8 +7,19 @@
 // its own shared memory, the leader (rank 0) issues M = 256, N = 256 block-scaled MMAs
 // that read both halves, and each CTA's TMEM receives its 128 rows x 256 columns.  Per
 // CTA and K slice (256 FP4 values) that is 16 KB of A, 16 KB of B and 6 KB of scale
-// chunks for 128 x 256 x 256 MACs, against 54 KB on one CTA: the single-CTA kernel is
-// bound by the rate TMA fills shared memory, so fewer bytes per MAC are what move it.
+// chunks for 128 x 256 x 256 MACs, against 54 KB on one CTA.
+//
+// Measured on a GB300 at a prefill chunk (131072 expert rows over 256 experts, p = I =
+// 4096): the down GEMM takes 1.07 ms on pairs against 1.26 ms on single CTAs, the gate/up
+// GEMM 2.28 against 2.16 ms (its SwiGLU + requantisation epilogue is longer, and with
+// one accumulator the MMAs wait for it).  Timing copies with parts removed show what
+// bounds both: without epilogues the gate/up GEMM takes 1.76 ms on pairs and 1.69 ms on
+// single CTAs, without MMAs as well 1.57 and 1.41 ms.  Operand delivery, not the tensor
+// pipe, sets the pace, and a stage takes about as long on a pair (38 KB per CTA) as on
+// one CTA (54 KB), about 850 clocks: the round trip of a ring slot through the barriers
+// of both CTAs, more than its bytes, is the limit.  A 256 x 128 variant with two
+// accumulators (the epilogue under the next tile's MMAs) measured slower still (3.2 ms):
+// half the MACs per stage at the same round trip.
 //
 // Scales: each CTA's TMEM holds the scales of its own 128 A rows and of all 256 B
 // columns (the placement the pair MMA reads), so each CTA bulk-copies its own A scale
@@ -82,6 +93,17 @@ __device__ __forceinline__ void mma_issue_nvf4_pair(uint32_t d_tmem, uint64_t ad
       "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(scale_a), "r"(scale_b), "r"(accumulate)
       : "memory");
+}
+
+// Arrive on the leader's barrier from either CTA of the pair with the default (CTA) scope
+// of the release.  What these arrivals publish is TMEM that tcgen05 operations completed
+// before the arrive (tcgen05.wait::st / wait::ld) and that only the tensor core touches
+// next, so no write of generic memory has to become visible to the other CTA: a release
+// at cluster scope (a cluster-wide memory fence per stage and warp) measured as the
+// bottleneck of the pipeline (ncu: 4.5 membar stalls per issued instruction, the kernel
+// at half the one-CTA kernel's speed).
+__device__ __forceinline__ void mbar_arrive_cluster_addr(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Pair tile t -> this CTA's rows.  `half`: the tile's second CTA holds no rows of the
@@ -301,7 +323,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV_THREADS, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(ready + stage * 8);
+        if (lane == 0) {
+          if (leader) mbar_arrive(&S->sf_ready[stage]);
+          else mbar_arrive_cluster_addr(ready + stage * 8);
+        }
         if (++stage == NVP_STAGES) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
@@ -324,12 +349,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV_THREADS, 1)
         break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + hh * 128 + (static_cast<uint32_t>(q * 32) << 16);
+      const int col0 = EPI == NV_EPI_SWIGLU_Q ? tc.n_blk * (NV_BN / 2) + hh * 64
+                                              : tc.n_blk * NV_BN + hh * 128;
       if (tc.valid > 0)
-        nvf4_epilogue<EPI>(P, tc, taddr, r, hh, S->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
+        nvf4_epilogue<EPI>(P, tc, taddr, r, col0, S->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
                            x0, x1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(tempty);
+      if (lane == 0) {
+        if (leader) mbar_arrive(&S->tempty);
+        else mbar_arrive_cluster_addr(tempty);
+      }
     }
     if (EPI == NV_EPI_STORE_Y && lane == 0) tma_store_wait_all();   // y fully written
   }

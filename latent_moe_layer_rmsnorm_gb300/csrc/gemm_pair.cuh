@@ -196,10 +196,8 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
         store16(P.out, base + c0 + 16, P.out_fmt, vb);
       }
       const int rb = P.out_fmt;                    // squared as stored
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
-#pragma unroll
-      for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], rb); ss = fmaf(q, q, ss); }
+      ss = add_stored_squares(ss, va, rb);
+      ss = add_stored_squares(ss, vb, rb);
     }
     // same column order as the full-tile epilogue, so the block sums agree bit for bit
     if (P.row_ssq && row_ok)
@@ -212,17 +210,22 @@ __device__ __forceinline__ void pair_small_epilogue(const GemmParams& P, const T
 __device__ __forceinline__ void box_put16(uint8_t* box, int lane, int off, int fmt,
                                           const float (&v)[16]) {
   uint8_t* row = box + lane * 128;
-  if (fmt == OUT_BF16 || fmt == OUT_F16) {
-    const bool h16 = fmt == OUT_F16;
+  if (fmt == OUT_F16) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int j = (off >> 4) + h;
       const float* w = v + 8 * h;
-      uint4 o;
-      o.x = h16 ? pack_f16x2(w[0], w[1]) : pack_bf16x2(w[0], w[1]);
-      o.y = h16 ? pack_f16x2(w[2], w[3]) : pack_bf16x2(w[2], w[3]);
-      o.z = h16 ? pack_f16x2(w[4], w[5]) : pack_bf16x2(w[4], w[5]);
-      o.w = h16 ? pack_f16x2(w[6], w[7]) : pack_bf16x2(w[6], w[7]);
+      const uint4 o = make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]),
+                                 pack_f16x2(w[4], w[5]), pack_f16x2(w[6], w[7]));
+      *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
+    }
+  } else if (fmt == OUT_BF16) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = (off >> 4) + h;
+      const float* w = v + 8 * h;
+      const uint4 o = make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]),
+                                 pack_bf16x2(w[4], w[5]), pack_bf16x2(w[6], w[7]));
       *reinterpret_cast<uint4*>(row + ((j ^ (lane & 7)) << 4)) = o;
     }
   } else {
@@ -278,10 +281,8 @@ __device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const T
       put(col_base + c0 + 16, vb, col_base);
       if (P.row_ssq) {                                // squared as stored
         const int rb = P.out_fmt;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], rb); ss = fmaf(q, q, ss); }
+        ss = add_stored_squares(ss, va, rb);
+        ss = add_stored_squares(ss, vb, rb);
         if (((c0 + 32) & 127) == 0) {
           P.row_ssq[row * (P.N >> 7) + ((col_base + c0) >> 7)] = ss;
           ss = 0.f;

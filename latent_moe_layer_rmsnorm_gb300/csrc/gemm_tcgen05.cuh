@@ -219,10 +219,8 @@ __device__ __forceinline__ void gemm_epilogue(const GemmParams& P, const TileCoo
       }
       if (P.row_ssq) {          // expert outputs (bn is 128 or 256), squared as stored
         const int rb = P.out_fmt;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) { const float q = stored_value(va[i], rb); ss = fmaf(q, q, ss); }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) { const float q = stored_value(vb[i], rb); ss = fmaf(q, q, ss); }
+        ss = add_stored_squares(ss, va, rb);
+        ss = add_stored_squares(ss, vb, rb);
         if (((c0 + 32) & 127) == 0) {
           if (row_ok)
             P.row_ssq[row * (P.N >> 7) + ((tc.n_blk * P.bn + c0) >> 7)] = ss;

@@ -179,7 +179,10 @@ moe_status_t validate(const moe_config_t* c) {
   } else if (c->expert != c->act) {
     return MOE_ERR_UNSUPPORTED;
   }
-  if ((c->flags & ~(MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_WEIGHT_TILES | MOE_FLAG_NVFP4_PAIR)) != 0)
+  if ((c->flags & ~(MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_WEIGHT_TILES | MOE_FLAG_NVFP4_PAIR |
+                    MOE_FLAG_NVFP4_ONE_CTA)) != 0)
+    return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_NVFP4_PAIR) && (c->flags & MOE_FLAG_NVFP4_ONE_CTA))
     return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED;
   if (c->d % 128 || c->p % 128 || c->I % 128) return MOE_ERR_UNSUPPORTED;
@@ -538,7 +541,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = s_buf; P.ld_out = I;
     P.sf_a = sf_u; P.sf_b = W->sf13; P.row_scale = alpha; P.grp_scale = W->gs13;
     P.out_scale = W->gs_act2; P.out_sf = sf_s;
-    if (!(c.flags & MOE_FLAG_NVFP4_PAIR)) {
+    if (!(c.flags & MOE_FLAG_NVFP4_PAIR)) {   // default: one CTA per 128 x 256 tile
       const int grid = std::min(sms, max_mt * (2 * I / NV_BN));
       MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_SWIGLU_Q>, dim3(grid), dim3(NV_THREADS),
                           nvf4_smem_bytes(), st, ta, tb, ta, P));
@@ -610,7 +613,11 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.row_off = row_off; P.mt_off = mt_off; P.row_cnt = row_cnt;
     P.out = y_buf; P.ld_out = p; P.row_ssq = ssq;
     P.sf_a = sf_s; P.sf_b = W->sf2; P.grp_scale = W->gs2; P.out_scale = W->gs_act2;
-    if (!(c.flags & MOE_FLAG_NVFP4_PAIR)) {
+    // pairs by default once the experts average a full 256-row pair tile
+    const bool pair = (c.flags & MOE_FLAG_NVFP4_PAIR) ||
+                      (!(c.flags & MOE_FLAG_NVFP4_ONE_CTA) &&
+                       static_cast<int64_t>(c.T) * c.top_k >= int64_t(256) * E_);
+    if (!pair) {
       const int grid = std::min(sms, max_mt * (p / NV_BN));
       MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_STORE_Y>, dim3(grid), dim3(NV_THREADS),
                           nvf4_smem_bytes(), st, ta, tb, ty, P));

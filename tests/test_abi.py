@@ -45,7 +45,8 @@ def test_workspace_size_and_validation():
     assert L.moe_workspace_size(cfg(T=0)) > 0
     bad = [dict(top_k=9), dict(top_k=0), dict(E=0), dict(E=300), dict(d=200), dict(p=96),
            dict(I=100), dict(act=7), dict(out=2), dict(eps=-1.0), dict(flags=1),
-           dict(expert=L.MOE_F32), dict(T=-1), dict(top_k=9, E=8)]
+           dict(expert=L.MOE_F32), dict(T=-1), dict(top_k=9, E=8),
+           dict(flags=L.MOE_FLAG_NVFP4_PAIR | L.MOE_FLAG_NVFP4_ONE_CTA)]
     for b in bad:
         assert L.moe_workspace_size(cfg(**b)) == 0, b
 

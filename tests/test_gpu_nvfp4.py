@@ -179,16 +179,19 @@ def test_nvfp4_stages_and_layer(shape):
 @pytest.mark.parametrize("shape", [SMALL, MID, DECODE_LIKE], ids=lambda s: s.name)
 def test_pair_kernel_matches_one_cta_kernel(shape):
     """The CTA-pair NVFP4 GEMMs (MOE_FLAG_NVFP4_PAIR: 256 x 256 tiles, each CTA staging
-    half of the weight tile) against the one-CTA kernels (the default) on the same
-    inputs: requantised SwiGLU codes and scales, expert outputs and the layer output.
-    The shapes give experts with an odd number of 128-row blocks, whose last pair tile
-    has rows in one CTA only, and (decode-like) experts of one or two rows."""
+    half of the weight tile) against the one-CTA kernels (MOE_FLAG_NVFP4_ONE_CTA) on the
+    same inputs: requantised SwiGLU codes and scales, expert outputs and the layer
+    output; the default choice (one CTA for gate/up, pairs for the down GEMM once the
+    experts average 256 rows) gives the same output.  The shapes give experts with an
+    odd number of 128-row blocks, whose last pair tile has rows in one CTA only, and
+    (decode-like) experts of one or two rows."""
     need_gpu()
     from latent_moe_layer_rmsnorm_gb300 import _lib as L
     inp, dev, layer = build(shape, 2)
     T, I = shape.T, shape.I
     x = dev["x"]
-    one = layer.forward(x).clone()
+    auto = layer.forward(x).clone()
+    one = layer.forward(x, flags=L.MOE_FLAG_NVFP4_ONE_CTA).clone()
     s_one = layer.intermediate("s", T)
     sf_one = layer.intermediate("sf_s", T)
     y_one = layer.intermediate("y", T)
@@ -215,3 +218,4 @@ def test_pair_kernel_matches_one_cta_kernel(shape):
     # same operands, same K order per output element: the pair MMA gives the same sums
     assert same_s and same_sf and same_y
     assert torch.equal(pair, one)
+    assert torch.equal(auto, one)
