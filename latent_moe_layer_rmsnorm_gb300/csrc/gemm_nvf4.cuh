@@ -114,39 +114,44 @@ __device__ __forceinline__ void nvf4_scalars(const GemmParams& P, const TileCoor
 // One warp's 32 rows of one 128-column block of the accumulator (taddr points at its
 // first column); `col0` is the block's first output column: of s (64 SwiGLU outputs per
 // block) for the gate/up GEMM, of y for the down GEMM.  x0, x1 from nvf4_scalars.
-template <int EPI>
+// `release()` is called once by every thread as soon as its last TMEM read has completed,
+// before the rest of the epilogue, so the MMAs of the next tile can start under it: the
+// gate/up GEMM holds the 64 SwiGLU values of its row in registers and requantises them
+// after the release; the down GEMM releases after its last accumulator load.
+template <int EPI, typename Release>
 __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoord& tc,
                                               uint32_t taddr, int r, int col0, const float* recip,
                                               const CUtensorMap* tmY, uint8_t* ybox, float x0,
-                                              float x1) {
+                                              float x1, Release&& release) {
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
     // columns [0, 64) of the block gate, [64, 128) up, of output features col0 ..
     const float sc = x0;
     const float gam = x1;
+    float sv[64];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      uint32_t g[16], u[16];
+      tmem_ld16(taddr + c0, g);
+      tmem_ld16(taddr + 64 + c0, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a = __uint_as_float(g[i]) * sc, b = __uint_as_float(u[i]) * sc;
+        sv[c0 + i] = __fdividef(a, 1.0f + __expf(-a)) * b;   // silu(a) * b
+      }
+    }
+    release();
     const float six_g = 6.0f * gam;
     const float inv_g = gam > 0.f ? 1.0f / gam : 0.f;
     const int I = P.ld_out;
     uint8_t* codes = static_cast<uint8_t*>(P.out) + row * (I / 2);
-    // 32 output columns (two quantisation blocks) per TMEM wait: the two blocks' SwiGLU
-    // and quantisation chains are independent, so one warp overlaps them
-#pragma unroll 1
-    for (int c0 = 0; c0 < 64; c0 += 32) {
-      uint32_t g0[16], g1[16], u0[16], u1[16];
-      tmem_ld16(taddr + c0, g0);
-      tmem_ld16(taddr + c0 + 16, g1);
-      tmem_ld16(taddr + 64 + c0, u0);
-      tmem_ld16(taddr + 64 + c0 + 16, u1);
-      tmem_ld_wait();
-      float s0[16], s1[16];
+    // two quantisation blocks at a time: their chains are independent
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float a0 = __uint_as_float(g0[i]) * sc, b0 = __uint_as_float(u0[i]) * sc;
-        const float a1 = __uint_as_float(g1[i]) * sc, b1 = __uint_as_float(u1[i]) * sc;
-        s0[i] = __fdividef(a0, 1.0f + __expf(-a0)) * b0;   // silu(a) * b
-        s1[i] = __fdividef(a1, 1.0f + __expf(-a1)) * b1;
-      }
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      const float(&s0)[16] = *reinterpret_cast<const float(*)[16]>(sv + c0);
+      const float(&s1)[16] = *reinterpret_cast<const float(*)[16]>(sv + c0 + 16);
       uint2 q0, q1;
       float ratio0, ratio1, fin = 0.f;
       const uint32_t code0 = quantize16(s0, six_g, inv_g, q0, recip, &ratio0);
@@ -167,7 +172,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
   } else {
     const float sc = x0;
     const int lane = r & 31;
-    float ss = 0.f;     // the half is one 128-column block of the row (row_ssq)
+    float ss = 0.f;     // the block is one 128-column block of the row (row_ssq)
     // one 32-row x 64-column FP16 staging box per TMEM wait: row `lane`, 16-byte chunk j
     // (columns 8j..8j+7) at chunk (j ^ lane % 8), the 128-byte swizzle of the tensor map
 #pragma unroll 1
@@ -178,6 +183,7 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
       tmem_ld16(taddr + c0 + 32, a2);
       tmem_ld16(taddr + c0 + 48, a3);
       tmem_ld_wait();
+      if (c0 == 64) release();
       float v[64];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -404,10 +410,11 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
       const int col0 = EPI == NV_EPI_SWIGLU_Q ? tc.n_blk * (NV_BN / 2) + hh * 64
                                               : tc.n_blk * NV_BN + hh * 128;
       nvf4_epilogue<EPI>(P, tc, taddr, r, col0, N->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
-                         x0, x1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S->tempty[0]);
+                         x0, x1, [&] {
+                           tc_fence_before();
+                           __syncwarp();
+                           if (lane == 0) mbar_arrive(&S->tempty[0]);
+                         });
     }
     if (EPI == NV_EPI_STORE_Y && lane == 0) tma_store_wait_all();   // y fully written
   }

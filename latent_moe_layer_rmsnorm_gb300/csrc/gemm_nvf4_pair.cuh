@@ -351,15 +351,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV_THREADS, 1)
       const uint32_t taddr = tmem_base + hh * 128 + (static_cast<uint32_t>(q * 32) << 16);
       const int col0 = EPI == NV_EPI_SWIGLU_Q ? tc.n_blk * (NV_BN / 2) + hh * 64
                                               : tc.n_blk * NV_BN + hh * 128;
+      auto release = [&] {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&S->tempty);
+          else mbar_arrive_cluster_addr(tempty);
+        }
+      };
       if (tc.valid > 0)
         nvf4_epilogue<EPI>(P, tc, taddr, r, col0, S->recip, &tmY, sY + (hh * 4 + q) * NV_Y_BOX,
-                           x0, x1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(&S->tempty);
-        else mbar_arrive_cluster_addr(tempty);
-      }
+                           x0, x1, release);
+      else
+        release();
     }
     if (EPI == NV_EPI_STORE_Y && lane == 0) tma_store_wait_all();   // y fully written
   }

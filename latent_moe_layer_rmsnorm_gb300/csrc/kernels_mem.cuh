@@ -785,16 +785,32 @@ __global__ void pack_w13_kernel(const void* __restrict__ gate, const void* __res
 // ---- split-K reductions ----------------------------------------------------------------
 // out[i] = sum over s of part[s * n + i], in slice order (deterministic), written as FP32,
 // BF16 or TF32-rounded FP32.  n % 4 == 0.
+constexpr int SPLITK_BATCH = 8;
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int ksplit, size_t n,
                                      void* __restrict__ out, int fmt) {
   pdl_wait();
   pdl_allow_next();
   for (size_t i = (blockIdx.x * size_t(blockDim.x) + threadIdx.x) * 4; i < n;
        i += size_t(gridDim.x) * blockDim.x * 4) {
-    // slices in groups of 4 (loads in flight together), summed in a fixed order
+    // the first SPLITK_BATCH slices' loads all in flight, then the sums in a fixed order:
+    // groups of 4 summed pairwise and added in slice order, then single slices
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    for (; s + 4 <= ksplit; s += 4) {
+    float4 v[SPLITK_BATCH];
+#pragma unroll
+    for (int s = 0; s < SPLITK_BATCH; ++s)
+      if (s < ksplit) v[s] = *reinterpret_cast<const float4*>(part + s * n + i);
+    const int full = ksplit / 4 * 4;
+#pragma unroll
+    for (int s = 0; s < SPLITK_BATCH; s += 4) {
+      if (s + 4 <= full) {
+        acc.x += (v[s].x + v[s + 1].x) + (v[s + 2].x + v[s + 3].x);
+        acc.y += (v[s].y + v[s + 1].y) + (v[s + 2].y + v[s + 3].y);
+        acc.z += (v[s].z + v[s + 1].z) + (v[s + 2].z + v[s + 3].z);
+        acc.w += (v[s].w + v[s + 1].w) + (v[s + 2].w + v[s + 3].w);
+      }
+    }
+    int s = SPLITK_BATCH < full ? SPLITK_BATCH : full;
+    for (; s + 4 <= full; s += 4) {
       const float4 v0 = *reinterpret_cast<const float4*>(part + (s + 0) * n + i);
       const float4 v1 = *reinterpret_cast<const float4*>(part + (s + 1) * n + i);
       const float4 v2 = *reinterpret_cast<const float4*>(part + (s + 2) * n + i);
@@ -804,9 +820,14 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int ksplit,
       acc.z += (v0.z + v1.z) + (v2.z + v3.z);
       acc.w += (v0.w + v1.w) + (v2.w + v3.w);
     }
-    for (; s < ksplit; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(part + s * n + i);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+#pragma unroll
+    for (int j = 0; j < SPLITK_BATCH; ++j)     // single slices after the groups, in order
+      if (j >= full && j < ksplit) {
+        acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+      }
+    for (s = full > SPLITK_BATCH ? full : SPLITK_BATCH; s < ksplit; ++s) {
+      const float4 w = *reinterpret_cast<const float4*>(part + s * n + i);
+      acc.x += w.x; acc.y += w.y; acc.z += w.z; acc.w += w.w;
     }
     if (fmt == 0) {          // BF16
       uint2 o;
@@ -824,49 +845,37 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int ksplit,
 
 // Router logits from split-K partials [ksplit][T][ld] (sum in slice order), then the
 // top-k (descending, ties to the lower id) and the softmax over the chosen logits.
-// One warp per token; lane l owns experts l, l+32, ...
-__global__ void router_reduce_topk_kernel(const float* __restrict__ part, int ksplit, int T,
-                                          int ld, int E, int k, int32_t* __restrict__ ids,
-                                          float* __restrict__ wts) {
+// One block of 256 threads per token: thread e sums expert e's slices (every load in
+// flight at once, ksplit <= ROUTER_MAX_SPLIT), then warp 0 picks the top k, lane l
+// holding experts l, l+32, ...
+constexpr int ROUTER_MAX_SPLIT = 32;
+__global__ void __launch_bounds__(256)
+    router_reduce_topk_kernel(const float* __restrict__ part, int ksplit, int T, int ld, int E,
+                              int k, int32_t* __restrict__ ids, float* __restrict__ wts) {
   pdl_wait();
   pdl_allow_next();
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (t >= T) return;
+  __shared__ float logit[256];
+  const int t = blockIdx.x;
+  const int e = threadIdx.x;
+  float sum = 0.f;
+  if (e < E) {
+    const float* p = part + size_t(t) * ld + e;
+    const size_t stride = size_t(T) * ld;
+    float q[ROUTER_MAX_SPLIT];
+#pragma unroll
+    for (int s = 0; s < ROUTER_MAX_SPLIT; ++s) q[s] = s < ksplit ? p[s * stride] : 0.f;
+#pragma unroll
+    for (int s = 0; s < ROUTER_MAX_SPLIT; ++s)
+      if (s < ksplit) sum += q[s];
+  }
+  logit[e] = sum;
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   constexpr int PER = 8;                 // E <= 256
   float v[PER];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) v[j] = 0.f;
-  // this lane's experts of four slices at a time: 32 independent loads in flight, then
-  // the sums in slice order
-  int s = 0;
-  for (; s + 4 <= ksplit; s += 4) {
-    float q[4][PER];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float* row = part + (size_t(s + u) * T + t) * ld;
-#pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const int e = lane + 32 * j;
-        q[u][j] = e < E ? row[e] : 0.f;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int j = 0; j < PER; ++j) v[j] += q[u][j];
-  }
-  for (; s < ksplit; ++s) {
-    const float* row = part + (size_t(s) * T + t) * ld;
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane + 32 * j;
-      if (e < E) v[j] += row[e];
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < PER; ++j)
-    if (lane + 32 * j >= E) v[j] = -INFINITY;
+  for (int j = 0; j < PER; ++j) v[j] = lane + 32 * j < E ? logit[lane + 32 * j] : -INFINITY;
   // k rounds of warp arg-max: larger logit wins, equal logits go to the lower id
   float chosen[MAX_TOPK];
   int chosen_id[MAX_TOPK];

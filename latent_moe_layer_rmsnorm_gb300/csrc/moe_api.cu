@@ -214,7 +214,7 @@ SplitPlan split_plan(const moe_config_t& c) {
   SplitPlan sp{};
   const int Ep = (c.E + 15) / 16 * 16;
   const bool f32 = c.act == MOE_F32;
-  sp.router = std::min(split_for(c.T, Ep, Ep, c.d, 32), 32);
+  sp.router = std::min(split_for(c.T, Ep, Ep, c.d, 32), ROUTER_MAX_SPLIT);
   sp.pool = split_for(c.T, c.p, bn_for(c.p), c.d, f32 ? 32 : 64);
   sp.unpool = split_for(c.T, c.d, bn_for(c.d), c.p, f32 ? 32 : 64);
   size_t m = 0;
@@ -423,17 +423,22 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   float* part = reinterpret_cast<float*>(base + L.part);
   if (internal_route) {
     const int bn = (E_ + 15) / 16 * 16;
+    // split-K partial logits: 128-column tiles when they divide the experts, so twice the
+    // CTAs share the 8 MiB GEMV at E = 256
+    const int bn_split = bn % 128 == 0 ? 128 : bn;
     CUtensorMap ta, tb;
     if (!make_tmap(&ta, h32, OP_TF32, d, T, GEMM_BM) ||
-        !make_tmap(&tb, W->w_router, OP_TF32, d, E_, bn))
+        !make_tmap(&tb, W->w_router, OP_TF32, d, E_, sp.router > 1 ? bn_split : bn))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = bn; P.K = d; P.bn = bn; P.groups = 0;
     if (sp.router > 1) {     // small T: K slices -> partial logits -> sum + top-k
+      P.bn = bn_split;
       P.ksplit = sp.router; P.split_stride = size_t(T) * bn;
       P.out = part; P.ld_out = bn; P.out_fmt = OUT_F32;
-      MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, std::min(sms, mtiles * sp.router), st)));
-      MOE_TRY(launch_step(router_reduce_topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, part,
+      MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(
+          ta, tb, P, std::min(sms, mtiles * (bn / bn_split) * sp.router), st)));
+      MOE_TRY(launch_step(router_reduce_topk_kernel, dim3(T), dim3(256), 0, st, part,
                           sp.router, T, bn, E_, k, ids, wts));
     } else if (bn == 256) {   // CTA pairs: each CTA loads 128 of the 256 router rows
       P.E = E_; P.top_k = k; P.ids = ids; P.wts = wts;
@@ -938,20 +943,22 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_weights_t* W, 
     norm_in_kernel<false><<<c.T, MEM_THREADS, 0, st>>>(x, W->g_in, h32, nullptr, c.d, c.eps, status);
   MOE_TRY(last_launch());
   const int bn = (c.E + 15) / 16 * 16;
+  const int ks = noalloc_router_split(c);
+  const int bn_split = bn % 128 == 0 ? 128 : bn;   // as in moe_forward's split router
   CUtensorMap ta, tb;
   if (!make_tmap(&ta, h32, OP_TF32, c.d, c.T, GEMM_BM) ||
-      !make_tmap(&tb, W->w_router, OP_TF32, c.d, c.E, bn))
+      !make_tmap(&tb, W->w_router, OP_TF32, c.d, c.E, ks > 1 ? bn_split : bn))
     return MOE_ERR_CUDA;
   GemmParams P = base_params(status, c.flags);
   P.M = c.T; P.N = bn; P.K = c.d; P.bn = bn; P.groups = 0;
   const int mtiles = (c.T + GEMM_BM - 1) / GEMM_BM;
-  const int ks = noalloc_router_split(c);
   if (ks > 1) {     // small T: K slices -> partial logits in the array -> sum + top-k
+    P.bn = bn_split;
     P.ksplit = ks; P.split_stride = size_t(c.T) * bn;
     P.out = part; P.ld_out = bn; P.out_fmt = OUT_F32;
-    MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, std::min(sms, mtiles * ks), st)));
-    router_reduce_topk_kernel<<<(c.T + 7) / 8, 256, 0, st>>>(part, ks, c.T, bn, c.E, c.top_k,
-                                                             ids, w);
+    MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P,
+                                             std::min(sms, mtiles * (bn / bn_split) * ks), st)));
+    router_reduce_topk_kernel<<<c.T, 256, 0, st>>>(part, ks, c.T, bn, c.E, c.top_k, ids, w);
     return last_launch();
   }
   P.E = c.E; P.top_k = c.top_k; P.ids = ids; P.wts = w;
