@@ -125,6 +125,10 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
                                               float x1, Release&& release) {
   const bool row_ok = r < tc.valid;
   const size_t row = static_cast<size_t>(tc.a_row + r);
+  if (r - (r & 31) >= tc.valid) {   // the warp's 32 rows are all padding: nothing to store
+    release();
+    return;
+  }
   if constexpr (EPI == NV_EPI_SWIGLU_Q) {
     // columns [0, 64) of the block gate, [64, 128) up, of output features col0 ..
     const float sc = x0;

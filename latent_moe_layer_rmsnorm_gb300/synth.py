@@ -75,10 +75,15 @@ PREFILL_EIGHTH_BF16 = Shape("prefill_eighth_bf16", T=2048, d=8192, p=4096, E=32,
 BOUNDARY_BF16 = Shape("boundary_bf16", T=4096, d=8192, p=256, E=8, top_k=2, I=256)
 # Decode with NVFP4 experts: the weight stream is 4.5 bits per weight instead of 16.
 DECODE_NVFP4 = DECODE_BF16.replace(name="decode_nvfp4", expert="nvfp4")
+# Decode with narrow experts (I = 256): the norm, router, pooler, dispatch, combine and
+# unpooler see exactly the decode batch's shapes, with ~1.7 GB on the device, for full
+# profiler captures of those kernels.
+DECODE_SLICE_BF16 = DECODE_BF16.replace(name="decode_slice_bf16", I=256)
 
 WORKLOADS = {s.name: s for s in (TINY_F32, PREFILL_BF16, DECODE_BF16, PREFILL_NVFP4,
                                  SKEWED_BF16, PREFILL_SLICE_BF16, PREFILL_SLICE_NVFP4,
-                                 DECODE_NVFP4, PREFILL_EIGHTH_BF16, BOUNDARY_BF16)}
+                                 DECODE_NVFP4, PREFILL_EIGHTH_BF16, BOUNDARY_BF16,
+                                 DECODE_SLICE_BF16)}
 
 
 def storage_dtype(kind: str) -> torch.dtype:
