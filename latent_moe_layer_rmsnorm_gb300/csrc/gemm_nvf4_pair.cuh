@@ -41,6 +41,12 @@
 //   empty[s]    both CTAs: the leader's commit multicasts when stage s's MMAs are done
 //   tfull       both CTAs: multicast commit after a tile's last MMA
 //   tempty      leader only: the 8 epilogue warps of each CTA arrive (the peer remotely)
+// The follower's arrivals (scales written, accumulator read) publish TMEM that tcgen05
+// operations completed before the arrive (tcgen05.wait::st / wait::ld) and that only the
+// tensor core touches next, so they carry the default CTA scope of release: a release at
+// cluster scope (a cluster-wide fence per stage and warp) measured as the bottleneck of
+// the pipeline (ncu: 4.5 membar stalls per issued instruction, the kernel at half the
+// one-CTA kernel's speed).
 #pragma once
 
 #include "gemm_nvf4.cuh"
@@ -95,16 +101,6 @@ __device__ __forceinline__ void mma_issue_nvf4_pair(uint32_t d_tmem, uint64_t ad
       : "memory");
 }
 
-// Arrive on the leader's barrier from either CTA of the pair with the default (CTA) scope
-// of the release.  What these arrivals publish is TMEM that tcgen05 operations completed
-// before the arrive (tcgen05.wait::st / wait::ld) and that only the tensor core touches
-// next, so no write of generic memory has to become visible to the other CTA: a release
-// at cluster scope (a cluster-wide memory fence per stage and warp) measured as the
-// bottleneck of the pipeline (ncu: 4.5 membar stalls per issued instruction, the kernel
-// at half the one-CTA kernel's speed).
-__device__ __forceinline__ void mbar_arrive_cluster_addr(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
 
 // Pair tile t -> this CTA's rows.  `half`: the tile's second CTA holds no rows of the
 // expert (its valid count is <= 0 then).
@@ -325,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (leader) mbar_arrive(&S->sf_ready[stage]);
-          else mbar_arrive_cluster_addr(ready + stage * 8);
+          else mbar_arrive_cluster(ready + stage * 8);
         }
         if (++stage == NVP_STAGES) { stage = 0; phase ^= 1; }
       }
@@ -356,7 +352,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV_THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (leader) mbar_arrive(&S->tempty);
-          else mbar_arrive_cluster_addr(tempty);
+          else mbar_arrive_cluster(tempty);
         }
       };
       if (tc.valid > 0)

@@ -113,9 +113,9 @@ __device__ __forceinline__ void mma_commit_pair_local(uint64_t* bar) {
       : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+// Arrive on a barrier of the cluster (any CTA's) with the default CTA scope of release.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Pair tile t -> this CTA's rows; `small` marks an M = 128 tile (64 rows per CTA).
@@ -478,7 +478,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       else gemm_epilogue<EPI>(P, tc, taddr, r);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&S->tempty[acc]), 0));
+      if (lane == 0) {
+        // the accumulator's loads have completed (tcgen05.wait::ld): no memory write has
+        // to reach the leader, so the arrive needs no cluster-scope release
+        if (leader) mbar_arrive(&S->tempty[acc]);
+        else mbar_arrive_cluster(mapa_shared(smem_u32(&S->tempty[acc]), 0));
+      }
     }
     if (lane == 0) tma_store_wait_all();   // the box stores have landed
   }
