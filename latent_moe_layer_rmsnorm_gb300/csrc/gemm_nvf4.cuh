@@ -58,7 +58,8 @@ enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_Y = 1 };
 
 struct NvSmem {
   GemmSmem g;                // barriers and schedule (its `full`/`empty` sized for GEMM_STAGES)
-  uint64_t full[NV_MAX_STAGES];
+  uint64_t full[NV_MAX_STAGES];       // the stage's operand tiles landed
+  uint64_t sfull[NV_MAX_STAGES];      // its scale chunks landed (copied first)
   uint64_t empty[NV_MAX_STAGES];
   uint64_t sf_ready[NV_MAX_STAGES];   // the 4 scale warps have written the stage's scales
   float recip[256];
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(&N->full[s], 1);
+      mbar_init(&N->sfull[s], 1);
       mbar_init(&N->empty[s], 1);
       mbar_init(&N->sf_ready[s], 4);
     }
@@ -274,7 +276,9 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer ----------------
-    const uint32_t bytes = NV_A_STAGE + NV_B_STAGE + NV_SFA_STAGE + NV_SFB_STAGE;
+    // the scale chunks go first, on their own barrier, so the scale warps can move them
+    // into TMEM while the operand tiles are still arriving
+    const uint32_t bytes = NV_A_STAGE + NV_B_STAGE;
     int stage = 0;
     uint32_t phase = 0;
     int last_phase[NS];
@@ -289,13 +293,14 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
         if (!mbar_wait_bounded(&N->empty[stage], phase ^ 1, abort_flag, P.status,
                                WAIT_PRODUCER_EMPTY, limit))
           goto producer_done;
+        mbar_arrive_expect_tx(&N->sfull[stage], NV_SFA_STAGE + NV_SFB_STAGE);
+        bulk_load(sSA + stage * NV_SFA_STAGE, sfa + kb * NV_SFA_STAGE, NV_SFA_STAGE,
+                  &N->sfull[stage]);
+        bulk_load(sSB + stage * NV_SFB_STAGE, sfb + kb * 2048, 2048, &N->sfull[stage]);
+        bulk_load(sSB + stage * NV_SFB_STAGE + 2048, sfb1 + kb * 2048, 2048, &N->sfull[stage]);
         mbar_arrive_expect_tx(&N->full[stage], bytes);
         tma_load_2d(sA + stage * NV_A_STAGE, &tmA, &N->full[stage], kb * 128, tc.a_row);
         tma_load_2d(sB + stage * NV_B_STAGE, &tmB, &N->full[stage], kb * 128, tc.b_row);
-        bulk_load(sSA + stage * NV_SFA_STAGE, sfa + kb * NV_SFA_STAGE, NV_SFA_STAGE,
-                  &N->full[stage]);
-        bulk_load(sSB + stage * NV_SFB_STAGE, sfb + kb * 2048, 2048, &N->full[stage]);
-        bulk_load(sSB + stage * NV_SFB_STAGE + 2048, sfb1 + kb * 2048, 2048, &N->full[stage]);
         last_phase[stage] = static_cast<int>(phase);
         if (++stage == NS) { stage = 0; phase ^= 1; }
       }
@@ -304,9 +309,12 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     if (*abort_flag) {
       volatile int never = 0;
       for (int s = 0; s < NS; ++s)
-        if (last_phase[s] >= 0)
+        if (last_phase[s] >= 0) {
           mbar_wait_bounded(&N->full[s], static_cast<uint32_t>(last_phase[s]), &never, nullptr,
                             WAIT_DRAIN, limit);
+          mbar_wait_bounded(&N->sfull[s], static_cast<uint32_t>(last_phase[s]), &never, nullptr,
+                            WAIT_DRAIN, limit);
+        }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer ----------------
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__(NV_THREADS, 1)
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       bool ok = true;
       for (int kb = 0; kb < kblocks; ++kb) {
-        if (!mbar_wait_bounded(&N->full[stage], phase, abort_flag, P.status, WAIT_MMA_FULL,
+        if (!mbar_wait_bounded(&N->sfull[stage], phase, abort_flag, P.status, WAIT_MMA_FULL,
                                limit)) {
           ok = false;
           break;

@@ -213,15 +213,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NV_THREADS, 1)
         const uint32_t bar = mapa_shared(smem_u32(&S->full[stage]), 0);
         if (leader) mbar_arrive_expect_tx(&S->full[stage], op_bytes);
         uint8_t* sf = sSF + stage * NVP_SF_STAGE;
+        // scale chunks first, so the scale warps can start while the operands arrive
         mbar_arrive_expect_tx(&S->sfull[stage], sf_bytes);
-        if (load_a) {
-          tma_load_2d_pair(sA + stage * NVP_A_STAGE, &tmA, bar, kb * 128, tc.a_row);
-          bulk_load(sf, sfa + kb * NV_SFA_STAGE, NV_SFA_STAGE, &S->sfull[stage]);
-        }
-        tma_load_2d_pair(sB + stage * NVP_B_STAGE, &tmB, bar, kb * 128,
-                         tc.b_row + 128 * static_cast<int>(rank));
+        if (load_a) bulk_load(sf, sfa + kb * NV_SFA_STAGE, NV_SFA_STAGE, &S->sfull[stage]);
         bulk_load(sf + NV_SFA_STAGE, sfb + kb * 2048, 2048, &S->sfull[stage]);
         bulk_load(sf + NV_SFA_STAGE + 2048, sfb1 + kb * 2048, 2048, &S->sfull[stage]);
+        if (load_a) tma_load_2d_pair(sA + stage * NVP_A_STAGE, &tmA, bar, kb * 128, tc.a_row);
+        tma_load_2d_pair(sB + stage * NVP_B_STAGE, &tmB, bar, kb * 128,
+                         tc.b_row + 128 * static_cast<int>(rank));
         last_sf_phase[stage] = static_cast<int>(phase);
         issued_any = true;
         if (++stage == NVP_STAGES) { stage = 0; phase ^= 1; }
