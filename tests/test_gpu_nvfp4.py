@@ -93,6 +93,75 @@ def test_weight_quantizer_bit_exact():
         np.testing.assert_array_equal(sf2_rows[e], ref["sf2"])
 
 
+# E2M1 rounding decisions in units of the block scale: the seven midpoints (ties go to
+# the even code) and values 2^-5 (relative) to either side of them, then the block maximum.
+SWEEP_M = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0,
+           0.25 * (1 + 2 ** -5), 0.75 * (1 - 2 ** -5), 1.25 * (1 + 2 ** -5),
+           1.75 * (1 - 2 ** -5), 2.5 * (1 + 2 ** -5), 3.5 * (1 - 2 ** -5), 5.0 * (1 + 2 ** -5)]
+# block scales (UE4M3 values; the powers of two keep every element exact in BF16, so the
+# midpoints are exact ties), including the largest (448) that fixes the tensor's amax
+SWEEP_S = [448.0, 2.0 ** -6, 2.0 ** -3, 0.5, 1.0, 2.0, 8.0, 64.0, 1.5, 3.75, 26.0, 0.0]
+
+
+def sweep_matrix(rows: int, K: int, seed: int) -> torch.Tensor:
+    """A [rows, K] BF16 weight whose 16-element blocks sit on E2M1 rounding boundaries:
+    with beta = 2^-8 (tensor amax 6 * 448 * 2^-8 = 10.5, in the first block), a block
+    of scale S holds 6 * S * beta and then m * S * beta for m in SWEEP_M, signs and
+    order shuffled per block (S = 0: an all-zero block)."""
+    rng = np.random.default_rng(seed)
+    beta = 2.0 ** -8
+    out = np.zeros((rows, K), np.float64)
+    nb = K // 16
+    for r in range(rows):
+        for b in range(nb):
+            S = SWEEP_S[(r * nb + b) % len(SWEEP_S)] if (r, b) != (0, 0) else 448.0
+            vals = np.array([6.0] + SWEEP_M + [6.0 * (1 - 2 ** -6)]) * S * beta
+            vals = vals[rng.permutation(16)] * rng.choice([-1.0, 1.0], 16)
+            out[r, 16 * b:16 * b + 16] = vals
+    return torch.from_numpy(out).to(torch.bfloat16)
+
+
+def test_quantizer_rounding_sweep_bit_exact():
+    """The device encoder (shared by the weight quantiser, the activation quantiser and
+    the SwiGLU requantisation) against the oracle's on exact E2M1 ties, values just past
+    them, block scales across the UE4M3 range and all-zero blocks: codes, block scales
+    and global scales bit for bit."""
+    need_gpu()
+    shape = SMALL
+    E, I, p = shape.E, shape.I, shape.p
+    inp = synth.make_inputs(shape, seed=0, device="cpu")
+    for e in range(E):
+        inp["w_gate"][e] = sweep_matrix(I, p, 100 + e)
+        inp["w_up"][e] = sweep_matrix(I, p, 200 + e)
+        inp["w_down"][e] = sweep_matrix(p, I, 300 + e)
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+    dev = {k: v.cuda() for k, v in inp.items()}
+    layer = LatentMoE(shape, dev, out="f32")
+    torch.cuda.synchronize()
+    codes13 = layer.w13.cpu().numpy().reshape(E, 2 * I, p // 2)
+    sf13 = unchunk_sf(layer.sf13.cpu().numpy(), E * 2 * I, p).reshape(E, 2 * I, p // 16)
+    codes2 = layer.w2.cpu().numpy().reshape(E, p, I // 2)
+    sf2 = unchunk_sf(layer.sf2.cpu().numpy(), E * p, I).reshape(E, p, I // 16)
+    gs13, gs2 = layer.gs13.cpu().numpy(), layer.gs2.cpu().numpy()
+    view = oracle_view(inp)
+    rmap = w13_row_map(I)
+    ties = 0
+    for e in range(E):
+        ref = oracle.nvfp4_expert_weights(view["w_gate"][e], view["w_up"][e], view["w_down"][e])
+        assert gs13[e] == ref["g13"] == np.float32(2.0 ** -8), e
+        assert gs2[e] == ref["g2"] == np.float32(2.0 ** -8), e
+        np.testing.assert_array_equal(unpack_codes(codes13[e]), ref["q13"][rmap])
+        np.testing.assert_array_equal(sf13[e], ref["sf13"][rmap])
+        np.testing.assert_array_equal(unpack_codes(codes2[e]), ref["q2"])
+        np.testing.assert_array_equal(sf2[e], ref["sf2"])
+        # the sweep really lands on ties: codes of exact midpoints are even
+        mags = np.abs(view["w_down"][e]).reshape(p, I // 16, 16)
+        blk = mags.max(axis=2, keepdims=True)
+        rel = np.where(blk > 0, mags / np.where(blk > 0, blk, 1) * 6.0, 0)
+        ties += int(np.isin(rel, [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]).sum())
+    assert ties > 0
+
+
 @pytest.mark.parametrize("shape", [SMALL, MID, DECODE_LIKE], ids=lambda s: s.name)
 def test_nvfp4_stages_and_layer(shape):
     need_gpu()
