@@ -54,7 +54,10 @@ constexpr int NV_THREADS = 512;
 // writes and include/latent_moe.h documents)
 constexpr int NV_W13_GROUP = 64;
 
-enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_Y = 1 };
+// STORE_Y writes y through TMA store boxes (3-stage ring); STORE_Y_ROWS writes each valid
+// row with plain 16-byte stores and keeps a 4-stage ring (no boxes): the down GEMM when
+// tiles hold few rows (decode), where the weight stream is all that matters.
+enum NvEpi : int { NV_EPI_SWIGLU_Q = 0, NV_EPI_STORE_Y = 1, NV_EPI_STORE_Y_ROWS = 2 };
 
 struct NvSmem {
   GemmSmem g;                // barriers and schedule (its `full`/`empty` sized for GEMM_STAGES)
@@ -73,22 +76,23 @@ struct NvSmem {
 constexpr int NV_Y_BOX = 32 * 128;
 
 template <int EPI> __host__ __device__ constexpr int nv_stages() {
-  return EPI == NV_EPI_SWIGLU_Q ? 4 : 3;
+  return EPI == NV_EPI_STORE_Y ? 3 : 4;
 }
 template <int EPI> __host__ __device__ constexpr int nv_boxes() {
-  return EPI == NV_EPI_SWIGLU_Q ? 0 : 8;
+  return EPI == NV_EPI_STORE_Y ? 8 : 0;
 }
 template <int EPI>
 constexpr size_t nvf4_smem_bytes_for() {
   return 1024 + size_t(nv_stages<EPI>()) * (NV_A_STAGE + NV_B_STAGE + NV_SFA_STAGE + NV_SFB_STAGE) +
          size_t(nv_boxes<EPI>()) * NV_Y_BOX + sizeof(NvSmem);
 }
-// one dynamic shared-memory size for both kernels: the larger of the two
+// one dynamic shared-memory size for every variant: the largest
 constexpr size_t nvf4_smem_bytes() {
   return nvf4_smem_bytes_for<NV_EPI_SWIGLU_Q>() > nvf4_smem_bytes_for<NV_EPI_STORE_Y>()
              ? nvf4_smem_bytes_for<NV_EPI_SWIGLU_Q>()
              : nvf4_smem_bytes_for<NV_EPI_STORE_Y>();
 }
+static_assert(nvf4_smem_bytes_for<NV_EPI_STORE_Y_ROWS>() <= nvf4_smem_bytes(), "row-store size");
 static_assert(nvf4_smem_bytes() <= 232448, "more than 227 KB of shared memory per CTA");
 static_assert(NV_SF_COL0 + NV_MAX_STAGES * NV_SF_COLS <= GEMM_TMEM_COLS, "scale ring past TMEM");
 
@@ -174,6 +178,40 @@ __device__ __forceinline__ void nvf4_epilogue(const GemmParams& P, const TileCoo
         P.out_sf[sf_offset(row, col / 16 + 1, I)] = static_cast<uint8_t>(code1);
       }
     }
+  } else if constexpr (EPI == NV_EPI_STORE_Y_ROWS) {
+    const float sc = x0;
+    float ss = 0.f;     // the block is one 128-column block of the row (row_ssq)
+    __half* yrow = static_cast<__half*>(P.out) + row * P.ld_out + col0;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 128; c0 += 64) {
+      uint32_t a0[16], a1[16], a2[16], a3[16];
+      tmem_ld16(taddr + c0, a0);
+      tmem_ld16(taddr + c0 + 16, a1);
+      tmem_ld16(taddr + c0 + 32, a2);
+      tmem_ld16(taddr + c0 + 48, a3);
+      tmem_ld_wait();
+      if (c0 == 64) release();
+      float v[64];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        v[i] = __uint_as_float(a0[i]) * sc;
+        v[16 + i] = __uint_as_float(a1[i]) * sc;
+        v[32 + i] = __uint_as_float(a2[i]) * sc;
+        v[48 + i] = __uint_as_float(a3[i]) * sc;
+      }
+      if (row_ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float* w = v + 8 * j;
+          *reinterpret_cast<uint4*>(yrow + c0 + 8 * j) =
+              make_uint4(pack_f16x2(w[0], w[1]), pack_f16x2(w[2], w[3]),
+                         pack_f16x2(w[4], w[5]), pack_f16x2(w[6], w[7]));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 64; ++i) { const float q = stored_value(v[i], OUT_F16); ss = fmaf(q, q, ss); }
+    }
+    if (P.row_ssq && row_ok) P.row_ssq[row * (P.N >> 7) + (col0 >> 7)] = ss;
   } else {
     const float sc = x0;
     const int lane = r & 31;

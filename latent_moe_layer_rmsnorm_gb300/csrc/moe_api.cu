@@ -122,6 +122,10 @@ moe_status_t device_ready(int* sms) {
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_smem_bytes()));
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_nvf4_kernel<NV_EPI_STORE_Y_ROWS>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(nvf4_smem_bytes()));
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_nvf4_pair_kernel<NV_EPI_SWIGLU_Q>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(nvf4_pair_smem_bytes()));
@@ -624,8 +628,14 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
                        static_cast<int64_t>(c.T) * c.top_k >= int64_t(256) * E_);
     if (!pair) {
       const int grid = std::min(sms, max_mt * (p / NV_BN));
-      MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_STORE_Y>, dim3(grid), dim3(NV_THREADS),
-                          nvf4_smem_bytes(), st, ta, tb, ty, P));
+      // experts averaging under 128 rows: tiles are mostly padding and the weights stream
+      // from HBM; rows stored directly, with a ring a stage deeper than the boxes allow
+      if (static_cast<int64_t>(c.T) * c.top_k < int64_t(128) * E_)
+        MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_STORE_Y_ROWS>, dim3(grid), dim3(NV_THREADS),
+                            nvf4_smem_bytes(), st, ta, tb, ty, P));
+      else
+        MOE_TRY(launch_step(gemm_nvf4_kernel<NV_EPI_STORE_Y>, dim3(grid), dim3(NV_THREADS),
+                            nvf4_smem_bytes(), st, ta, tb, ty, P));
     } else {
       CUtensorMap tb128;      // each CTA of a pair loads 128 of the tile's 256 weight rows
       if (!make_tmap(&tb128, W->w2, OP_NVF4, I / 2, static_cast<uint64_t>(E_) * p, 128))
