@@ -180,7 +180,7 @@ moe_status_t moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 /* Bytes of the packed buffers moe_pack_weights / moe_quantize_nvfp4 write.  which:
  * 0 = w_router (TF32 copy), 1 = w13, 2 = w2, 3 = w_pool, 4 = w_unpool, and for NVFP4
  * configs 5 = sf13, 6 = sf2, 7 = gs13, 8 = gs2.  Returns 0 for a buffer this config does
- * not need packed (a BF16 w2 is used as given). */
+ * not use (the scale buffers of a BF16 or FP32 config). */
 size_t moe_packed_bytes(const moe_config_t* cfg, int which);
 
 /* Prepares weights for moe_forward ("SGLang and Miles Add Day-0 Support for Muse Spark

@@ -377,3 +377,34 @@ def test_weight_tile_variant_matches(name):
     w = to_np(layer.intermediate("w", T))
     check_stagewise(layer, oracle_view(inp), shape, T, ids, w, b)
     assert rel_err(to_np(b), to_np(a)) <= tol_for(shape)
+
+
+def test_forward_captures_into_a_cuda_graph():
+    """moe_forward is asynchronous and reads nothing back on the host, so it captures into
+    a CUDA graph; replays give the eager call's output bit for bit and follow a new input
+    written into the captured buffer."""
+    need_gpu()
+    shape = MID_BF16
+    inp = make_case(shape, seed=17)
+    layer, dev = gpu_layer(shape, inp)
+    x = dev["x"].clone()
+    eager = layer.forward(x).clone()
+    other = layer.forward(x.flip(0).contiguous()).clone()
+    out = torch.empty_like(eager)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # warm the call on the capture stream first
+        layer.forward(x, out=out)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x, out=out)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager)
+    x.copy_(x.flip(0))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, other)
+    assert layer.read_status() == (0, 0)
