@@ -288,3 +288,24 @@ def test_pair_kernel_matches_one_cta_kernel(shape):
     assert same_s and same_sf and same_y
     assert torch.equal(pair, one)
     assert torch.equal(auto, one)
+
+
+def test_nvfp4_rows_do_not_depend_on_the_batch():
+    """NVFP4 experts keep the block's row independence bit for bit: each token's
+    activation scale, codes and expert products are its own, so a single-token call (one
+    row per expert: the one-CTA down GEMM storing rows directly) and a permuted batch
+    (other tile placements) give the batch rows (T x k = 2400 >= 256 x E: the down GEMM
+    on CTA pairs) exactly."""
+    need_gpu()
+    shape = MID
+    inp, dev, layer = build(shape, 5)
+    x = dev["x"]
+    full = layer.forward(x).clone()
+    perm = torch.randperm(shape.T, generator=torch.Generator().manual_seed(3)).cuda()
+    permuted = layer.forward(x[perm].contiguous()).clone()
+    singles = [layer.forward(x[t:t + 1].contiguous()).clone() for t in (0, 77, shape.T - 1)]
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    assert torch.equal(permuted, full[perm])
+    for one, t in zip(singles, (0, 77, shape.T - 1)):
+        assert torch.equal(one[0], full[t]), t
