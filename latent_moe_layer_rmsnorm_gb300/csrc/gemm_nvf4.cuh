@@ -10,23 +10,23 @@
 //            with the static global scale gamma[e] (codes + chunked scales)
 //   down     s [rows, I] x W2_e [p, I]; epilogue y = acc * gamma[e] * beta2[e] (FP16)
 //
-// Same pipeline as gemm_tcgen05.cuh (TMA producer warp, one MMA-issuing thread, four
-// epilogue warps, double-buffered TMEM accumulators, bounded waits), with per-stage
-// scale tiles: the producer bulk-copies the 4 scale chunks (512 B each) of the A and B
-// tiles next to the operand tiles, and four scale warps (one per TMEM lane quadrant)
-// write them into TMEM with tcgen05.st, each quadrant getting the same 32 lanes x 16
-// columns per operand that a tcgen05.cp .32x128b.warpx4 of the chunks would leave.
-// Copying them with tcgen05.cp instead costs about 50 tensor-pipe cycles per chunk,
-// more than the 4 MMAs of the slice take (measured on GB300).  The MMA thread issues
-// 4 block-scaled MMAs (K = 64 each) per 128-byte K slice once its scales are in place.
-// Tiles are 128 rows x 256 columns: per K slice 16 KB of A, 32 KB of B and 6 KB of
-// scales for 128 x 256 x 256 MACs, a quarter fewer bytes per MAC than 128 x 128 tiles
-// (the kernel is bound by the rate TMA fills shared memory, about 52 B/clk per SM
-// measured).  TMEM then holds one 256-column accumulator (columns [0, 256)) and a ring
-// of per-stage scale columns after it, so the epilogue of a tile runs before the next
-// tile's MMAs start; eight epilogue warps (two per lane quadrant, one per 128-column
-// half) keep that gap short, each taking 32 SwiGLU columns or a 64-column y box per
-// TMEM wait.
+// The pipeline of gemm_tcgen05.cuh (TMA producer warp, one MMA-issuing thread, epilogue
+// warps, bounded waits) with per-stage scale tiles: the producer bulk-copies the 4 scale
+// chunks (512 B each) of the A and B tiles first, on a barrier of their own, then the
+// operand tiles, and four scale warps (one per TMEM lane quadrant) write the chunks into
+// TMEM with tcgen05.st while the operands still arrive, each quadrant getting the same
+// 32 lanes x 16 columns per operand that a tcgen05.cp .32x128b.warpx4 of the chunks
+// would leave.  Copying them with tcgen05.cp instead costs about 50 tensor-pipe cycles
+// per chunk, more than the 4 MMAs of the slice take (measured on GB300).  The MMA thread
+// issues 4 block-scaled MMAs (K = 64 each) per 128-byte K slice once its operands and
+// scales are in place.  Tiles are 128 rows x 256 columns: per K slice 16 KB of A, 32 KB
+// of B and 6 KB of scales for 128 x 256 x 256 MACs, a quarter fewer bytes per MAC than
+// 128 x 128 tiles (the kernel is bound by the rate operands reach shared memory, about
+// 52-64 B/clk per SM measured).  TMEM then holds one 256-column accumulator (columns
+// [0, 256)) and a ring of per-stage scale columns after it, so the next tile's MMAs wait
+// until the epilogue has read the accumulator: eight epilogue warps (two per lane
+// quadrant, one per 128-column half) read it first (the gate/up epilogue forms its row's
+// 64 SwiGLU values in registers) and hand it back before requantising and storing.
 // A rows are 128-aligned per expert (padded dispatch), so a tile's scales are whole chunks.
 #pragma once
 
