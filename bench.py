@@ -106,10 +106,10 @@ def projection_bytes(s, T: int) -> dict:
 def expert_gemm_bytes(s, n_experts_touched: int, T: int) -> dict:
     """Compulsory HBM bytes of one launch of each expert GEMM: the weights of the experts
     the batch routes to (read once), the R = T * top_k dispatched rows in and the rows
-    out.  BF16 experts: FP16 W13 and u, BF16 W2 and s; FP32 experts: FP32 throughout.
-    NVFP4 experts: 4-bit codes plus
-    one FP8 scale per 16 elements for the weights, u and s.  The down GEMM writes y (BF16;
-    FP32 for FP32 experts) and one FP32 sum of squares per 128 columns."""
+    out.  BF16 experts: FP16 copies of W13 and W2, FP16 u and s; FP32 experts: FP32
+    throughout.  NVFP4 experts: 4-bit codes plus one FP8 scale per 16 elements for the
+    weights, u and s.  The down GEMM writes y (FP16; FP32 for FP32 experts) and one FP32
+    sum of squares per 128 columns."""
     R = T * s.top_k
     if s.expert == "nvfp4":
         q = 0.5 + 1.0 / 16
