@@ -89,23 +89,31 @@ def unit(v, kind):
 
 
 # Values near zero that come out of a cancellation (silu(a) * b with a ~ 0) carry
-# the FP32 accumulation noise of their GEMM in absolute terms: ~sqrt(K) * 2^-24 of
-# the accumulated magnitudes, below 3e-5 of the stage's rms.
+# the FP32 accumulation noise of their GEMM in absolute terms: below 3e-5 of the
+# stage's rms, and it moves under 1 % of the stored values by one unit, for the
+# reductions of up to 1024 terms of the fixed shapes above.  The tensor cores' FP32
+# accumulator aligns each addend to the larger exponent and drops the low bits (round
+# toward zero, as measured on earlier NVIDIA tensor cores by Fasi, Higham, Mikaitis and
+# Pranesh, "Numerical behavior of NVIDIA tensor cores", 2021), so its error has a bias
+# that grows linearly with the number of k-steps: beyond 1024 terms both the floor and
+# the share of one-unit differences grow as K (measured on s: 0.24 % of the values one
+# unit apart at K = 256, 0.9 % at 1024, 5.5 % at 8192).
 ATOL_NOISE = 3e-5
+NOISE_K = 1024
 
 
-def assert_one_unit(name, gpu, ref, kind):
-    """Equal, or one storage unit apart (plus the accumulation-noise floor), and
-    rarely apart."""
+def assert_one_unit(name, gpu, ref, kind, K=NOISE_K):
+    """Equal, or one storage unit apart (plus the accumulation-noise floor of a K-term
+    FP32 reduction), and rarely apart."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     d = np.abs(gpu - ref)
     u = unit(np.maximum(np.abs(gpu), np.abs(ref)), kind)
-    floor = ATOL_NOISE * float(np.sqrt(np.mean(ref * ref)))
+    floor = ATOL_NOISE * max(1.0, K / NOISE_K) * float(np.sqrt(np.mean(ref * ref)))
     bad = d > u * (1 + 1e-9) + floor
     assert not np.any(bad), (name, int(bad.sum()), float(d[bad].max()))
     frac = float(np.mean(d > 0))
-    assert frac <= MAX_FLIP_FRACTION, (name, frac)
+    assert frac <= MAX_FLIP_FRACTION * max(1.0, K / NOISE_K), (name, frac)
     return frac
 
 
@@ -157,7 +165,7 @@ def check_stagewise(layer, view, shape, T, ids, w, out):
         "pooled", pooled,
         oracle.store(oracle.pool(h_in, wconv(view["w_pool"], st["w_proj"])), "f32"))
     u_ref = oracle.store(oracle.rmsnorm(pooled, view["g_pool"], shape.eps), st["u"])
-    rep["u"] = assert_one_unit("u", u, u_ref[src // k], st["u"])
+    rep["u"] = assert_one_unit("u", u, u_ref[src // k], st["u"], K=shape.p)
     e_of_row = ids.reshape(-1)[src]
     s_ref = np.zeros(s.shape)
     y_ref = np.zeros(y.shape)
@@ -169,15 +177,15 @@ def check_stagewise(layer, view, shape, T, ids, w, out):
         y_ref[rows] = oracle.store(
             oracle.expert_down(s[rows].astype(np.float64), wconv(view["w_down"][e], st["w_down"])),
             st["y"])
-    rep["s"] = assert_one_unit("s", s, s_ref, st["s"])
+    rep["s"] = assert_one_unit("s", s, s_ref, st["s"], K=shape.p)
     if st["y"] == "f32":
         rep["y"] = assert_sum_close("y", y, y_ref)
     else:                                                  # one BF16 rounding of the sum
-        rep["y"] = assert_one_unit("y", y, y_ref, st["y"])
+        rep["y"] = assert_one_unit("y", y, y_ref, st["y"], K=shape.I)
     y_slots = y[inv].astype(np.float64)                    # [T, k, p]
     c_ref = oracle.store(oracle.combine(y_slots, ids, np.asarray(w, np.float64), view["g_exp"],
                                         shape.eps), st["c"])
-    rep["c"] = assert_one_unit("c", c, c_ref, st["c"])
+    rep["c"] = assert_one_unit("c", c, c_ref, st["c"], K=shape.p)
     rep["out"] = assert_sum_close(
         "out", to_np(out), oracle.store(oracle.unpool(c, wconv(view["w_unpool"], st["w_proj"])), "f32"))
     return rep
@@ -408,3 +416,29 @@ def test_forward_captures_into_a_cuda_graph():
     torch.cuda.synchronize()
     assert torch.equal(out, other)
     assert layer.read_status() == (0, 0)
+
+
+def test_maximum_widths():
+    """The largest widths the library accepts (d = 32768, p = 8192, I = 32768) on a few
+    tokens: ids exact, every stage against the oracle from the GPU's own stage inputs, end
+    to end within the BF16 bound.  (Split-K pooler, unsplit unpooler over 128 N tiles,
+    gate/up over 2I = 65536 weight rows.)"""
+    need_gpu()
+    shape = synth.Shape("max_widths", T=8, d=32768, p=8192, E=2, top_k=2, I=32768)
+    inp = make_case(shape, seed=31)
+    view = oracle_view(inp)
+    ref = oracle.moe_forward(view, **oracle_kwargs(shape, "f32"), chain=True, return_parts=True)
+    layer, dev = gpu_layer(shape, inp, out="f32")
+    T = shape.T
+    out = layer.forward(dev["x"])
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    ids = layer.intermediate("ids", T).cpu().numpy()
+    w = to_np(layer.intermediate("w", T))
+    np.testing.assert_array_equal(ids, ref["ids"])
+    np.testing.assert_allclose(w, ref["w"], rtol=0, atol=TOL_W)
+    check_dispatch(layer, T, ids)
+    check_stagewise(layer, view, shape, T, ids, w, out)
+    e2e = rel_err(to_np(out), ref["out"])
+    print("max widths e2e", f"{e2e:.2e}")
+    assert e2e <= tol_for(shape), e2e
