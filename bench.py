@@ -595,7 +595,29 @@ def run_ours(args):
         b_bytes = 3 * x.numel() * x.element_size() + out.numel() * out.element_size()
         boundary = {"ms": round(b_ms, 4), "gbs": round(b_bytes / (b_ms / 1e3) / 1e9, 1),
                     "bytes": b_bytes}
-        del xo, hn
+        # the block followed by that pass, against the block with the row pass inside its
+        # unpooler (moe_forward_boundary): same results, one pass over [T, d] fewer
+        yb = torch.empty_like(out)
+
+        def block_then_pass():
+            layer.forward(x, out=yb)
+            layer.boundary(x, yb, g_post, g_next, x_out=xo, h_next=hn)
+
+        def block_fused():
+            layer.forward_boundary(x, g_post, g_next, y=yb, x_out=xo, h_next=hn)
+
+        for name, fn in (("block_then_pass_ms", block_then_pass), ("fused_ms", block_fused)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            b0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b1.record(stream)
+            torch.cuda.synchronize()
+            boundary[name] = round(max_over_ranks(b0.elapsed_time(b1), "cuda") / args.steps, 4)
+        boundary["fused_saves_ms"] = round(boundary["block_then_pass_ms"] - boundary["fused_ms"], 4)
+        del xo, hn, yb
 
     # ---- roofline of the dominant kernel -------------------------------------------------
     peaks, peak_src = load_peaks()

@@ -284,6 +284,30 @@ moe_status_t moe_boundary(const moe_config_t* cfg, const void* x, const void* y,
                           const float* g_post, const float* gate, const float* g_next,
                           void* x_out, void* h_next, moe_stream_t stream);
 
+/* The block followed by its boundary, with the boundary's row pass inside the unpooler
+ * GEMM's kernel ("SGLang and Miles Add Day-0 Support for Muse Spark Open", section "Kernel
+ * Optimizations": the post-FFN norm, the gated residual add and the next block's pre-norm
+ * fused into one kernel).  Same results as moe_forward(x, ids, w -> y) followed by
+ * moe_boundary(x, y -> x_out, h_next) up to the order of FP32 additions in the two sums
+ * of squares:
+ *   y      [T,d] out dtype (device, written): the block output, as moe_forward's `out`;
+ *          its rows are reread from L2 by the row pass, not from HBM
+ *   x_out, h_next, g_post, gate, g_next: as for moe_boundary (x_out may be x)
+ *   x, ids, w, ws, ws_bytes: as for moe_forward
+ * The unpooler's epilogue stores the output tiles and their per-128-column sums of
+ * squares and counts, per 32-row block, the column tiles stored; warps that are idle
+ * during the GEMM's main loop run the row pass on each 2-row item once its block is
+ * complete (a bounded wait: code 7 of moe_read_status if a block never completes).  The
+ * kernel is launched with no more CTA pairs than the device can hold at once.  Shapes
+ * whose unpooler runs split-K or on 128-column tiles (small T, d not a multiple of 256)
+ * run moe_boundary's pass after the block instead.  Returns MOE_ERR_INVALID_ARG for null,
+ * misaligned or overlapping buffers (y may overlap none of x, x_out, h_next). */
+moe_status_t moe_forward_boundary(const moe_config_t* cfg, const moe_weights_t* W,
+                                  const void* x, const int32_t* ids, const float* w,
+                                  const float* g_post, const float* gate, const float* g_next,
+                                  void* y, void* x_out, void* h_next, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
 /* moe_forward with CUDA events recorded on `stream` at each stage boundary:
  * events[0] before the first kernel and events[i] after stage i-1 (i = 1..n_events-1,
  * at most moe_num_stages()+1 events).  For measurement only; same results. */
@@ -310,15 +334,19 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally);
  * NVFP4 configs: dispatched rows start at a 128-row boundary per expert (R rows in all,
  * R = 128 * (ceil(T*k/128) + E)); 8 A_perm [R, p/2] E2M1 codes, 9 s [R, I/2] codes,
  * 10 y [R, p] FP16, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
- * FP32 per-row scales.  All configs: 15 row_cnt [E+1] int32 rows per expert.
- * Writes min(n, 16) offsets and returns how many it wrote (0 for an invalid config). */
+ * FP32 per-row scales.  All configs: 15 row_cnt [E+1] int32 rows per expert;
+ * moe_forward_boundary: 16 [T, d/128] FP32 sums of squares of the block output per 128
+ * columns, 17 [8 * ceil(T/256) + 1] int32 column tiles stored per 32-row block, then the
+ * row workers' item counter (all zero when the boundary ran as a separate pass).
+ * Writes min(n, 18) offsets and returns how many it wrote (0 for an invalid config). */
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n);
 
 /* Synchronises `stream`, returns the device-side status of every call since the last
  * read (MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE_CHECK) and clears it.  detail (may
  * be NULL) receives a code naming the wait or check that failed first:
- *   1-6   a pipeline wait ran out (MOE_ERR_TIMEOUT): 1 producer slot, 2 MMA operands,
- *         3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain, 6 combine rows;
+ *   1-7   a pipeline wait ran out (MOE_ERR_TIMEOUT): 1 producer slot, 2 MMA operands,
+ *         3 MMA accumulator, 4 epilogue accumulator, 5 teardown drain, 6 combine rows,
+ *         7 the fused boundary's row workers (moe_forward_boundary);
  *   16    a replayed expert id outside [0, E) (its slot is skipped);
  *   17    a row index check;
  *   18    the full-width norm: a non-finite input row, or an h value beyond the FP16

@@ -36,13 +36,13 @@ PACK_ROUTER, PACK_W13, PACK_W2, PACK_POOL, PACK_UNPOOL, PACK_SF13, PACK_SF2, PAC
 EXPORTS = ("moe_workspace_size", "moe_workspace_init", "moe_packed_bytes", "moe_pack_weights",
            "moe_quantize_nvfp4", "moe_route", "moe_route_noalloc",
            "moe_read_noalloc_status", "moe_forward",
-           "moe_boundary", "moe_forward_profiled",
+           "moe_boundary", "moe_forward_boundary", "moe_forward_profiled",
            "moe_num_stages",
            "moe_stage_name", "moe_forward_launches", "moe_workspace_offsets",
            "moe_read_status", "moe_status_string")
 
 OFFSET_NAMES = ("h32", "h16", "ids", "w", "pooled", "row_off", "src", "inv", "a_perm", "s",
-                "y", "c", "sf_u", "sf_s", "alpha", "row_cnt")
+                "y", "c", "sf_u", "sf_s", "alpha", "row_cnt", "bnd_ssq", "bnd_cnt")
 
 
 class MoeError(RuntimeError):
@@ -108,6 +108,8 @@ def lib() -> ctypes.CDLL:
     L.moe_forward.argtypes = [cfgp, wp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_boundary.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_boundary.restype = i32
+    L.moe_forward_boundary.argtypes = [cfgp, wp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_forward_boundary.restype = i32
     L.moe_forward.restype = i32
     L.moe_forward_profiled.argtypes = [cfgp, wp, vp, vp, vp, vp, vp, sz, vp,
                                        ctypes.POINTER(vp), i32]
@@ -174,6 +176,12 @@ def moe_forward(cfg, W: moe_weights_t, x, ids, w, out, ws, ws_bytes, stream) -> 
 def moe_boundary(cfg, x, y, g_post, gate, g_next, x_out, h_next, stream) -> int:
     return int(lib().moe_boundary(ctypes.byref(cfg), x, y, g_post, gate, g_next, x_out,
                                   h_next, stream))
+
+
+def moe_forward_boundary(cfg, W: moe_weights_t, x, ids, w, g_post, gate, g_next, y, x_out,
+                         h_next, ws, ws_bytes, stream) -> int:
+    return int(lib().moe_forward_boundary(ctypes.byref(cfg), _ref(W), x, ids, w, g_post, gate,
+                                          g_next, y, x_out, h_next, ws, ws_bytes, stream))
 
 
 def moe_forward_profiled(cfg, W, x, ids, w, out, ws, ws_bytes, stream, events) -> int:

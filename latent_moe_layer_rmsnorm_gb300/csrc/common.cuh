@@ -22,6 +22,7 @@ enum : int {
   WAIT_EPI_TMEM_FULL = 4,
   WAIT_DRAIN = 5,
   WAIT_COMBINE = 6,
+  WAIT_BOUNDARY_ROWS = 7,   // the unpooler's row workers: a 32-row block never completed
   CHECK_EXPERT_ID = 16,
   CHECK_ROW = 17,
   // a stored intermediate left its format's range: a non-finite row, a value above the

@@ -308,8 +308,245 @@ __device__ __forceinline__ void pair_epilogue_boxes(const GemmParams& P, const T
   }
 }
 
+// ---- the block boundary in the unpooler's kernel (EPI_BOUNDARY) --------------------------
+// "SGLang and Miles Add Day-0 Support for Muse Spark Open", section "Kernel Optimizations":
+// the post-FFN norm, the gated residual add and the next block's pre-attention norm are
+// fused.  Here they run inside the unpooler GEMM that produces the block's output.  A
+// row's RMS needs all d / 256 column tiles of the row, which different CTA pairs compute,
+// so the tile epilogues (warps 4-7) store the output and its per-128-column sums of
+// squares as for the plain unpooler and then count, per 32-row block, the tiles stored;
+// six more warps of every CTA, idle during the main loop, take 2-row items in order and
+// run the row pass on each once its block is complete:
+//   a = RMSNorm_{g_post}(out) (sum of squares from the stored partials);
+//   x' = x + gate * a, rounded to the residual stream's type and stored;
+//   h' = RMSNorm_{g_next}(x' as stored)
+// The output rows are reread from L2 within microseconds of their store, and the separate
+// pass over [T, d] (its launch and its reread of the output from HBM) is gone.  A worker
+// waits only for tiles of the same launch, whose CTAs never wait for a worker; the launch
+// is sized so that all its clusters are resident together, and every wait is bounded.
+// Measured at the prefill chunk (T = 16384, d = 8192): the row pass's reads (output rows,
+// residual rows, gains, x' again) share the path from L2 into the SMs with the GEMM's
+// operand copies, which bound the unpooler, and stretch its tiles from 0.59 to 0.71 ms;
+// with the tail of the last rows the call takes what moe_forward + moe_boundary take.
+constexpr int BND_ITEM_ROWS = 2;
+// The fused kernel runs 12 warps: 0 TMA, 1 MMA, 4-7 epilogue as in the plain kernel, and
+// the row workers 2, 3 and 8-11 (the epilogue warps join them after their last tile).
+constexpr int BND_THREADS = 384;
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 8 consecutive values of a row chunk held as 1 (BF16) or 2 (FP32) 16-byte words
+template <bool F32>
+struct Chunk8 {
+  uint4 w[F32 ? 2 : 1];
+};
+
+// Read at L2 (other SMs wrote these values during this launch; L1 may hold none of them)
+template <bool F32>
+__device__ __forceinline__ void chunk_ldcg(const void* base, size_t i, Chunk8<F32>& c) {
+  const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(base) + i * (F32 ? 4 : 2));
+  c.w[0] = __ldcg(p);
+  if constexpr (F32) c.w[1] = __ldcg(p + 1);
+}
+
+template <bool F32>
+__device__ __forceinline__ void chunk_unpack(const Chunk8<F32>& c, float (&v)[8]) {
+  if constexpr (F32) {
+    v[0] = __uint_as_float(c.w[0].x); v[1] = __uint_as_float(c.w[0].y);
+    v[2] = __uint_as_float(c.w[0].z); v[3] = __uint_as_float(c.w[0].w);
+    v[4] = __uint_as_float(c.w[1].x); v[5] = __uint_as_float(c.w[1].y);
+    v[6] = __uint_as_float(c.w[1].z); v[7] = __uint_as_float(c.w[1].w);
+  } else {
+    float2 f;
+    f = unpack_bf16x2(c.w[0].x); v[0] = f.x; v[1] = f.y;
+    f = unpack_bf16x2(c.w[0].y); v[2] = f.x; v[3] = f.y;
+    f = unpack_bf16x2(c.w[0].z); v[4] = f.x; v[5] = f.y;
+    f = unpack_bf16x2(c.w[0].w); v[6] = f.x; v[7] = f.y;
+  }
+}
+
+// Store 8 values (BF16: rounded to nearest even), streaming or plain
+template <bool F32, bool STREAM>
+__device__ __forceinline__ void chunk_store(void* base, size_t i, const float (&o)[8]) {
+  uint4* p = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + i * (F32 ? 4 : 2));
+  if constexpr (F32) {
+    const uint4 a = make_uint4(__float_as_uint(o[0]), __float_as_uint(o[1]), __float_as_uint(o[2]),
+                               __float_as_uint(o[3]));
+    const uint4 b = make_uint4(__float_as_uint(o[4]), __float_as_uint(o[5]), __float_as_uint(o[6]),
+                               __float_as_uint(o[7]));
+    if constexpr (STREAM) { __stcs(p, a); __stcs(p + 1, b); } else { p[0] = a; p[1] = b; }
+  } else {
+    const uint4 q = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]),
+                               pack_bf16x2(o[4], o[5]), pack_bf16x2(o[6], o[7]));
+    if constexpr (STREAM) __stcs(p, q); else *p = q;
+  }
+}
+
+__device__ __forceinline__ void load_vec8(const float* g, int col, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(g + col));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(g + col) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// The row pass on rows row0 and row1 (row1 == row0 for a lone last row) by one warp, in
+// lockstep so that each gain vector is read once for both: lane l takes the 8-value
+// chunks l, l + 32, ..., and every load of an iteration (U chunks of the gains and of
+// both rows' output and x) is issued before the first is used.  The gains do not fit
+// beside the GEMM's shared memory in L1, so they come from L2.
+template <bool XF, bool YF>
+__device__ __forceinline__ void boundary_rows(const GemmParams& P, int row0, int row1, int lane) {
+  constexpr int U = 2;
+  const BoundaryArgs& B = P.bnd;
+  const int d = P.N;
+  const int nch = d >> 3;
+  const size_t base[2] = {static_cast<size_t>(row0) * d, static_cast<size_t>(row1) * d};
+  const bool gated = B.gate != nullptr;
+  // 1. sums of squares of the stored output rows, from their 128-column partials
+  float rs_y[2], ss2[2] = {0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float* part = P.row_ssq + static_cast<size_t>(r ? row1 : row0) * (d >> 7);
+    float ss = 0.f;
+    for (int j = lane; j < (d >> 7); j += 32) ss += __ldcg(part + j);
+    rs_y[r] = rsqrtf(warp_sum(ss) / static_cast<float>(d) + B.eps);
+  }
+  // 2. residual add, rounded to the stream's type
+  for (int c0 = lane; c0 < nch; c0 += 32 * U) {
+    Chunk8<YF> yc[U][2];
+    Chunk8<XF> xc[U][2];
+    float gp[U][8], gt[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nch) {
+        load_vec8(B.g_post, 8 * c, gp[u]);
+        if (gated) load_vec8(B.gate, 8 * c, gt[u]);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          chunk_ldcg<YF>(P.out, base[r] + 8 * c, yc[u][r]);
+          chunk_ldcg<XF>(B.x, base[r] + 8 * c, xc[u][r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nch) continue;
+      if (!gated) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) gt[u][j] = 1.f;
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float yv[8], xv[8], o[8];
+        chunk_unpack<YF>(yc[u][r], yv);
+        chunk_unpack<XF>(xc[u][r], xv);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o[j] = xv[j] + gt[u][j] * (yv[j] * rs_y[r] * gp[u][j]);
+          if (!XF) o[j] = __bfloat162float(__float2bfloat16_rn(o[j]));
+          ss2[r] = fmaf(o[j], o[j], ss2[r]);
+        }
+        chunk_store<XF, false>(B.x_out, base[r] + 8 * c, o);
+      }
+    }
+  }
+  float rs_x[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) rs_x[r] = rsqrtf(warp_sum(ss2[r]) / static_cast<float>(d) + B.eps);
+  // 3. the next block's pre-norm on x' as stored (each lane rereads its own chunks)
+  for (int c0 = lane; c0 < nch; c0 += 32 * U) {
+    Chunk8<XF> xc[U][2];
+    float gn[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      if (c < nch) {
+        load_vec8(B.g_next, 8 * c, gn[u]);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) chunk_ldcg<XF>(B.x_out, base[r] + 8 * c, xc[u][r]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + 32 * u;
+      if (c >= nch) continue;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float v[8], o[8];
+        chunk_unpack<XF>(xc[u][r], v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = v[j] * rs_x[r] * gn[u][j];
+        chunk_store<XF, true>(B.h_next, base[r] + 8 * c, o);
+      }
+    }
+  }
+}
+
+// Row worker (one warp): claim items in order, wait (bounded) until the item's 32-row
+// block has all its column tiles stored, run the row pass.  Returns when every item is
+// claimed, or on a timeout / abort.
+template <bool XF, bool YF>
+__device__ void boundary_worker(const GemmParams& P, int lane, volatile int* abort_flag) {
+  const BoundaryArgs& B = P.bnd;
+  const int M = P.M;
+  const int tiles_n = P.N / P.bn;
+  int* claim = B.count + ((M + 255) / 256) * 8;
+  const int n_items = (M + BND_ITEM_ROWS - 1) / BND_ITEM_ROWS;
+  for (;;) {
+    int item = 0;
+    if (lane == 0) item = atomicAdd(claim, 1);
+    item = __shfl_sync(0xFFFFFFFFu, item, 0);
+    if (item >= n_items) return;
+    const int row0 = item * BND_ITEM_ROWS;
+    const int row1 = min(row0 + 1, M - 1);
+    const int* cnt = B.count + (row0 >> 5);
+    int ok = 1;
+    if (lane == 0 && ld_acquire_gpu(cnt) < tiles_n) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(cnt) < tiles_n) {
+        __nanosleep(256);
+        if (*abort_flag) { ok = 0; break; }
+        if (globaltimer_ns() - t0 > P.timeout_ns) {
+          report_error(P.status, ST_TIMEOUT, WAIT_BOUNDARY_ROWS);
+          *abort_flag = 1;
+          ok = 0;
+          break;
+        }
+      }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) return;
+    (void)ld_acquire_gpu(cnt);     // each lane acquires the block's stores
+    boundary_rows<XF, YF>(P, row0, row1, lane);
+  }
+}
+
+__device__ __forceinline__ void boundary_worker_any(const GemmParams& P, int lane,
+                                                    volatile int* abort_flag) {
+  const bool yf = P.out_fmt == OUT_F32;
+  if (P.bnd.x_f32) {
+    if (yf) boundary_worker<true, true>(P, lane, abort_flag);
+    else boundary_worker<true, false>(P, lane, abort_flag);
+  } else {
+    if (yf) boundary_worker<false, true>(P, lane, abort_flag);
+    else boundary_worker<false, false>(P, lane, abort_flag);
+  }
+}
+
+template <int EPI>
+constexpr int pair_threads() { return EPI == EPI_BOUNDARY ? BND_THREADS : GEMM_THREADS; }
+
 template <int KIND, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmA64,
                      const __grid_constant__ CUtensorMap tmB,
@@ -456,6 +693,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       volatile int never = 0;
       mbar_wait_bounded(&S->drain, 0, &never, P.status, WAIT_DRAIN, limit);
     }
+  } else if (EPI == EPI_BOUNDARY && (warp == 2 || warp == 3 || warp >= 8)) {
+    // ---------------- boundary row workers (both CTAs) ----------------
+    boundary_worker_any(P, lane, abort_flag);
   } else if (warp >= 4) {
     // ---------------- epilogue (both CTAs: own rows) ----------------
     const int q = warp & 3;
@@ -472,10 +712,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       const TileCoord tc = pair_tile(P, S, t, rank, small);
       const uint32_t taddr =
           tmem_base + acc * GEMM_BN_MAX + (static_cast<uint32_t>(q * 32) << 16);
-      if (small) pair_small_epilogue<EPI>(P, tc, taddr, (q & 1) * 32 + lane, q >> 1);
+      constexpr int EPI_T = EPI == EPI_BOUNDARY ? EPI_STORE : EPI;
+      if (small) pair_small_epilogue<EPI_T>(P, tc, taddr, (q & 1) * 32 + lane, q >> 1);
       else if (P.out_box && tc.valid >= 32 * (q + 1))
-        pair_epilogue_boxes<EPI>(P, tc, taddr, q, lane, &tmOut, boxes + q * PAIR_BOX);
-      else gemm_epilogue<EPI>(P, tc, taddr, r);
+        pair_epilogue_boxes<EPI_T>(P, tc, taddr, q, lane, &tmOut, boxes + q * PAIR_BOX);
+      else gemm_epilogue<EPI_T>(P, tc, taddr, r);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -484,8 +725,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
         if (leader) mbar_arrive(&S->tempty[acc]);
         else mbar_arrive_cluster(mapa_shared(smem_u32(&S->tempty[acc]), 0));
       }
+      if constexpr (EPI == EPI_BOUNDARY) {
+        // this warp's 32 rows of the tile (values and sums of squares) are stored: make
+        // the stores visible GPU-wide, then count the tile for the row workers
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_wait_all();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          red_release_gpu_add(P.bnd.count + (tc.a_row >> 5) + q, 1);
+        }
+        __syncwarp();
+      }
     }
     if (lane == 0) tma_store_wait_all();   // the box stores have landed
+    if constexpr (EPI == EPI_BOUNDARY) boundary_worker_any(P, lane, abort_flag);
   }
 
   tc_fence_before();

@@ -37,10 +37,28 @@ constexpr int GEMM_MAX_GROUPS = 256;
 constexpr int GEMM_TMEM_COLS = 512;
 constexpr int ROUTER_MAX_K = 8;
 
-enum EpiKind : int { EPI_ROUTER = 0, EPI_STORE = 1, EPI_SWIGLU = 2 };
+// EPI_BOUNDARY: EPI_STORE plus the block boundary's row pass (CTA-pair kernel only)
+enum EpiKind : int { EPI_ROUTER = 0, EPI_STORE = 1, EPI_SWIGLU = 2, EPI_BOUNDARY = 3 };
 // Operand kinds; the values of the first three are the instruction-descriptor format
 // codes of kind::f16 / kind::tf32.  OP_NVF4: packed E2M1 operands (gemm_nvf4.cuh).
 enum OpKind : int { OP_F16 = 0, OP_BF16 = 1, OP_TF32 = 2, OP_NVF4 = 3 };
+
+// The block boundary fused into the unpooler (gemm_pair_kernel<KIND, EPI_BOUNDARY>):
+// the residual stream, the gains and gate of the two norms, the row pass's outputs, and
+// the counters through which the tile epilogues tell the row workers that a 32-row block
+// of the output is stored in full.
+struct BoundaryArgs {
+  const void* x;         // [M, N] residual stream entering the block (act type)
+  void* x_out;           // [M, N] x + gate * RMSNorm_{g_post}(out); may be x
+  void* h_next;          // [M, N] RMSNorm_{g_next}(x_out)
+  const float* g_post;
+  const float* gate;     // NULL: plain residual
+  const float* g_next;
+  int* count;            // [8 * ceil(M / 256)] tiles stored per 32-row block, then one
+                         // item counter; zero before the launch
+  float eps;
+  int x_f32;             // residual stream in FP32 (else BF16)
+};
 
 struct GemmParams {
   int M;        // dense: rows of A and of the output
@@ -78,6 +96,7 @@ struct GemmParams {
   float* row_ssq;
   int out_box;   // CTA-pair kernels: 1 = write full 32-row blocks through the output's
                  // tensor map (the kernel's tmOut) instead of per-thread stores
+  BoundaryArgs bnd;   // EPI_BOUNDARY only (its row_ssq: [M, N / 128] of the output)
 };
 
 struct GemmSmem {

@@ -74,6 +74,7 @@ bool make_tmap(CUtensorMap* m, const void* base, int kind, uint64_t inner, uint6
 // ---- per-device cache -------------------------------------------------------------------
 struct DevInfo {
   int sms = 0;
+  int bnd_clusters = 0;   // CTA pairs of the fused unpooler + boundary kernel that fit at once
   bool ready = false;
 };
 DevInfo g_dev[64];
@@ -149,6 +150,29 @@ moe_status_t device_ready(int* sms) {
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_ROUTER>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_F16, EPI_BOUNDARY>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_pair_kernel<OP_TF32, EPI_BOUNDARY>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, pair_smem);
+    if (e == cudaSuccess) {
+      // the fused unpooler's row workers wait for tiles of other clusters of the same
+      // launch, so that launch never holds more clusters than can run at once
+      cudaLaunchConfig_t oc{};
+      oc.gridDim = dim3(D.sms);
+      oc.blockDim = dim3(BND_THREADS);
+      oc.dynamicSmemBytes = pair_smem;
+      int n16 = 0, n32 = 0;
+      if (cudaOccupancyMaxActiveClusters(&n16, gemm_pair_kernel<OP_F16, EPI_BOUNDARY>, &oc) !=
+              cudaSuccess ||
+          cudaOccupancyMaxActiveClusters(&n32, gemm_pair_kernel<OP_TF32, EPI_BOUNDARY>, &oc) !=
+              cudaSuccess) {
+        (void)cudaGetLastError();   // no figure: the fused path stays off on this device
+        n16 = n32 = 0;
+      }
+      D.bnd_clusters = std::min(std::min(n16, n32), D.sms / 2);
+    }
     // boundary kernel: x and y slices of up to BND_MAXV * MEM_THREADS FP32 columns each
     const int bnd_smem = static_cast<int>(boundary_smem_bytes(BND_MAXV * MEM_THREADS, 1, 1));
     if (e == cudaSuccess)
@@ -229,9 +253,12 @@ SplitPlan split_plan(const moe_config_t& c) {
   return sp;
 }
 
+// 32-row blocks whose column tiles the fused unpooler counts (whole 256-row pair tiles)
+inline size_t bnd_blocks(int T) { return size_t(8) * ((T + 255) / 256); }
+
 struct WsLayout {
   size_t status, h32, h16, ids, wts, pooled, chunk, row_off, mt_off, mt2_off, row_cnt, src, inv,
-      a_perm, s, y, ssq, c, sf_u, sf_s, alpha, part, total;
+      a_perm, s, y, ssq, c, sf_u, sf_s, alpha, part, bnd_ssq, bnd_cnt, total;
   int nchunks;
   size_t rows;    // dispatched rows (NVFP4: 128-aligned per expert)
 };
@@ -273,6 +300,10 @@ WsLayout ws_layout(const moe_config_t& c) {
   L.sf_s = take(q ? R * I / 16 : 0);
   L.alpha = take(q ? R * 4 : 0);
   L.part = take(split_plan(c).part_floats * 4);   // split-K partial sums (small T only)
+  // moe_forward_boundary with the boundary in the unpooler: the block output's sums of
+  // squares per 128 columns, and the per-32-row-block tile counters + the item counter
+  L.bnd_ssq = take(T * (d / 128) * 4);
+  L.bnd_cnt = take((bnd_blocks(c.T) + 1) * 4);
   L.total = off;
   return L;
 }
@@ -342,11 +373,12 @@ template <int KIND, int EPI>
 // all valid write through it (P.out_box is set here).
 moe_status_t launch_pair(const CUtensorMap& ta, const CUtensorMap& ta64, const CUtensorMap& tb,
                          const CUtensorMap& tb64, const CUtensorMap& tout, GemmParams P,
-                         int max_tiles, int sms, cudaStream_t st, bool boxes = true) {
-  const int clusters = std::min(sms / 2, max_tiles);
+                         int max_tiles, int sms, cudaStream_t st, bool boxes = true,
+                         int max_clusters = 0) {
+  const int clusters = std::min(max_clusters > 0 ? max_clusters : sms / 2, max_tiles);
   if (clusters <= 0) return MOE_OK;
   P.out_box = boxes ? 1 : 0;
-  return launch_step(gemm_pair_kernel<KIND, EPI>, dim3(2 * clusters), dim3(GEMM_THREADS),
+  return launch_step(gemm_pair_kernel<KIND, EPI>, dim3(2 * clusters), dim3(pair_threads<EPI>()),
                      pair_smem_bytes(), st, ta, ta64, tb, tb64, tout, P);
 }
 
@@ -373,11 +405,58 @@ struct Events {
     if (_s != MOE_OK) return _s;     \
   } while (0)
 
+// Arguments of the block boundary (moe_boundary, moe_forward_boundary): present, 16-byte
+// aligned, and no output overlapping an input other than x_out == x (in place); y_written:
+// y is an output too (moe_forward_boundary), so it may not overlap x either.
+moe_status_t check_boundary_buffers(const moe_config_t& c, const void* x, const void* y,
+                                    const float* g_post, const float* gate, const float* g_next,
+                                    const void* x_out, const void* h_next, bool y_written) {
+  if (!x || !y || !g_post || !g_next || !x_out || !h_next) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(g_post) || !aligned16(g_next) ||
+      !aligned16(x_out) || !aligned16(h_next) || (gate && !aligned16(gate)))
+    return MOE_ERR_INVALID_ARG;
+  const size_t ex = c.act == MOE_F32 ? 4 : 2, ey = c.out == MOE_F32 ? 4 : 2;
+  const size_t bx = size_t(c.T) * c.d * ex, by = size_t(c.T) * c.d * ey;
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+  };
+  // x_out may be x itself (in-place residual update); nothing else may overlap
+  if ((x_out != x && overlap(x_out, bx, x, bx)) || overlap(x_out, bx, y, by) ||
+      (y_written && overlap(x, bx, y, by)) || overlap(h_next, bx, x, bx) ||
+      overlap(h_next, bx, y, by) ||
+      overlap(h_next, bx, x_out, bx))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+// The boundary as its own pass over [T, d] (boundary_kernel<C>).
+moe_status_t launch_boundary_pass(const moe_config_t& c, const void* x, const void* y,
+                                  const float* g_post, const float* gate, const float* g_next,
+                                  void* x_out, void* h_next, cudaStream_t st, int sms) {
+  // CTAs per row: enough that a CTA holds at most BND_MAXV * MEM_THREADS columns, and
+  // more (up to a cluster of 8) while the rows alone would leave SMs idle
+  int C = 1;
+  while (C < 8 && (c.d / C > BND_MAXV * MEM_THREADS || static_cast<long long>(c.T) * C < 2 * sms))
+    C *= 2;
+  const int xf = c.act == MOE_F32, yf = c.out == MOE_F32;
+  const unsigned grid = static_cast<unsigned>(c.T) * C;
+  const size_t smem = boundary_smem_bytes(c.d / C, xf, yf);
+  switch (C) {
+    case 1: boundary_kernel<1><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 2: boundary_kernel<2><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    case 4: boundary_kernel<4><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+    default: boundary_kernel<8><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
+  }
+  return last_launch();
+}
+
 // The block.  route_only: stop after the router, writing ids_out / w_out.
 moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const void* x,
                        const int32_t* ids_in, const float* w_in, void* out, int32_t* ids_out,
                        float* w_out, bool route_only, void* ws, size_t ws_bytes,
-                       cudaStream_t st, cudaEvent_t* ev, int nev) {
+                       cudaStream_t st, cudaEvent_t* ev, int nev,
+                       const BoundaryArgs* bnd = nullptr) {
   MOE_TRY(validate(cfg));
   const moe_config_t& c = *cfg;
   const bool internal_route = route_only || ids_in == nullptr;
@@ -396,6 +475,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   MOE_TRY(device_ready(&sms));
 
   uint8_t* base = static_cast<uint8_t*>(ws);
+  if (bnd && cudaMemsetAsync(base + L.bnd_cnt, 0, (bnd_blocks(c.T) + 1) * 4, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   int* status = reinterpret_cast<int*>(base + L.status);
   float* h32 = reinterpret_cast<float*>(base + L.h32);
   __half* h16 = reinterpret_cast<__half*>(base + L.h16);
@@ -740,7 +821,27 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
           !make_tmap(&to, out, P.out_fmt == OUT_BF16 ? OP_BF16 : OP_TF32, d, T, 32))
         return MOE_ERR_CUDA;
       const int tiles = ((T + 255) / 256) * (d / 256);
-      if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
+      int bnd_clusters = 0;
+      if (bnd) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) bnd_clusters = g_dev[dev].bnd_clusters;
+      }
+      if (bnd && bnd_clusters > 0) {          // the boundary's row pass in this kernel
+        P.row_ssq = reinterpret_cast<float*>(base + L.bnd_ssq);
+        // test hook: this GEMM's tiles then never complete, so the row workers' bounded
+        // waits run out as well
+        P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
+        P.bnd = *bnd;
+        P.bnd.count = reinterpret_cast<int*>(base + L.bnd_cnt);
+        if (act_f32)
+          MOE_TRY((launch_pair<OP_TF32, EPI_BOUNDARY>(ta, ta, tb2, tb2, to, P, tiles, sms, st, true,
+                                                      bnd_clusters)));
+        else
+          MOE_TRY((launch_pair<OP_F16, EPI_BOUNDARY>(ta, ta, tb2, tb2, to, P, tiles, sms, st, true,
+                                                     bnd_clusters)));
+        bnd = nullptr;                        // done
+      } else if (act_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
       else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta, tb2, tb2, to, P, tiles, sms, st)));
     } else if (act_f32) MOE_TRY((launch_gemm<OP_TF32, EPI_STORE>(ta, tb, P, grid, st)));
     else MOE_TRY((launch_gemm<OP_F16, EPI_STORE>(ta, tb, P, grid, st)));
@@ -753,6 +854,10 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     }
   }
   E.mark(8);
+  // no fused row pass for this shape (split-K or 128-wide unpooler tiles): the pass
+  if (bnd)
+    MOE_TRY(launch_boundary_pass(c, bnd->x, out, bnd->g_post, bnd->gate, bnd->g_next, bnd->x_out,
+                                 bnd->h_next, st, sms));
   return MOE_OK;
 }
 
@@ -1003,39 +1108,29 @@ moe_status_t moe_boundary(const moe_config_t* cfg, const void* x, const void* y,
   if (v != MOE_OK) return v;
   const moe_config_t& c = *cfg;
   if (c.T == 0) return MOE_OK;
-  if (!x || !y || !g_post || !g_next || !x_out || !h_next) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(y) || !aligned16(g_post) || !aligned16(g_next) ||
-      !aligned16(x_out) || !aligned16(h_next) || (gate && !aligned16(gate)))
-    return MOE_ERR_INVALID_ARG;
-  const size_t ex = c.act == MOE_F32 ? 4 : 2, ey = c.out == MOE_F32 ? 4 : 2;
-  const size_t bx = size_t(c.T) * c.d * ex, by = size_t(c.T) * c.d * ey;
-  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
-    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
-    return pa < pb + nb && pb < pa + na;
-  };
-  // x_out may be x itself (in-place residual update); nothing else may overlap
-  if ((x_out != x && overlap(x_out, bx, x, bx)) || overlap(x_out, bx, y, by) ||
-      overlap(h_next, bx, x, bx) || overlap(h_next, bx, y, by) ||
-      overlap(h_next, bx, x_out, bx))
-    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_boundary_buffers(c, x, y, g_post, gate, g_next, x_out, h_next, false));
   int sms = 0;
   MOE_TRY(device_ready(&sms));
-  // CTAs per row: enough that a CTA holds at most BND_MAXV * MEM_THREADS columns, and
-  // more (up to a cluster of 8) while the rows alone would leave SMs idle
-  int C = 1;
-  while (C < 8 && (c.d / C > BND_MAXV * MEM_THREADS || static_cast<long long>(c.T) * C < 2 * sms))
-    C *= 2;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int xf = c.act == MOE_F32, yf = c.out == MOE_F32;
-  const unsigned grid = static_cast<unsigned>(c.T) * C;
-  const size_t smem = boundary_smem_bytes(c.d / C, xf, yf);
-  switch (C) {
-    case 1: boundary_kernel<1><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-    case 2: boundary_kernel<2><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-    case 4: boundary_kernel<4><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-    default: boundary_kernel<8><<<grid, MEM_THREADS, smem, st>>>(x, y, g_post, gate, g_next, x_out, h_next, c.d, c.eps, xf, yf); break;
-  }
-  return last_launch();
+  return launch_boundary_pass(c, x, y, g_post, gate, g_next, x_out, h_next,
+                              reinterpret_cast<cudaStream_t>(stream), sms);
+}
+
+moe_status_t moe_forward_boundary(const moe_config_t* cfg, const moe_weights_t* W,
+                                  const void* x, const int32_t* ids, const float* w,
+                                  const float* g_post, const float* gate, const float* g_next,
+                                  void* y, void* x_out, void* h_next, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
+  const moe_status_t v = validate(cfg);
+  if (v != MOE_OK) return v;
+  const moe_config_t& c = *cfg;
+  if (c.T > 0) MOE_TRY(check_boundary_buffers(c, x, y, g_post, gate, g_next, x_out, h_next, true));
+  BoundaryArgs B{};
+  B.x = x; B.x_out = x_out; B.h_next = h_next;
+  B.g_post = g_post; B.gate = gate; B.g_next = g_next;
+  B.eps = c.eps;
+  B.x_f32 = c.act == MOE_F32 ? 1 : 0;
+  return run_layer(cfg, W, x, ids, w, y, nullptr, nullptr, false, ws, ws_bytes,
+                   reinterpret_cast<cudaStream_t>(stream), nullptr, 0, &B);
 }
 
 moe_status_t moe_forward_profiled(const moe_config_t* cfg, const moe_weights_t* W,
@@ -1069,9 +1164,10 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally) {
 int moe_workspace_offsets(const moe_config_t* cfg, size_t* offsets, int n) {
   if (validate(cfg) != MOE_OK || !offsets || n <= 0) return 0;
   const WsLayout L = ws_layout(*cfg);
-  const size_t all[16] = {L.h32, L.h16, L.ids, L.wts, L.pooled, L.row_off, L.src, L.inv,
-                          L.a_perm, L.s, L.y, L.c, L.sf_u, L.sf_s, L.alpha, L.row_cnt};
-  const int m = n < 16 ? n : 16;
+  const size_t all[18] = {L.h32, L.h16, L.ids, L.wts, L.pooled, L.row_off, L.src, L.inv,
+                          L.a_perm, L.s, L.y, L.c, L.sf_u, L.sf_s, L.alpha, L.row_cnt,
+                          L.bnd_ssq, L.bnd_cnt};
+  const int m = n < 18 ? n : 18;
   for (int i = 0; i < m; ++i) offsets[i] = all[i];
   return m;
 }

@@ -164,6 +164,29 @@ class LatentMoE:
                                x_out.data_ptr(), h_next.data_ptr(), _stream()), "moe_boundary")
         return x_out, h_next
 
+    def forward_boundary(self, x: torch.Tensor, g_post: torch.Tensor, g_next: torch.Tensor,
+                         gate=None, ids=None, w=None, y=None, x_out=None, h_next=None,
+                         flags: int = 0):
+        """The block and its boundary in one call (moe_forward_boundary): the row pass
+        runs inside the unpooler's kernel.  Returns (y, x_out, h_next); x_out may be x."""
+        T = x.shape[0]
+        assert x.is_contiguous() and x.dtype == _TORCH[self.shape.act]
+        if y is None:
+            y = torch.empty((T, self.shape.d), dtype=self.out_dtype(), device=x.device)
+        if x_out is None:
+            x_out = torch.empty_like(x)
+        if h_next is None:
+            h_next = torch.empty_like(x)
+        if ids is not None:
+            ids = ids.to(torch.int32).contiguous()
+            w = w.to(torch.float32).contiguous()
+        ws, nbytes = self.workspace(T)
+        L.check(L.moe_forward_boundary(self.config(T, flags), self.W, x.data_ptr(), _ptr(ids),
+                                       _ptr(w), g_post.data_ptr(), _ptr(gate), g_next.data_ptr(),
+                                       y.data_ptr(), x_out.data_ptr(), h_next.data_ptr(), ws,
+                                       nbytes, _stream()), "moe_forward_boundary")
+        return y, x_out, h_next
+
     def read_status(self):
         ws, nbytes = self.workspace(1) if self.ws is None else (self.ws.data_ptr() + self.ws_off,
                                                                  self.ws_bytes)
@@ -189,7 +212,9 @@ class LatentMoE:
                 "ids": ((T, k), torch.int32), "w": ((T, k), torch.float32),
                 "pooled": ((T, sh.p), torch.float32), "row_off": ((sh.E + 1,), torch.int32),
                 "row_cnt": ((sh.E + 1,), torch.int32), "inv": ((T * k,), torch.int32),
-                "c": ((T, sh.p), op)}
+                "c": ((T, sh.p), op),
+                "bnd_ssq": ((T, sh.d // 128), torch.float32),
+                "bnd_cnt": ((8 * ((T + 255) // 256) + 1,), torch.int32)}
         spec.update(rows)
         shape, dtype = spec[name]
         off = L.moe_workspace_offsets(self.config(T))[name] + self.ws_off

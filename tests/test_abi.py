@@ -140,6 +140,31 @@ def test_boundary_host_side_errors():
     assert L.moe_boundary(cfg(T=0, d=256), X, Y, G, None, G, XO, H, None) == L.MOE_OK
 
 
+def test_fused_boundary_host_side_errors():
+    """moe_forward_boundary checks the boundary's buffers like moe_boundary (y, written by
+    the call, may not overlap x either) and the block's like moe_forward, before any
+    launch; T = 0 is a no-op."""
+    c = cfg(T=4, d=256)
+    ws = L.moe_workspace_size(c)
+    W = weights()
+    n = 4 * 256 * 2
+    X, Y, XO, H, G, WS = FAKE, 2 * FAKE, 3 * FAKE, 4 * FAKE, 5 * FAKE, 6 * FAKE
+    fb = L.moe_forward_boundary
+    assert fb(c, W, X, None, None, None, None, G, Y, XO, H, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert fb(c, W, X, None, None, G, None, G, None, XO, H, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert fb(c, W, X, None, None, G, G + 4, G, Y, XO, H, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert fb(c, W, X, None, None, G, None, G, X + n - 16, XO, H, WS, ws, None) \
+        == L.MOE_ERR_INVALID_ARG
+    assert fb(c, W, X, None, None, G, None, G, Y, Y, H, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert fb(c, W, X, None, None, G, None, G, Y, XO, XO, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert fb(c, None, X, None, None, G, None, G, Y, XO, H, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert fb(c, W, X, None, None, G, None, G, Y, XO, H, WS, ws - 1, None) == L.MOE_ERR_WORKSPACE
+    assert fb(c, W, X, FAKE, None, G, None, G, Y, XO, H, WS, ws, None) == L.MOE_ERR_INVALID_ARG
+    c0 = cfg(T=0, d=256)
+    assert fb(c0, W, X, None, None, G, None, G, Y, XO, H, WS, L.moe_workspace_size(c0), None) \
+        == L.MOE_OK
+
+
 def test_stage_names_and_status_strings():
     n = L.moe_num_stages()
     assert n == 8
