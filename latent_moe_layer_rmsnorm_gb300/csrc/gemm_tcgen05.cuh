@@ -97,6 +97,8 @@ struct GemmParams {
   int out_box;   // CTA-pair kernels: 1 = write full 32-row blocks through the output's
                  // tensor map (the kernel's tmOut) instead of per-thread stores
   BoundaryArgs bnd;   // EPI_BOUNDARY only (its row_ssq: [M, N / 128] of the output)
+  int b_const;   // dense: B is a weight, written before the forward began, so the first
+                 // ring stages' B tiles are requested before the wait on the previous kernel
 };
 
 struct GemmSmem {
@@ -335,6 +337,24 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
+  // A weight operand does not depend on the kernels before this one: the producer puts
+  // the B halves of the first ring stages in flight, and asks L2 for the rest of its first
+  // tile's B, while the previous kernel is still running (at decode the projections and
+  // the router stream their weights once, and the wait is most of their time).
+  int preloaded = 0;
+  if (P.b_const && P.groups == 0 && P.debug_skip_first_load == 0 && warp == 0 && lane == 0 &&
+      static_cast<int>(blockIdx.x) < gemm_num_tiles(P, nullptr)) {
+    constexpr int KB = KIND == OP_TF32 ? 32 : 64;
+    const int kb0 = P.K / KB / P.ksplit;
+    const TileCoord tc = gemm_tile(P, nullptr, static_cast<int>(blockIdx.x));
+    preloaded = kb0 < GEMM_STAGES ? kb0 : GEMM_STAGES;
+    for (int s = 0; s < preloaded; ++s) {
+      mbar_arrive_expect_tx(&S->full[s], GEMM_A_STAGE + P.bn * 128);
+      tma_load_2d(sB + s * GEMM_B_STAGE, &tmB, &S->full[s], (tc.split * kb0 + s) * KB, tc.b_row);
+    }
+    for (int kb = preloaded; kb < kb0; ++kb)
+      tma_prefetch_l2_2d(&tmB, (tc.split * kb0 + kb) * KB, tc.b_row);
+  }
   pdl_wait();          // the inputs and tables are the previous kernels' outputs
   pdl_allow_next();
   if (P.groups > 0) {
@@ -363,7 +383,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t phase = 0;
     int last_phase[GEMM_STAGES];   // parity of the last load issued into each stage
 #pragma unroll
-    for (int s = 0; s < GEMM_STAGES; ++s) last_phase[s] = -1;
+    for (int s = 0; s < GEMM_STAGES; ++s) last_phase[s] = s < preloaded ? 0 : -1;
     bool skip = P.debug_skip_first_load != 0;
     for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
       const TileCoord tc = gemm_tile(P, S, t);
@@ -373,6 +393,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           goto producer_done;
         if (skip) {
           skip = false;   // test hook: this stage never fills, so the MMA wait runs out
+        } else if (t == static_cast<int>(blockIdx.x) && kb < preloaded) {
+          // B is in flight since before the wait; the stage's barrier already expects both
+          const int kc = (tc.split * kblocks + kb) * (TF32 ? 32 : 64);
+          tma_load_2d(sA + stage * GEMM_A_STAGE, &tmA, &S->full[stage], kc, tc.a_row);
+          last_phase[stage] = static_cast<int>(phase);
         } else {
           mbar_arrive_expect_tx(&S->full[stage], bytes);
           const int kc = (tc.split * kblocks + kb) * (TF32 ? 32 : 64);

@@ -517,6 +517,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = bn; P.K = d; P.bn = bn; P.groups = 0;
+    P.b_const = 1;           // the router weights: loads may start before the norm ends
     if (sp.router > 1) {     // small T: K slices -> partial logits -> sum + top-k
       P.bn = bn_split;
       P.ksplit = sp.router; P.split_stride = size_t(T) * bn;
@@ -552,6 +553,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = p; P.K = d; P.bn = bn; P.groups = 0;
+    P.b_const = 1;           // W_pool
     P.out = pooled; P.ld_out = p; P.out_fmt = OUT_F32;
     if (sp.pool > 1) { P.ksplit = sp.pool; P.split_stride = size_t(T) * p; P.out = part; }
     const int grid = std::min(sms, mtiles * (p / bn) * sp.pool);
@@ -810,6 +812,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.M = T; P.N = d; P.K = p; P.bn = bn; P.groups = 0;
+    P.b_const = 1;           // W_unpool
     P.out = out; P.ld_out = d; P.out_fmt = c.out == MOE_F32 ? OUT_F32 : OUT_BF16;
     if (sp.unpool > 1) {
       P.ksplit = sp.unpool; P.split_stride = size_t(T) * d; P.out = part; P.out_fmt = OUT_F32;
