@@ -183,3 +183,75 @@ def test_routing_replay_and_external_routes_at_scale():
     err = rel_err(to_np(a[torch.as_tensor(tok, device="cuda")]), ref)
     print(f"external routes: {len(tok)} sampled tokens, out err {err:.2e}")
     assert err <= TOL
+
+
+def test_boundary_in_the_unpooler_at_scale():
+    """The prefill chunk through moe_forward_boundary, in the bench's configuration (BF16
+    stream and output): the row workers of all 76 CTA pairs claim 8192 two-row items
+    while the unpooler's tiles complete.  The block output equals moe_forward's bit for
+    bit; x' and h' equal moe_forward + moe_boundary's within one BF16 unit on at most 1 %
+    of the elements (h' also carrying any x' difference, scaled by the row's norm factor
+    and gain); 256 sampled rows against the oracle's boundary of the GPU's own y; every
+    32-row block counted its 32 column tiles; repeated calls give the same bits."""
+    need_gpu()
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+    shape = synth.PREFILL_BF16
+    host, dev = fullsize_inputs(shape, 0, EXPERT_SEED)
+    layer = LatentMoE(shape, dev, out="bf16", keep_canonical=False)
+    T, d = shape.T, shape.d
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    g_post = torch.rand(d, generator=gen) + 0.5
+    g_next = torch.rand(d, generator=gen) + 0.5
+    gate = torch.rand(d, generator=gen) * 2.0 - 0.5
+    gp, gn, gt = g_post.cuda(), g_next.cuda(), gate.cuda()
+    x = dev["x"]
+    y1 = layer.forward(x)
+    x1, h1 = layer.boundary(x, y1, gp, gn, gate=gt)
+    y2, x2, h2 = layer.forward_boundary(x, gp, gn, gate=gt)
+    torch.cuda.synchronize()
+    assert layer.read_status() == (0, 0)
+    cnt = layer.intermediate("bnd_cnt", T).cpu().numpy()
+    assert np.all(cnt[:8 * ((T + 255) // 256)] == d // 256)
+    assert torch.equal(y1, y2)
+
+    def unit(v):
+        return torch.exp2(torch.floor(torch.log2(v.abs().clamp_min(1e-30))) - 7)
+
+    # x' = bf16(x + gate * y * rs * g_post): the two paths' FP32 values differ by a few
+    # units of 2^-24 of the terms added (rs from sums in another order), which where the
+    # terms cancel is more than a BF16 unit of the small result
+    a, b = x2.float(), x1.float()
+    yv = y2.float()
+    rs_y = torch.rsqrt((yv * yv).mean(dim=1, keepdim=True) + shape.eps)
+    terms = x.float().abs() + (gt * (yv * rs_y * gp)).abs()
+    u_x = unit(torch.maximum(a.abs(), b.abs()))
+    dx = (a - b).abs()
+    over = dx > u_x * (1 + 1e-6)
+    print(f"x' beyond one unit: {int(over.sum())} elements, worst {float((dx / terms)[over].max()) if bool(over.any()) else 0.0:.2e} of the terms")
+    assert bool((dx <= (u_x + terms * 2.0 ** -20) * (1 + 1e-6)).all())
+    fx = float((dx > 0).float().mean())
+    rs = torch.rsqrt((b * b).mean(dim=1, keepdim=True) + shape.eps)
+    ha, hb = h2.float(), h1.float()
+    tol = unit(torch.maximum(ha.abs(), hb.abs())) + dx * rs * gn
+    assert bool(((ha - hb).abs() <= tol * (1 + 1e-6)).all())
+    fh = float((ha != hb).float().mean())
+    print(f"fused boundary at scale: x' differs from the pass on {fx:.1e}, h' on {fh:.1e}")
+    assert fx <= 0.01 and fh <= 0.01
+
+    rows = np.linspace(0, T - 1, 256).round().astype(int)
+    sel = torch.as_tensor(rows, device="cuda")
+    xr, _ = oracle.boundary(to_np(host["x"])[rows], to_np(y2[sel]), g_post.numpy(),
+                            g_next.numpy(), shape.eps, gate=gate.numpy(), act="bf16")
+    xg = to_np(x2[sel])
+    assert np.all(np.abs(xg - xr) <= (np.exp2(np.floor(np.log2(np.maximum(
+        np.maximum(np.abs(xg), np.abs(xr)), 1e-30))) - 7) + to_np(terms[sel]) * 2.0 ** -20)
+        * (1 + 1e-9))
+    hr = oracle.store(oracle.rmsnorm(xg, g_next.numpy(), shape.eps), "bf16")
+    hg = to_np(h2[sel])
+    assert np.all(np.abs(hg - hr) <= np.exp2(np.floor(np.log2(np.maximum(
+        np.maximum(np.abs(hg), np.abs(hr)), 1e-30))) - 7) * (1 + 1e-9))
+
+    again = layer.forward_boundary(x, gp, gn, gate=gt)
+    torch.cuda.synchronize()
+    for u, v in zip((y2, x2, h2), again):
+        assert torch.equal(u, v)
