@@ -141,7 +141,15 @@ def test_fused_equals_separate_calls():
     assert layer.read_status() == (0, 0)
     assert torch.equal(y1, y2)
     xa, xb = to_np(x2), to_np(x1)
-    assert_one_unit("x_out", xa, xb, "bf16")
+    # where x and gate * a cancel, the few 2^-24 of rounding the two paths' FP32 sums
+    # carry can exceed a BF16 unit of the small result: allow 2^-20 of the terms
+    yv = to_np(y1)
+    rs_y = 1.0 / np.sqrt(np.mean(yv * yv, axis=-1, keepdims=True) + shape.eps)
+    terms = np.abs(to_np(dev["x"])) + np.abs(yv * rs_y * to_np(g_post))
+    d = np.abs(xa - xb)
+    u = unit(np.maximum(np.abs(xa), np.abs(xb)), "bf16")
+    assert np.all(d <= (u + terms * 2.0 ** -20) * (1 + 1e-9)), int(np.sum(d > u))
+    assert float(np.mean(d > 0)) <= 0.01
     ha, hb = to_np(h2), to_np(h1)
     rs = 1.0 / np.sqrt(np.mean(xb * xb, axis=-1, keepdims=True) + shape.eps)
     carried = np.abs(xa - xb) * rs * to_np(g_next)
