@@ -47,11 +47,12 @@ def assert_one_unit(name, gpu, ref, kind):
     return frac
 
 
-def run_fused(T, act, out, gated, inplace, seed, expect_fused, d=8192, p=256):
+def run_fused(T, act, out, gated, inplace, seed, expect_fused, d=8192, p=256, expert=None,
+              replay=False):
     from latent_moe_layer_rmsnorm_gb300 import synth
     from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
     shape = synth.Shape("fused_boundary", T=T, d=d, p=p, E=8, top_k=2, I=256,
-                        act=act, expert=act)
+                        act=act, expert=expert or act)
     inp = synth.make_inputs(shape, seed=seed, device="cpu")
     fix_margins(inp, shape, seed=seed)
     dev = {k: v.cuda() for k, v in inp.items()}
@@ -62,11 +63,14 @@ def run_fused(T, act, out, gated, inplace, seed, expect_fused, d=8192, p=256):
     gate = (torch.rand(d, generator=gen) * 2.0 - 0.5) if gated else None
     x = dev["x"]
     x_before = x.clone()
-    y_ref = layer.forward(x)
+    ids = w = None
+    if replay:                  # routes passed in: the router's own, replayed
+        ids, w = layer.route(x)
+    y_ref = layer.forward(x, ids=ids, w=w)
     torch.cuda.synchronize()
     y, x_out, h_next = layer.forward_boundary(
         x, g_post.cuda(), g_next.cuda(), gate=None if gate is None else gate.cuda(),
-        x_out=x if inplace else None)
+        ids=ids, w=w, x_out=x if inplace else None)
     torch.cuda.synchronize()
     assert layer.read_status() == (0, 0)
     assert torch.equal(y, y_ref)
@@ -107,6 +111,19 @@ def test_fused_boundary_f32_stream():
     """FP32 activations: the unpooler on TF32 CTA pairs, FP32 rows in the row pass."""
     need_gpu()
     run_fused(600, "f32", "f32", True, False, seed=11, expect_fused=True)
+
+
+def test_fused_boundary_nvfp4_experts():
+    """NVFP4 experts: the unpooler, and so the row pass, are those of the BF16 stream."""
+    need_gpu()
+    run_fused(600, "bf16", "bf16", True, False, seed=15, expect_fused=True, expert="nvfp4")
+
+
+def test_fused_boundary_with_replayed_routes():
+    """Routes passed in (routing replay) through the fused call: the same block output as
+    moe_forward with those routes, and the row pass on it."""
+    need_gpu()
+    run_fused(700, "bf16", "f32", False, False, seed=16, expect_fused=True, replay=True)
 
 
 def test_small_batches_run_the_pass():
