@@ -222,3 +222,42 @@ def test_bounded_waits_in_the_fused_kernel():
     assert layer.read_status() == (0, 0)
     for a, b in zip(good, again):
         assert torch.equal(a, b)
+
+
+def test_fused_call_captures_into_a_cuda_graph():
+    """moe_forward_boundary (its counter reset included) captures into a CUDA graph:
+    replays give the eager call's bits, again and again (the counters start from zero on
+    every replay), and follow a new input written into the captured buffer."""
+    need_gpu()
+    from latent_moe_layer_rmsnorm_gb300 import synth
+    from latent_moe_layer_rmsnorm_gb300.layer import LatentMoE
+    shape = synth.Shape("fused_boundary", T=600, d=8192, p=256, E=8, top_k=2, I=256)
+    inp = synth.make_inputs(shape, seed=51, device="cpu")
+    dev = {k: v.cuda() for k, v in inp.items()}
+    layer = LatentMoE(shape, dev, out="bf16")
+    g = (torch.rand(shape.d, generator=torch.Generator().manual_seed(52)) + 0.5).cuda()
+    x = dev["x"].clone()
+    eager = [t.clone() for t in layer.forward_boundary(x, g, g)]
+    flipped = x.flip(0).contiguous()
+    other = [t.clone() for t in layer.forward_boundary(flipped, g, g)]
+    y, xo, hn = (torch.empty_like(t) for t in eager)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # warm the call on the capture stream first
+        layer.forward_boundary(x, g, g, y=y, x_out=xo, h_next=hn)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward_boundary(x, g, g, y=y, x_out=xo, h_next=hn)
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip((y, xo, hn), eager):
+            assert torch.equal(a, b)
+    x.copy_(flipped)
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip((y, xo, hn), other):
+        assert torch.equal(a, b)
+    assert layer.read_status() == (0, 0)
