@@ -80,9 +80,11 @@ typedef enum {
  *   out    MOE_BF16 or MOE_F32: dtype of the layer output
  *   flags  0 or MOE_FLAG_TEST_TIMEOUT, MOE_FLAG_WEIGHT_TILES, one of MOE_FLAG_NVFP4_PAIR
  *          and MOE_FLAG_NVFP4_ONE_CTA (other bits must be zero) */
-/* Test hook for the error path: the gate/up GEMM never issues its first operand load,
- * so its MMA wait runs out after 20 ms; the call's kernels then end early and
- * moe_read_status reports MOE_ERR_TIMEOUT.  Outputs are undefined.  Tests only. */
+/* Test hook for the error path: the gate/up GEMM (and, in moe_forward_boundary, the
+ * unpooler with the boundary's row workers) never issues its first operand load, so its
+ * MMA wait runs out after 20 ms and every wait depending on it after as long; the call's
+ * kernels then end early and moe_read_status reports MOE_ERR_TIMEOUT.  Outputs are
+ * undefined.  Tests only. */
 #define MOE_FLAG_TEST_TIMEOUT 0x80000000u
 /* Run the BF16 / FP32 expert GEMMs with weight rows on the MMA's M side and each
  * expert's tokens on N (tiles shrink to the tokens present, in steps of 16) instead of
