@@ -136,6 +136,13 @@ def test_small_batches_run_the_pass():
     run_fused(64, "bf16", "bf16", False, False, seed=14, expect_fused=True)
 
 
+def test_widths_off_the_pair_tiles_run_the_pass():
+    """d not a multiple of 256 (d = 1152: 128-column unpooler tiles on single CTAs): the
+    boundary runs as its own pass after the block, with the same results."""
+    need_gpu()
+    run_fused(600, "bf16", "bf16", True, True, seed=17, expect_fused=False, d=1152)
+
+
 def test_fused_equals_separate_calls():
     """moe_forward + moe_boundary and moe_forward_boundary agree: y bit for bit; x' equal
     or one BF16 unit apart (the two sum the row's squares in different orders) on at most
