@@ -329,14 +329,19 @@ int moe_forward_launches(const moe_config_t* cfg, int route_internally);
  * inspect after a call (the buffers stay valid until the next call on the workspace):
  *   0 h32 [T,d] FP32 (TF32-rounded)   1 h16 [T,d] FP16     2 ids [T,k] int32
  *   3 w [T,k] FP32                    4 pooled [T,p] FP32   5 row_off [E+1] int32
- *   6 src [T*k] int32 (dispatched row -> t*k+j)              7 inv [T*k] int32
- *   8 A_perm [T*k,p] (FP16 / FP32)   9 s [T*k,I] (FP16 / FP32)
- *  10 y [T*k,p] (FP16 / FP32: FP32 for FP32 experts only)
+ * Dispatched rows: row_off[e] is expert e's first row, row_cnt[e] its rows.  NVFP4
+ * experts, and BF16 / FP32 experts when T*k >= 256*E, start every expert on a 128-row
+ * boundary (R = 128 * (ceil(T*k/128) + E) rows in all), the rows after an expert's last
+ * one being padding (zeros in A_perm and s for BF16 / FP32 experts); otherwise the rows
+ * are packed (T*k of them).
+ *   6 src [R] int32 (dispatched row -> t*k+j; padding rows hold no entry)
+ *   7 inv [T*k] int32 (t*k+j -> dispatched row)
+ *   8 A_perm [R,p] (FP16 / FP32)   9 s [R,I] (FP16 / FP32)
+ *  10 y [R,p] (FP16 / FP32: FP32 for FP32 experts only)
  *  11 c [T,p] (FP16 / FP32)
- * NVFP4 configs: dispatched rows start at a 128-row boundary per expert (R rows in all,
- * R = 128 * (ceil(T*k/128) + E)); 8 A_perm [R, p/2] E2M1 codes, 9 s [R, I/2] codes,
- * 10 y [R, p] FP16, 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R]
- * FP32 per-row scales.  All configs: 15 row_cnt [E+1] int32 rows per expert;
+ * NVFP4 configs: 8 A_perm [R, p/2] E2M1 codes, 9 s [R, I/2] codes, 10 y [R, p] FP16,
+ * 12 sf_u, 13 sf_s chunked UE4M3 scales of A_perm / s, 14 alpha [R] FP32 per-row scales.
+ * All configs: 15 row_cnt [E+1] int32 rows per expert;
  * moe_forward_boundary: 16 [T, d/128] FP32 sums of squares of the block output per 128
  * columns, 17 [8 * ceil(T/256) + 1] int32 column tiles stored per 32-row block, then the
  * row workers' item counter (all zero when the boundary ran as a separate pass).

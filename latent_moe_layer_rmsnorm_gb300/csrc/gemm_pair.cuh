@@ -152,7 +152,7 @@ __device__ __forceinline__ TileCoord pair_tile(const GemmParams& P, const PairSm
   const int half = small ? 64 : 128;
   c.a_row = __ldg(P.row_off + e) + pr * 256 + half * static_cast<int>(rank);
   c.b_row = e * P.N + c.n_blk * P.bn + 128 * static_cast<int>(rank);
-  c.valid = min(half, left - half * static_cast<int>(rank));
+  c.valid = P.pad_rows ? half : min(half, left - half * static_cast<int>(rank));
   c.e = e;
   return c;
 }

@@ -99,6 +99,8 @@ struct GemmParams {
   BoundaryArgs bnd;   // EPI_BOUNDARY only (its row_ssq: [M, N / 128] of the output)
   int b_const;   // dense: B is a weight, written before the forward began, so the first
                  // ring stages' B tiles are requested before the wait on the previous kernel
+  int pad_rows;  // grouped on CTA pairs: the rows of a tile past the expert's last row lie
+                 // in its zeroed padding; store them too (the zeros they compute to)
 };
 
 struct GemmSmem {

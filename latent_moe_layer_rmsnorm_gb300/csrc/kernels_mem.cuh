@@ -320,12 +320,28 @@ template <bool OUT_F32>
 __global__ void __launch_bounds__(MEM_THREADS)
     pool_permute_kernel(const float* __restrict__ pooled, const float* __restrict__ g,
                         const int* __restrict__ inv, void* __restrict__ a_perm, int p, int k,
-                        float eps, int* status) {
+                        float eps, int* status, const int* __restrict__ row_off,
+                        const int* __restrict__ row_cnt, int zero_blocks) {
   pdl_wait();
   pdl_allow_next();
+  if (blockIdx.x < static_cast<unsigned>(zero_blocks)) {
+    // blocks 4e .. 4e+3: a quarter each of expert e's padding rows (its rows start on
+    // 128-row boundaries), written as zeros, so the grouped GEMMs' tiles that run past the
+    // expert's last row multiply zeros: the same results, and far less switching power in
+    // the tensor cores, which under the power cap buys clock
+    const int e = static_cast<int>(blockIdx.x) >> 2, part = static_cast<int>(blockIdx.x) & 3;
+    const size_t es = OUT_F32 ? 4 : 2;
+    const size_t r0 = static_cast<size_t>(row_off[e]) + row_cnt[e];
+    const size_t n16 = (static_cast<size_t>(row_off[e + 1]) - r0) * p * es / 16;
+    const size_t q = (n16 + 3) / 4;
+    const size_t i0 = part * q, i1 = n16 < i0 + q ? n16 : i0 + q;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a_perm) + r0 * p * es);
+    for (size_t i = i0 + threadIdx.x; i < i1; i += blockDim.x) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   __shared__ float red[32];
   __shared__ int rows[MAX_TOPK];
-  const size_t t = blockIdx.x;
+  const size_t t = blockIdx.x - zero_blocks;
   if (threadIdx.x < k) rows[threadIdx.x] = inv[t * k + threadIdx.x];
   const int nchunk = p >> 3;
   constexpr int CPT = 4;  // chunks of 8 per thread: p <= 8192

@@ -276,7 +276,7 @@ WsLayout ws_layout(const moe_config_t& c) {
   const size_t ee = c.expert == MOE_F32 ? 4 : 2;
   const bool q = c.expert == MOE_NVFP4;
   L.nchunks = static_cast<int>((T * k + DISPATCH_CHUNK - 1) / DISPATCH_CHUNK);
-  L.rows = q ? 128 * ((T * k + 127) / 128 + E) : T * k;
+  L.rows = 128 * ((T * k + 127) / 128 + E);   // every expert's rows start on a 128-row boundary
   const size_t R = L.rows;
   L.status = take(256);
   L.h32 = take(T * d * 4);
@@ -579,6 +579,14 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
 
   // ---- stage: dispatch (counting sort) + pooled RMSNorm + permute ---------------------
   const bool nvf4 = c.expert == MOE_NVFP4;
+  // Zero padding rows pay where the expert GEMMs run into the power cap: batches whose
+  // experts average a full 256-row pair tile (prefill: +3 % SM clock, both GEMMs 3 %
+  // faster).  At decode sizes almost every tile row is padding: zeroing it (and storing
+  // it again as s) costs more than it saves, and even unzeroed, 128-row aligned experts
+  // make each tile read rows of its own instead of its neighbours' rows already in L2.
+  // NVFP4 experts keep the aligned layout always (their scale chunks need it).
+  const bool zero_pad = !nvf4 && static_cast<int64_t>(T) * k >= int64_t(256) * E_;
+  const int padded = (nvf4 || zero_pad) ? 1 : 0;
   int* chunk = reinterpret_cast<int*>(base + L.chunk);
   int* row_off = reinterpret_cast<int*>(base + L.row_off);
   int* mt_off = reinterpret_cast<int*>(base + L.mt_off);
@@ -593,29 +601,34 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
   if (L.nchunks == 1) {     // small batches (decode): the three steps in one block
     MOE_TRY(launch_step(dispatch_small_kernel, dim3(1), dim3(256), 0, st,
                         static_cast<const int32_t*>(ids), rows, E_, row_off, mt_off, mt2_off,
-                        row_cnt, inv, src, nvf4 ? 1 : 0, status));
+                        row_cnt, inv, src, padded, status));
   } else {
     MOE_TRY(launch_step(dispatch_hist_kernel, dim3(L.nchunks), dim3(MEM_THREADS), 0, st,
                         static_cast<const int32_t*>(ids), rows, E_, chunk, status));
     MOE_TRY(launch_step(dispatch_scan_kernel, dim3(1), dim3(256), 0, st, chunk, L.nchunks, E_,
-                        row_off, mt_off, mt2_off, row_cnt, nvf4 ? 1 : 0));
+                        row_off, mt_off, mt2_off, row_cnt, padded));
     MOE_TRY(launch_step(dispatch_scatter_kernel, dim3(L.nchunks), dim3(32), 0, st,
                         static_cast<const int32_t*>(ids), rows, E_,
                         static_cast<const int*>(chunk), inv, src));
   }
+  const int zero_blocks = zero_pad ? 4 * E_ : 0;
   if (nvf4)
     MOE_TRY(launch_step(pool_quant_kernel, dim3(T), dim3(MEM_THREADS), 0, st,
                         static_cast<const float*>(pooled), W->g_pool,
                         static_cast<const int*>(inv), static_cast<uint8_t*>(a_perm), sf_u, alpha,
                         p, k, c.eps, status));
   else if (exp_f32)
-    MOE_TRY(launch_step(pool_permute_kernel<true>, dim3(T), dim3(MEM_THREADS), 0, st,
-                        static_cast<const float*>(pooled), W->g_pool,
-                        static_cast<const int*>(inv), a_perm, p, k, c.eps, status));
+    MOE_TRY(launch_step(pool_permute_kernel<true>, dim3(T + zero_blocks), dim3(MEM_THREADS), 0,
+                        st, static_cast<const float*>(pooled), W->g_pool,
+                        static_cast<const int*>(inv), a_perm, p, k, c.eps, status,
+                        static_cast<const int*>(row_off), static_cast<const int*>(row_cnt),
+                        zero_blocks));
   else
-    MOE_TRY(launch_step(pool_permute_kernel<false>, dim3(T), dim3(MEM_THREADS), 0, st,
-                        static_cast<const float*>(pooled), W->g_pool,
-                        static_cast<const int*>(inv), a_perm, p, k, c.eps, status));
+    MOE_TRY(launch_step(pool_permute_kernel<false>, dim3(T + zero_blocks), dim3(MEM_THREADS), 0,
+                        st, static_cast<const float*>(pooled), W->g_pool,
+                        static_cast<const int*>(inv), a_perm, p, k, c.eps, status,
+                        static_cast<const int*>(row_off), static_cast<const int*>(row_cnt),
+                        zero_blocks));
   E.mark(4);
 
   // ---- stage: grouped gate/up GEMM + SwiGLU -------------------------------------------
@@ -650,7 +663,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     // weights on the MMA's M side (256-row W13 blocks: 128 gate + 128 up), tokens on N
     CUtensorMap tw, tx;
     if (!make_tmap(&tw, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, 256) ||
-        !make_tmap(&tx, a_perm, k_up, p, rows, 128))
+        !make_tmap(&tx, a_perm, k_up, p, R, 128))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = 2 * I; P.K = p; P.bn = 256; P.groups = E_;
@@ -668,8 +681,8 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     // CTA pairs over 256-row tiles of each expert (M = 128 pair tiles for remainders);
     // each CTA of a pair loads half of a 256-row W13 block: 128 gate or 128 up rows
     CUtensorMap ta, ta64, tb, tb64;
-    if (!make_tmap(&ta, a_perm, k_up, p, rows, GEMM_BM) ||
-        !make_tmap(&ta64, a_perm, k_up, p, rows, GEMM_BM / 2) ||
+    if (!make_tmap(&ta, a_perm, k_up, p, R, GEMM_BM) ||
+        !make_tmap(&ta64, a_perm, k_up, p, R, GEMM_BM / 2) ||
         !make_tmap(&tb, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, W13_GROUP) ||
         !make_tmap(&tb64, W->w13, k_up, p, static_cast<uint64_t>(E_) * 2 * I, W13_GROUP / 2))
       return MOE_ERR_CUDA;
@@ -677,9 +690,12 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.N = 2 * I; P.K = p; P.bn = 2 * W13_GROUP; P.groups = E_;
     P.row_off = row_off; P.mt_off = mt2_off; P.row_cnt = row_cnt;
     P.out = s_buf; P.ld_out = I; P.out_fmt = exp_f32 ? OUT_TF32 : OUT_F16;
+    // the tiles cover each expert's rows up to its 128-row boundary; with zeroed padding
+    // rows of A, storing their s (exact zeros) keeps the down GEMM's padding zero too
+    P.pad_rows = zero_pad ? 1 : 0;
     P.debug_skip_first_load = (c.flags & MOE_FLAG_TEST_TIMEOUT) ? 1 : 0;
     CUtensorMap to;
-    if (!make_tmap(&to, s_buf, exp_f32 ? OP_TF32 : OP_F16, I, rows, 32)) return MOE_ERR_CUDA;
+    if (!make_tmap(&to, s_buf, exp_f32 ? OP_TF32 : OP_F16, I, R, 32)) return MOE_ERR_CUDA;
     const int tiles = (rows / 256 + E_) * (2 * I / P.bn);
     if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_SWIGLU>(ta, ta64, tb, tb64, to, P, tiles, sms, st)));
     else MOE_TRY((launch_pair<OP_F16, EPI_SWIGLU>(ta, ta64, tb, tb64, to, P, tiles, sms, st)));
@@ -732,7 +748,7 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     // weights on M (128 rows of p), up to 256 tokens on N
     CUtensorMap tw, tx;
     if (!make_tmap(&tw, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128) ||
-        !make_tmap(&tx, s_buf, k_down, I, rows, 256))
+        !make_tmap(&tx, s_buf, k_down, I, R, 256))
       return MOE_ERR_CUDA;
     GemmParams P = base_params(status, c.flags);
     P.N = p; P.K = I; P.bn = 128; P.groups = E_;
@@ -746,14 +762,14 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     else
       MOE_TRY(launch_step(gemm_swap_kernel<OP_F16, SWAP_STORE>, dim3(grid), dim3(GEMM_THREADS),
                           swap_smem_bytes(), st, tw, tx, P));
-    const size_t n = rows * static_cast<size_t>(p / 128);
+    const size_t n = static_cast<size_t>(R) * (p / 128);
     const int ssq_grid = static_cast<int>(std::min<size_t>((n + MEM_THREADS - 1) / MEM_THREADS, 4096));
     if (y_f16)
       MOE_TRY(launch_step(row_ssq_kernel<true>, dim3(ssq_grid), dim3(MEM_THREADS), 0, st,
-                          static_cast<const void*>(y_buf), rows, p, ssq));
+                          static_cast<const void*>(y_buf), R, p, ssq));
     else
       MOE_TRY(launch_step(row_ssq_kernel<false>, dim3(ssq_grid), dim3(MEM_THREADS), 0, st,
-                          static_cast<const void*>(y_buf), rows, p, ssq));
+                          static_cast<const void*>(y_buf), R, p, ssq));
   } else {
     CUtensorMap ta, tb;
     const int bn = bn_for(p);
@@ -763,17 +779,17 @@ moe_status_t run_layer(const moe_config_t* cfg, const moe_weights_t* W, const vo
     P.out = y_buf; P.ld_out = p; P.out_fmt = y_fmt; P.row_ssq = ssq;
     if (bn == 256) {    // CTA pairs over 256-row tiles (M = 128 pair tiles for remainders)
       CUtensorMap ta64, to;
-      if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
-          !make_tmap(&ta64, s_buf, k_down, I, rows, GEMM_BM / 2) ||
+      if (!make_tmap(&ta, s_buf, k_down, I, R, GEMM_BM) ||
+          !make_tmap(&ta64, s_buf, k_down, I, R, GEMM_BM / 2) ||
           !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, 128) ||
-          !make_tmap(&to, y_buf, y_op, p, rows, 32))
+          !make_tmap(&to, y_buf, y_op, p, R, 32))
         return MOE_ERR_CUDA;
       P.mt_off = mt2_off;
       const int tiles = (rows / 256 + E_) * (p / 256);
       if (exp_f32) MOE_TRY((launch_pair<OP_TF32, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
       else MOE_TRY((launch_pair<OP_F16, EPI_STORE>(ta, ta64, tb, tb, to, P, tiles, sms, st)));
     } else {
-      if (!make_tmap(&ta, s_buf, k_down, I, rows, GEMM_BM) ||
+      if (!make_tmap(&ta, s_buf, k_down, I, R, GEMM_BM) ||
           !make_tmap(&tb, W->w2, k_down, I, static_cast<uint64_t>(E_) * p, bn))
         return MOE_ERR_CUDA;
       P.mt_off = mt_off;

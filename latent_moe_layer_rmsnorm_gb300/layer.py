@@ -197,16 +197,16 @@ class LatentMoE:
         sh, k = self.shape, self.shape.top_k
         f32 = sh.act == "f32"
         op = torch.float32 if f32 else torch.float16
+        R = 128 * ((T * k + 127) // 128 + sh.E)    # every expert's rows start on a 128-row boundary
         if sh.expert == "nvfp4":
-            R = 128 * ((T * k + 127) // 128 + sh.E)
             rows = {"src": ((R,), torch.int32), "a_perm": ((R, sh.p // 2), torch.uint8),
                     "s": ((R, sh.I // 2), torch.uint8), "y": ((R, sh.p), torch.float16),
                     "sf_u": ((R * sh.p // 16,), torch.uint8),
                     "sf_s": ((R * sh.I // 16,), torch.uint8), "alpha": ((R,), torch.float32)}
         else:
-            rows = {"src": ((T * k,), torch.int32), "a_perm": ((T * k, sh.p), op),
-                    "s": ((T * k, sh.I), torch.float32 if f32 else torch.float16),
-                    "y": ((T * k, sh.p),
+            rows = {"src": ((R,), torch.int32), "a_perm": ((R, sh.p), op),
+                    "s": ((R, sh.I), torch.float32 if f32 else torch.float16),
+                    "y": ((R, sh.p),
                           torch.float32 if sh.expert == "f32" else torch.float16)}
         spec = {"h32": ((T, sh.d), torch.float32), "h16": ((T, sh.d), torch.float16),
                 "ids": ((T, k), torch.int32), "w": ((T, k), torch.float32),

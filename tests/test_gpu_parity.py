@@ -48,9 +48,13 @@ MAX_FLIP_FRACTION = 0.01
 
 TINY_BF16 = synth.TINY_F32.replace(name="tiny_bf16", act="bf16", expert="bf16")
 NARROW_BF16 = synth.Shape("narrow_bf16", T=300, d=512, p=256, E=16, top_k=4, I=384)
+# experts averaging a full 256-row pair tile (T k >= 256 E): zeroed padding rows
+PADDED_BF16 = synth.Shape("padded_bf16", T=700, d=512, p=256, E=4, top_k=2, I=256)
+PADDED_F32 = synth.Shape("padded_f32", T=600, d=512, p=256, E=4, top_k=2, I=256,
+                         act="f32", expert="f32")
 MID_BF16 = synth.Shape("mid_bf16", T=300, d=1024, p=1024, E=16, top_k=4, I=512)
 SHAPES = {"tiny_f32": synth.TINY_F32, "tiny_bf16": TINY_BF16, "narrow_bf16": NARROW_BF16,
-          "mid_bf16": MID_BF16}
+          "mid_bf16": MID_BF16, "padded_bf16": PADDED_BF16, "padded_f32": PADDED_F32}
 
 
 def need_gpu():
@@ -124,23 +128,48 @@ def assert_sum_close(name, gpu, ref):
     return e
 
 
-def check_dispatch(layer, T, ids):
-    """Counting-sort invariants: offsets are the exclusive scan of the expert counts,
-    src is a permutation, each expert's rows are in (token, slot) order, inv inverts src."""
-    k = layer.shape.top_k
+def dispatched_rows(layer, T):
+    """(row_off, row_cnt, positions of the routed rows).  In prefill-sized batches every
+    expert's rows start on a 128-row boundary, and the rows between an expert's last
+    routed row and the next expert's first are padding; smaller batches pack the rows."""
     E = layer.shape.E
     row_off = to_np(layer.intermediate("row_off", T)).astype(np.int64)
+    row_cnt = layer.intermediate("row_cnt", T).cpu().numpy().astype(np.int64)
+    pos = np.concatenate([np.arange(row_off[e], row_off[e] + row_cnt[e]) for e in range(E)])
+    return row_off, row_cnt, pos
+
+
+def zero_padded(layer, T):
+    """Batches whose experts average a full 256-row pair tile get zeroed padding rows."""
+    sh = layer.shape
+    return sh.expert != "nvfp4" and T * sh.top_k >= 256 * sh.E
+
+
+def check_dispatch(layer, T, ids):
+    """Counting-sort invariants: expert offsets are the exclusive scan of the counts
+    (prefill-sized batches: rounded up to 128 rows), the routed rows hold every (token,
+    slot) pair once, each expert's rows in (token, slot) order, inv inverts src on them,
+    and the padding rows of the gate/up operand are zeros."""
+    k = layer.shape.top_k
+    E = layer.shape.E
+    row_off, row_cnt, pos = dispatched_rows(layer, T)
     src = layer.intermediate("src", T).cpu().numpy().astype(np.int64)
     inv = layer.intermediate("inv", T).cpu().numpy().astype(np.int64)
     flat = ids.reshape(-1)
     counts = np.bincount(flat, minlength=E)
-    np.testing.assert_array_equal(row_off, np.concatenate([[0], np.cumsum(counts)]))
-    assert sorted(src.tolist()) == list(range(T * k))
-    np.testing.assert_array_equal(inv[src], np.arange(T * k))
+    np.testing.assert_array_equal(row_cnt[:E], counts)
+    span = (counts + 127) // 128 * 128 if zero_padded(layer, T) else counts
+    np.testing.assert_array_equal(row_off, np.concatenate([[0], np.cumsum(span)]))
+    assert sorted(src[pos].tolist()) == list(range(T * k))
+    np.testing.assert_array_equal(inv[src[pos]], pos)
     for e in range(E):
-        seg = src[row_off[e]: row_off[e + 1]]
+        seg = src[row_off[e]: row_off[e] + counts[e]]
         assert np.all(np.diff(seg) > 0)
         assert np.all(flat[seg] == e)
+    pad = np.setdiff1d(np.arange(row_off[E]), pos)
+    if len(pad) and zero_padded(layer, T):
+        u = layer.intermediate("a_perm", T)
+        assert int(torch.count_nonzero(u[torch.as_tensor(pad, device=u.device)])) == 0
     return src
 
 
@@ -152,13 +181,15 @@ def check_stagewise(layer, view, shape, T, ids, w, out):
 
     def wconv(a, kind):
         return oracle.store(np.asarray(a, np.float64), kind)
-    src = layer.intermediate("src", T).cpu().numpy().astype(np.int64)
+    _, _, pos = dispatched_rows(layer, T)      # routed rows (the rest is padding)
+    src = layer.intermediate("src", T).cpu().numpy().astype(np.int64)[pos]
     inv = layer.intermediate("inv", T).cpu().numpy().astype(np.int64).reshape(T, k)
     h_in = to_np(layer.intermediate("h32" if f32 else "h16", T))
     pooled = to_np(layer.intermediate("pooled", T))
-    u = to_np(layer.intermediate("a_perm", T))
-    s = to_np(layer.intermediate("s", T))
-    y = to_np(layer.intermediate("y", T))
+    u = to_np(layer.intermediate("a_perm", T))[pos]
+    s = to_np(layer.intermediate("s", T))[pos]
+    y_all = to_np(layer.intermediate("y", T))
+    y = y_all[pos]
     c = to_np(layer.intermediate("c", T))
     rep = {}
     rep["pooled"] = assert_sum_close(
@@ -182,7 +213,7 @@ def check_stagewise(layer, view, shape, T, ids, w, out):
         rep["y"] = assert_sum_close("y", y, y_ref)
     else:                                                  # one BF16 rounding of the sum
         rep["y"] = assert_one_unit("y", y, y_ref, st["y"], K=shape.I)
-    y_slots = y[inv].astype(np.float64)                    # [T, k, p]
+    y_slots = y_all[inv].astype(np.float64)                # [T, k, p]
     c_ref = oracle.store(oracle.combine(y_slots, ids, np.asarray(w, np.float64), view["g_exp"],
                                         shape.eps), st["c"])
     rep["c"] = assert_one_unit("c", c, c_ref, st["c"], K=shape.p)
@@ -210,6 +241,14 @@ def test_layer_matches_oracle(name):
     np.testing.assert_allclose(w, ref["w"], rtol=0, atol=TOL_W)
     np.testing.assert_allclose(w.sum(1), 1.0, rtol=0, atol=1e-6)
     check_dispatch(layer, T, ids)
+    if zero_padded(layer, T):
+        # the gate/up tiles store their padding rows, which compute to exact zeros, so the
+        # down GEMM's padding rows are zeros as well
+        row_off, _, pos = dispatched_rows(layer, T)
+        pad = np.setdiff1d(np.arange(row_off[shape.E]), pos)
+        assert len(pad)
+        s_all = layer.intermediate("s", T)
+        assert int(torch.count_nonzero(s_all[torch.as_tensor(pad, device=s_all.device)])) == 0
     stages = check_stagewise(layer, view, shape, T, ids, w, out)
     e2e = rel_err(to_np(out), ref["out"])
     print(name, "stage-wise", {k_: f"{v:.1e}" for k_, v in stages.items()}, f"e2e {e2e:.2e}")
