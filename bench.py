@@ -606,16 +606,25 @@ def run_ours(args):
         def block_fused():
             layer.forward_boundary(x, g_post, g_next, y=yb, x_out=xo, h_next=hn)
 
-        for name, fn in (("block_then_pass_ms", block_then_pass), ("fused_ms", block_fused)):
+        # interleaved repetitions, so that drift of the clock under the power cap falls on
+        # both arms alike
+        arms = (("block_then_pass_ms", block_then_pass), ("fused_ms", block_fused))
+        for _, fn in arms:
             for _ in range(3):
                 fn()
-            torch.cuda.synchronize()
-            b0.record(stream)
-            for _ in range(args.steps):
-                fn()
-            b1.record(stream)
-            torch.cuda.synchronize()
-            boundary[name] = round(max_over_ranks(b0.elapsed_time(b1), "cuda") / args.steps, 4)
+        torch.cuda.synchronize()
+        reps, per = 4, max(1, args.steps // 4)
+        acc = {name: 0.0 for name, _ in arms}
+        for _ in range(reps):
+            for name, fn in arms:
+                b0.record(stream)
+                for _ in range(per):
+                    fn()
+                b1.record(stream)
+                torch.cuda.synchronize()
+                acc[name] += max_over_ranks(b0.elapsed_time(b1), "cuda")
+        for name, _ in arms:
+            boundary[name] = round(acc[name] / (reps * per), 4)
         boundary["fused_saves_ms"] = round(boundary["block_then_pass_ms"] - boundary["fused_ms"], 4)
         del xo, hn, yb
 
